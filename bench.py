@@ -1,0 +1,387 @@
+"""Benchmark of the quantized sparse MoE FFN layer (one JSON line on rank 0).
+
+Default workload: decode, T=1 token through 40 independent Qwen3.6-35B-A3B
+shaped MoE layers (H=2048, 256 experts, top-8 + shared expert, I=512, Q8_0
+weights, 34.4 GB resident).  One step = one pass of the whole hot path
+(route -> group -> FFN with SwiGLU and combine) over the 40 layers, in
+sequence, captured in a CUDA graph.  Metric: MoE-layer tokens/s = T * 40 /
+step time.  Inputs are synthetic, seeded, drawn on the device before the
+timed region; the 1.3 GB of expert weights a step touches is ~10x the L2,
+so no flush is needed.
+
+Other workloads (--workload): prefill (T=4096, Zipf-skewed routing, one
+layer), batched16 / batched64 / batched1 (affine 4-bit, 40 layers), gemv
+(Llama-3.2-1B Q8_0 projections).
+
+--impl reference times the fp64 CPU oracle on the host cores, on a bounded
+sample of the same workload, and reports it in the same metric.
+Multi-GPU (torchrun): replicas only, each rank runs its own copy; the time is
+the max over ranks and value = all ranks' tokens / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+Q8_EXPERT_BYTES = {  # per expert, H=2048, I=512
+    synth.Q8_0: (2 * 512 * 2048 + 2 * 512 * 64 * 2, 2048 * 512 + 2048 * 16 * 2),
+    synth.AFFINE4_G64: (1024 * 1024 + 1024 * 32 * 4, 2048 * 256 + 2048 * 8 * 4),
+}
+ROUTER_BYTES = 256 * 2048 * 4
+
+WORKLOADS = {
+    "decode": dict(shape=synth.QWEN, T=1, layers=40, zipf=None,
+                   desc="decode T=1, 40 layers, H=2048, E=256, top-8 + shared, "
+                        "I=512, Q8_0"),
+    "batched1": dict(shape=synth.QWEN_A4, T=1, layers=40, zipf=None,
+                     desc="batched decode T=1, 40 layers, affine-4 g64"),
+    "batched16": dict(shape=synth.QWEN_A4, T=16, layers=40, zipf=None,
+                      desc="batched decode T=16, 40 layers, affine-4 g64"),
+    "batched64": dict(shape=synth.QWEN_A4, T=64, layers=40, zipf=None,
+                      desc="batched decode T=64, 40 layers, affine-4 g64"),
+    "prefill": dict(shape=synth.QWEN, T=4096, layers=1, zipf="noise",
+                    desc="prefill T=4096, 1 layer, Zipf-offset routing, Q8_0"),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- ours
+
+def build_layers(qsm, wl, device, seed):
+    shape = wl["shape"]
+    layers, xs, fwds, syn = [], [], [], []
+    for l in range(wl["layers"]):
+        Lg = synth.draw_layer(shape, device, seed=seed, layer=l, zipf=wl["zipf"])
+        syn.append(Lg)
+        L = qsm.Layer.from_synth(Lg)
+        layers.append(L)
+        xs.append(synth.draw_x(wl["T"], shape.H, device, seed, l))
+        fwds.append(qsm.MoEForward(L, wl["T"], device))
+    return layers, xs, fwds, syn
+
+
+def touched_bytes(layers, fwds, qtype):
+    """Distinct touched experts (from the device routing) + shared +
+    router + x + y, per step."""
+    gu, dn = Q8_EXPERT_BYTES[qtype]
+    total = 0
+    n_exp = 0
+    for L, f in zip(layers, fwds):
+        ne = int((f.grouping.counts > 0).sum().item())
+        n_exp += ne
+        T = f.T
+        total += (ne + 1) * (gu + dn) + ROUTER_BYTES + 2 * T * L.H * 2
+    return total, n_exp
+
+
+def run_ours(args, wl, rank, world):
+    import quantized_sparse_moe_gb300 as qsm
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    layers, xs, fwds, syn = build_layers(qsm, wl, dev, seed=0)
+    T, nL = wl["T"], wl["layers"]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s):
+        for f, x in zip(fwds, xs):
+            f(x, stream=s)
+
+    # warm-up (also builds the library and fixes the routing)
+    with torch.cuda.stream(stream):
+        step(stream)
+    torch.cuda.synchronize()
+    for f in fwds:
+        assert f.dev_status.item() == 0, "device status set"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks, torch.cuda.stream(stream):
+        time.sleep(0.25)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    value = world * T * nL / (ms / 1e3)
+
+    # dominant launch pair: the expert FFN (gate_up+SwiGLU, down+combine),
+    # timed per layer with events on its stream, outside the graph
+    ffn_ms = []
+    for rep in range(3):
+        evs = [(torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
+        for (a, b), f, x, L in zip(evs, fwds, xs, layers):
+            qsm.moe_route(x, L.w_router, L.k, L.logit_bias, True, f.topk_idx,
+                          f.topk_w, f.route_ws, f.dev_status, stream)
+            qsm.moe_group_tokens(f.topk_idx, L.E, f.grouping.tile_rows,
+                                 f.grouping, f.dev_status, stream)
+            a.record(stream)
+            qsm.moe_ffn_forward(L, x, f.topk_idx, f.topk_w, f.grouping, f.y,
+                                False, f.ffn_ws, f.dev_status, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        ffn_ms.append(sum(a.elapsed_time(b) for a, b in evs) / nL)
+    ffn_ms = min(ffn_ms)
+    qtype = wl["shape"].qtype
+    step_bytes, n_exp = touched_bytes(layers, fwds, qtype)
+    gu, dn = Q8_EXPERT_BYTES[qtype]
+    ffn_bytes_per_layer = (n_exp / nL + 1) * (gu + dn) + 2 * T * 2048 * 2
+    hbm, _, peak_kind = peaks()
+
+    # end to end through the public API: pinned host x in, host y out
+    xh = torch.stack(xs).cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(xs[0]).new_empty((nL,) + tuple(xs[0].shape))
+    e_ms = []
+    for rep in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            xd.copy_(xh, non_blocking=True)
+            for l, f in enumerate(fwds):
+                f(xd[l], stream=stream)
+                yh[l].copy_(f.y, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        if rep >= args.warmup:
+            e_ms.append((t1 - t0) * 1e3)
+    e2e_ms = statistics.median(e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = t.item()
+
+    achieved = ffn_bytes_per_layer / (ffn_ms / 1e3) / 1e9
+    result = {
+        "metric": "MoE-layer tokens/s",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "q8_0/affine4 weights, f16 MMA inputs, f32 accumulate",
+        "data": "synthetic (seeded; random-init weights of the layer shapes)",
+        "config": {"workload": wl["desc"], "tokens_per_layer": T,
+                   "layers": nL, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (touched weights per step "
+                         f"{step_bytes / 1e9:.2f} GB)"},
+        "layer_roofline": {
+            "bound": "hbm", "touched_bytes_per_step": step_bytes,
+            "floor_ms": step_bytes / (hbm * 1e9) * 1e3,
+            "frac": step_bytes / (hbm * 1e9) / (ms / 1e3),
+            "peak_gbs": hbm, "peak_kind": peak_kind},
+        "roofline": {
+            "kernel": "moe_ffn_forward (d1 gate_up+SwiGLU, d2 down+combine)",
+            "bound": "hbm", "achieved": achieved, "peak": hbm,
+            "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+            "bytes_per_launch": ffn_bytes_per_layer,
+            "launch_ms": ffn_ms, "peak_kind": peak_kind},
+        "e2e": {"value": world * T * nL / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": xh.numel() * 2,
+                "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * nL * 4,
+        "clocks": clocks.summary(),
+    }
+    return result, (syn, fwds, xs)
+
+
+# ----------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, layers_dev, xs_dev, budget_s=12.0, reps_max=1000):
+    """The fp64 oracle on the host cores over a bounded sample of the
+    workload's layers; returns (tokens/s, description, cores)."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _helpers import bits16, oracle_q
+    T = wl["T"]
+    done_tokens, t_used, n_layers = 0, 0.0, 0
+    for Lg, x in zip(layers_dev, xs_dev):
+        q = [oracle_q(t) for t in (Lg.gate_up, Lg.down, Lg.shared_gate_up,
+                                   Lg.shared_down)]
+        xb = bits16(x)
+        wr = Lg.w_router.cpu().numpy()
+        bias = None if Lg.logit_bias is None else Lg.logit_bias.cpu().numpy()
+        toks = np.arange(T, dtype=np.int32)
+        if T > 64:  # prefill: a token sample of the full routing
+            toks = np.random.default_rng(0).choice(T, 64, replace=False).astype(np.int32)
+        t0 = time.perf_counter()
+        idx, w = oracle.route(xb, wr, Lg.shape.k, bias)
+        oracle.group(idx, Lg.shape.E, 8)
+        oracle.moe_layer(xb, idx, w, *q, tokens=toks)
+        t_used += time.perf_counter() - t0
+        done_tokens += len(toks)
+        n_layers += 1
+        del q
+        if t_used > budget_s:
+            break
+    return done_tokens / t_used, n_layers, oracle.max_threads(), t_used
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return None
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    vals = []
+    n_l = 0
+    # each step: a bounded sample (the first layers of the workload)
+    for s in range(args.warmup + args.steps):
+        Ls = [synth.draw_layer(wl["shape"], dev, seed=0, layer=l, zipf=wl["zipf"])
+              for l in range(min(wl["layers"], 2))]
+        xs = [synth.draw_x(wl["T"], wl["shape"].H, dev, 0, l) for l in range(len(Ls))]
+        v, n_l, cores, t = oracle_sample(wl, Ls, xs, budget_s=6.0)
+        if s >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    return {
+        "impl": "reference", "metric": "MoE-layer tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl["desc"], "tokens_per_layer": wl["T"],
+                   "layers": wl["layers"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{n_l} layer(s) per step of the workload "
+                                   "(route, group, expert FFNs, combine; fp64)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        res = run_reference(args, wl, rank, world)
+    else:
+        res, (syn, fwds, xs) = run_ours(args, wl, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            v, n_l, cores, t = oracle_sample(wl, syn, xs, budget_s=10.0)
+            res["cpu_baseline"] = {
+                "value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"{n_l} of {wl['layers']} layers, {t:.1f} s of fp64 "
+                          "oracle (route, group, expert FFNs, combine)"}
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

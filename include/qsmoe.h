@@ -1,0 +1,237 @@
+/*
+ * qsmoe: the quantized sparse mixture-of-experts FFN layer of a
+ * Qwen3.6-35B-A3B-style model, as a C ABI over hand-written CUDA kernels
+ * for sm_103a (GB300).
+ *
+ * The layer, in the terms of the pages it follows:
+ *   "Optimizing on-device inference for Apple Silicon" (Perplexity, 2026),
+ *     section "Qwen creates three distinct workload shapes": a router scores
+ *     256 experts per token and selects eight, next to a shared expert that
+ *     processes every token;
+ *     section "Keeping expert routing on the GPU": a histogram of the
+ *     assignments per expert, a prefix scan into start offsets, a scatter
+ *     of the rows into their expert groups and a block map of fixed-size
+ *     row blocks, all without a host round trip;
+ *     section "Dequantizing weights during matrix multiplication": 4-bit
+ *     affine weights in groups of 64 with a scale and a bias, expanded on
+ *     chip tile by tile, fp32 accumulation;
+ *     section "Reducing intermediate and state traffic": the two input
+ *     projections fused with their gated activation, and the output
+ *     projection fused with its routing score and the shared expert;
+ *   "oMLX MoE gate/up 融合优化：qwen35_moe_gate_up 实现剖析", section
+ *     "融合原理": gate and up weights concatenated along the output axis in
+ *     [gate, up] order, one quantized matmul, per-row bit-identical results;
+ *   "Ember: packed Q8 decode" (voidwest.dev): the Q8_0 row format, 32 int8
+ *     codes with one fp16 scale.
+ *
+ * Conventions (every entry point):
+ *  - Pointers named in the argument lists are DEVICE pointers unless said
+ *    otherwise; all arrays are dense row-major.  bf16 and fp16 values are
+ *    passed as their 16-bit patterns (uint16_t).
+ *  - The caller owns every buffer, including workspaces, and the stream.
+ *    The library allocates nothing, never synchronises the stream and never
+ *    reads device data on the host: every call only enqueues work on
+ *    `stream` (stream-ordered, capturable into a CUDA graph).
+ *  - The return value reports argument errors, found synchronously before
+ *    anything is enqueued, and launch errors.  Problems only visible on the
+ *    device (an expert id out of range, a non-finite logit, an fp16 operand
+ *    out of range) are OR-ed into *dev_status as QSM_DEV_* bits; the kernels
+ *    then skip the offending item and never trap.  *dev_status is never
+ *    cleared by the library; the caller zeroes it and reads it after the
+ *    stream has synchronised.
+ *  - Pointers must be 16-byte aligned, except dev_status and logit_bias
+ *    (4-byte).
+ */
+#ifndef QSMOE_H
+#define QSMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSM_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define QSM_API __attribute__((visibility("default")))
+#else
+#define QSM_API
+#endif
+
+typedef enum {
+  QSM_OK = 0,
+  QSM_ERR_INVALID_ARGUMENT = 1, /* null / misaligned pointer, bad size */
+  QSM_ERR_UNSUPPORTED = 2,      /* valid but not implemented (shape, type) */
+  QSM_ERR_WORKSPACE_TOO_SMALL = 3,
+  QSM_ERR_CUDA = 4              /* a CUDA launch or runtime call failed */
+} qsm_status;
+
+/* Bits of the device status word. */
+#define QSM_DEV_BAD_EXPERT_ID 1 /* topk_idx entry outside [0, E) */
+#define QSM_DEV_NONFINITE 2     /* non-finite router logit */
+#define QSM_DEV_FP16_RANGE 4    /* a value staged in fp16 overflowed */
+
+typedef enum { QSM_Q8_0 = 0, QSM_AFFINE4_G64 = 1 } qsm_qtype;
+
+/* A quantized weight tensor of shape [experts, rows, cols], rows = outputs,
+ * cols = inputs (reduction axis).
+ *  QSM_Q8_0:        codes int8 [experts, rows, cols]; scales fp16
+ *                   [experts, rows, cols/32]; weight = code * scale of its
+ *                   block of 32 inputs.  biases must be NULL.
+ *  QSM_AFFINE4_G64: codes uint32 [experts, rows, cols/8], input c stored in
+ *                   bits 4*(c%8)..4*(c%8)+3 of word c/8; scales and biases
+ *                   fp16 [experts, rows, cols/64]; weight = scale*code + bias
+ *                   for its group of 64 inputs. */
+typedef struct {
+  int32_t qtype;
+  int32_t experts, rows, cols;
+  const void* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+} qsm_qweights;
+
+/* One MoE FFN layer: hidden size H, expert (and shared expert) intermediate
+ * size I, E routed experts of which each token uses k.
+ *   gate_up        [E, 2I, H]  rows 0..I-1 gate, rows I..2I-1 up
+ *   down           [E, H, I]
+ *   shared_gate_up [1, 2I, H], shared_down [1, H, I]
+ * All four tensors must share one qtype.  Requires H % 64 == 0,
+ * I % 64 == 0, 1 <= k <= E <= 1024. */
+typedef struct {
+  int32_t H, I, E, k;
+  qsm_qweights gate_up, down, shared_gate_up, shared_down;
+} qsm_moe_layer;
+
+/* The token grouping produced by moe_group_tokens (all device arrays).
+ * Assignment a = t*k + j is token t's j-th selected expert.
+ *   counts   [E]     assignments per expert
+ *   offsets  [E+1]   exclusive prefix sum of counts (offsets[E] = T*k when
+ *                    every expert id is valid)
+ *   perm     [T*k]   assignment at each sorted position, sorted by
+ *                    (expert, assignment id): stable
+ *   inv_perm [T*k]   sorted position of each assignment, -1 if its expert
+ *                    id is invalid
+ *   tile_map [2*max_tiles]  (expert, first sorted row) of every block of at
+ *                    most tile_rows rows of one expert, experts ascending
+ *   n_tiles  [1]     number of blocks written (stays on the device)
+ * tile_rows and max_tiles are host values chosen by the caller:
+ * max_tiles >= moe_group_max_tiles(T, k, E, tile_rows), tile_rows as
+ * returned by moe_ffn_tile_rows() when the grouping feeds moe_ffn_forward. */
+typedef struct {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* tile_map;
+  int32_t* n_tiles;
+  int32_t tile_rows;
+  int32_t max_tiles;
+} qsm_grouping;
+
+/* ----------------------------------------------------------------- router */
+
+/* Bytes of workspace moe_route needs for T tokens and E experts. */
+QSM_API size_t moe_route_workspace_bytes(int32_t T, int32_t E);
+
+/* Router: logits l[t,e] = sum_h x[t,h] * w_router[e,h] + logit_bias[e]
+ * (fp32 accumulation), then per token the k largest logits (ties to the
+ * lower expert index) in descending order, and their weights
+ *   renormalize != 0: softmax over the k selected logits;
+ *   renormalize == 0: full softmax over all E logits, taken at the selected.
+ * [Perplexity page, "Qwen creates three distinct workload shapes".]
+ *   x          [T, H] bf16
+ *   w_router   [E, H] fp32
+ *   logit_bias [E] fp32 or NULL (added to the logits before selection)
+ *   topk_idx   [T, k] int32 (out), topk_w [T, k] fp32 (out)
+ *   workspace  >= moe_route_workspace_bytes(T, E) bytes.  It must hold
+ *              zeros before its first use; every call leaves it zeroed.
+ * Requires H % 64 == 0, 1 <= k <= min(E, 32), E <= 1024, T >= 0.
+ * A non-finite logit sets QSM_DEV_NONFINITE. */
+QSM_API qsm_status moe_route(const uint16_t* x, const float* w_router,
+                     const float* logit_bias, int32_t T, int32_t H, int32_t E,
+                     int32_t k, int32_t renormalize, int32_t* topk_idx,
+                     float* topk_w, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, cudaStream_t stream);
+
+/* --------------------------------------------------------------- grouping */
+
+/* Upper bound on the number of blocks of tile_rows rows over any routing:
+ * n + floor((T*k - n) / tile_rows) with n = min(E, T*k). */
+QSM_API int32_t moe_group_max_tiles(int32_t T, int32_t k, int32_t E,
+                            int32_t tile_rows);
+
+/* Histogram, exclusive scan, stable scatter and block map of the
+ * assignments [Perplexity page, "Keeping expert routing on the GPU"]; see
+ * qsm_grouping for the outputs.  An expert id outside [0, E) sets
+ * QSM_DEV_BAD_EXPERT_ID; that assignment is left out of every group
+ * (inv_perm = -1) and the FFN skips it.
+ * Requires 1 <= k, E <= 1024, tile_rows >= 1, T*k <= 2^24. */
+QSM_API qsm_status moe_group_tokens(const int32_t* topk_idx, int32_t T, int32_t k,
+                            int32_t E, const qsm_grouping* g,
+                            int32_t* dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------- FFN */
+
+/* The tile_rows moe_ffn_forward expects in its grouping for T tokens. */
+QSM_API int32_t moe_ffn_tile_rows(int32_t T);
+
+/* Bytes of workspace moe_ffn_forward needs for layer L and T tokens. */
+QSM_API size_t moe_ffn_workspace_bytes(const qsm_moe_layer* L, int32_t T);
+
+/* The expert FFNs and the combine:
+ *   for every assignment (t, j) with expert e = topk_idx[t, j]:
+ *     gu = W_gate_up[e] x[t]            (one fused quantized matmul)
+ *     h  = silu(gu[:I]) * gu[I:]        (SwiGLU, silu(g) = g / (1 + e^-g))
+ *     o  = W_down[e] h
+ *   the same for the shared expert, then
+ *     y[t] = sum_j topk_w[t, j] * o(t, j) + o_shared(t)
+ * [Perplexity page, "Reducing intermediate and state traffic"; oMLX page,
+ * "融合原理" and "前向传播补丁"].
+ *   x          [T, H] bf16;  y [T, H] bf16 (out, round-to-nearest-even of
+ *              the fp32 result);  y_f32 [T, H] fp32 (out, optional: the
+ *              same result before rounding, for parity checks) or NULL
+ *   topk_idx, topk_w  as written by moe_route;  g as written by
+ *              moe_group_tokens for the same topk_idx, with tile_rows ==
+ *              moe_ffn_tile_rows(T)
+ *   workspace  >= moe_ffn_workspace_bytes(L, T) bytes, no initial content.
+ * T <= 64 runs the decode kernels (weight streaming GEMV), larger T the
+ * grouped-GEMM prefill kernels. */
+QSM_API qsm_status moe_ffn_forward(const qsm_moe_layer* L, const uint16_t* x,
+                           int32_t T, const int32_t* topk_idx,
+                           const float* topk_w, const qsm_grouping* g,
+                           uint16_t* y, float* y_f32, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------ dense GEMV */
+
+/* Batch-1 Q8_0 projection y[n] = sum_c q[n,c] * d[n, c/32] * x[c]
+ * [Perplexity page, "Optimizing the single-row weight path"; Ember page,
+ * Q8_0 rows].
+ *   x [K] bf16;  q [N, K] int8;  d [N, K/32] fp16;  y [N] bf16 (out).
+ * Requires K % 64 == 0, 64 <= K <= 16384, N >= 1. */
+QSM_API qsm_status q8_gemv(const uint16_t* x, const int8_t* q, const uint16_t* d,
+                   int32_t N, int32_t K, uint16_t* y, int32_t* dev_status,
+                   cudaStream_t stream);
+
+/* ------------------------------------------------------------------ misc */
+
+/* Static description of a status code. */
+QSM_API const char* qsm_status_str(qsm_status s);
+
+/* QSM_ABI_VERSION of the loaded library. */
+QSM_API int32_t qsm_abi_version(void);
+
+/* Test hook: 0 = choose the FFN path by T (default), 1 = always the decode
+ * kernels, 2 = always the prefill kernels (when T allows).  Process-wide. */
+QSM_API qsm_status qsm_debug_force_path(int32_t mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSMOE_H */

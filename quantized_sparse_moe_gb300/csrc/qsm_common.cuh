@@ -1,0 +1,136 @@
+// Shared device and host helpers for the qsmoe CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qsmoe.h"
+
+#define QSM_CUDA_TRY(expr)                      \
+  do {                                          \
+    cudaError_t err_ = (expr);                  \
+    if (err_ != cudaSuccess) return QSM_ERR_CUDA; \
+  } while (0)
+
+namespace qsm {
+
+// ------------------------------------------------------------ host helpers
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+inline bool aligned4(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
+}
+
+// Launch with programmatic dependent launch enabled: the kernel may start
+// while its predecessor on the stream drains; it must execute
+// pdl_wait() before touching anything the predecessor writes (or reads).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------- device helpers
+
+// Wait until the preceding grid on the stream has completed and its memory
+// is visible (no-op when launched without programmatic serialization).
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid on the stream to begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void set_status(int32_t* st, int32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) {
+  return __uint_as_float(v << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t v) {
+  return __uint_as_float(v & 0xffff0000u);
+}
+
+// Two bf16 (packed) -> two fp16 (packed), round to nearest even.  Exact for
+// bf16 values whose magnitude lies in [2^-17, 65504].
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  __half2 h = __floats2half2_rn(bf16_lo(v), bf16_hi(v));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Four signed int8 codes (one 32-bit word) -> two packed fp16 pairs holding
+// the exact integers: lo = (b0, b1), hi = (b2, b3).  The byte is biased to
+// unsigned (xor 0x80), placed under the fp16 exponent of 1024 (0x64xx =
+// 1024 + byte), and 1152 = 1024 + 128 is subtracted.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo,
+                                                uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];"
+               : "=r"(r)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float silu(float g) {
+  return g / (1.0f + __expf(-g));
+}
+
+}  // namespace qsm

@@ -1,0 +1,120 @@
+"""Router and grouping kernels against the oracle: bit-exact ids, counts,
+permutations and block maps; routing weights within 1e-5."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _gpu_cases import TOPK_W_ATOL, layer, oracle_route, x_for
+
+pytestmark = pytest.mark.gpu
+
+ROUTE_CASES = [
+    # (shape, T, zipf, renormalize)
+    (synth.TINY, 4, None, True),
+    (synth.TINY, 1, None, False),
+    (synth.QWEN, 1, None, True),
+    (synth.QWEN, 3, None, True),
+    (synth.QWEN, 16, None, True),
+    (synth.QWEN, 40, None, True),
+    (synth.QWEN, 64, None, False),
+    (synth.QWEN, 65, None, True),
+    (synth.QWEN, 1000, "noise", True),
+    (synth.QWEN, 4096, "noise", True),
+]
+
+
+def _router_only(shape, seed, zipf):
+    wr = synth.draw_router(shape.E, shape.H, "cpu", seed, 0)
+    bias = None
+    if zipf:
+        bias = synth.zipf_logit_bias(shape.E, shape.H, seed, 0,
+                                     in_noise_units=(zipf == "noise"))
+    return wr, bias
+
+
+@pytest.mark.parametrize("shape,T,zipf,renorm", ROUTE_CASES)
+def test_route_matches_oracle(qsm, shape, T, zipf, renorm):
+    seed = 100 + T
+    wr, bias = _router_only(shape, seed, zipf)
+    L = synth.MoELayer(shape, wr, bias, None, None, None, None)
+    from _helpers import tie_free_x
+    x = tie_free_x(L, T, seed=seed)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx, w = qsm.moe_route(x.cuda(), wr.cuda(), shape.k,
+                           None if bias is None else bias.cuda(), renorm,
+                           dev_status=st)
+    torch.cuda.synchronize()
+    idx_o, w_o = oracle_route(x, wr, bias, shape.k, renorm)
+    assert st.item() == 0
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    np.testing.assert_allclose(w.cpu().numpy(), w_o, rtol=0, atol=TOPK_W_ATOL)
+
+
+def test_route_workspace_is_rearmed(qsm):
+    """Two calls in a row on one workspace give the same result."""
+    shape = synth.QWEN
+    wr, bias = _router_only(shape, 7, None)
+    x = synth.draw_x(24, shape.H, "cuda", 7)
+    ws = torch.zeros(qsm.route_workspace_bytes(24, shape.E), dtype=torch.uint8,
+                     device="cuda")
+    a = qsm.moe_route(x, wr.cuda(), 8, workspace=ws)
+    a = (a[0].clone(), a[1].clone())
+    b = qsm.moe_route(x, wr.cuda(), 8, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    counters = ws[qsm.route_workspace_bytes(24, shape.E) - 256:]
+    assert int(counters.sum().item()) == 0
+
+
+def _check_grouping(g, idx, E, BM):
+    ref = oracle.group(idx, E, BM)
+    assert np.array_equal(g.counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(g.offsets.cpu().numpy(), ref["offsets"])
+    A = idx.size
+    assert np.array_equal(g.perm.cpu().numpy()[:A], ref["perm"])
+    assert np.array_equal(g.inv_perm.cpu().numpy()[:A], ref["inv_perm"])
+    nt = int(g.n_tiles.item())
+    assert nt == ref["n_tiles"]
+    assert np.array_equal(g.tile_map.cpu().numpy()[:2 * nt].reshape(nt, 2),
+                          ref["tile_map"])
+
+
+@pytest.mark.parametrize("T,k,E,BM", [
+    (0, 8, 256, 8), (1, 8, 256, 8), (3, 2, 16, 8), (64, 8, 256, 8),
+    (65, 8, 256, 128), (4096, 8, 256, 128), (4096, 8, 256, 8),
+    (777, 4, 1024, 16), (2048, 8, 256, 32)])
+def test_group_matches_oracle(qsm, T, k, E, BM):
+    rng = np.random.default_rng(T * 31 + E)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) \
+        if T else np.zeros((0, k), np.int32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = qsm.moe_group_tokens(torch.from_numpy(idx).cuda(), E, BM, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _check_grouping(g, idx, E, BM)
+
+
+def test_group_skewed_all_to_one_expert_block(qsm):
+    """Every token routed to the same k experts (one huge group each)."""
+    T, k, E, BM = 3000, 8, 256, 128
+    idx = np.tile(np.arange(100, 100 + k, dtype=np.int32), (T, 1))
+    g = qsm.moe_group_tokens(torch.from_numpy(idx).cuda(), E, BM)
+    torch.cuda.synchronize()
+    _check_grouping(g, idx, E, BM)
+
+
+def test_group_flags_bad_expert_id(qsm):
+    T, k, E = 5, 2, 16
+    idx = np.array([[0, 1], [2, 99], [3, 4], [-1, 5], [6, 7]], np.int32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = qsm.moe_group_tokens(torch.from_numpy(idx).cuda(), E, 8, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & qsm.DEV_BAD_EXPERT_ID
+    inv = g.inv_perm.cpu().numpy()
+    assert inv[3] == -1 and inv[6] == -1
+    assert int(g.offsets[E].item()) == T * k - 2
+    valid = idx.ravel().copy()
+    ok = (valid >= 0) & (valid < E)
+    assert int(g.counts.sum().item()) == ok.sum()
