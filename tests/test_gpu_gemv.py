@@ -10,6 +10,20 @@ from _helpers import bits16, tol_metric
 pytestmark = pytest.mark.gpu
 
 
+def assert_faithful_bf16(y, ref):
+    """The bf16 output is within one bf16 ulp of the correctly rounded fp64
+    result (plus 1e-6 of max |ref| for fp32 accumulation near zero).  The
+    max-normalised 2e-3 bound cannot apply to a bf16-only output: rounding
+    alone reaches 2^-8 of a value."""
+    ref_b = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    _, e = np.frexp(np.abs(ref_b))
+    ulp = np.ldexp(1.0, e - 8)
+    slack = 1e-6 * np.max(np.abs(ref))
+    bad = np.abs(y - ref_b) > ulp + slack
+    assert not bad.any(), f"{bad.sum()} outputs off by more than one bf16 ulp"
+    assert tol_metric(y, ref) <= 2.0 ** -8
+
+
 @pytest.mark.parametrize("name", sorted(synth.GEMV_SHAPES))
 def test_gemv_shapes(qsm, name):
     N, K = synth.GEMV_SHAPES[name]
@@ -20,12 +34,7 @@ def test_gemv_shapes(qsm, name):
     qn = q[rows].cpu().numpy()
     ref = oracle.q8_gemv(bits16(x), qn, bits16(d[rows]))
     yc = y.float().cpu().numpy()[rows]
-    # bf16 output: compare after the same rounding on the reference side
-    ref_b = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
-    assert tol_metric(yc, ref) <= 2e-3
-    # at most one bf16 ulp away from the correctly rounded reference
-    ulp = np.abs(ref_b) * 2.0 ** -7 + 1e-30
-    assert np.all(np.abs(yc - ref_b) <= ulp * 1.01)
+    assert_faithful_bf16(yc, ref)
 
 
 def test_gemv_one_hot_bit_exact(qsm):
@@ -58,4 +67,4 @@ def test_gemv_ragged_rows(qsm):
         x, q, d = synth.draw_gemv(N, 512, "cuda", seed=N)
         y = qsm.q8_gemv(x, q, d)
         ref = oracle.q8_gemv(bits16(x), q.cpu().numpy(), bits16(d))
-        assert tol_metric(y.float().cpu().numpy(), ref) <= 2e-3
+        assert_faithful_bf16(y.float().cpu().numpy(), ref)
