@@ -207,6 +207,32 @@ QSM_API qsm_status moe_ffn_forward(const qsm_moe_layer* L, const uint16_t* x,
                            size_t workspace_bytes, int32_t* dev_status,
                            cudaStream_t stream);
 
+/* moe_ffn_forward without a workspace argument, for callers that cannot
+ * allocate device memory (code running inside another runtime's memory
+ * pool, latency-critical threads where an allocation and the device
+ * synchronisation it may cause are not allowed, hosts that own only the
+ * activations and the stream).  The pages have no counterpart: this is an
+ * interface convenience of this library, not a step of the method.
+ *   Arguments and results are those of moe_ffn_forward.  The scratch comes
+ *   from an array inside the library (1 MiB per device, held by every GPU
+ *   that loads the library until the process exits), so T must be <= 64 and
+ *   the layer's decode scratch ((T*k + T) * I * 2 bytes) must fit in 1 MiB;
+ *   otherwise QSM_ERR_UNSUPPORTED is returned and nothing is enqueued.
+ *   The call allocates nothing.  The first call on each device looks up that
+ *   device's copy of the array (make the stream's device current); make that
+ *   first call before any stream capture.  All calls on a device share the
+ *   one array and it keeps the last call's contents (no value has to start
+ *   at zero); calls whose work overlaps on the GPU (different streams, or
+ *   different threads without ordering) race on it and must be serialised
+ *   by the caller. */
+QSM_API qsm_status moe_ffn_forward_noalloc(const qsm_moe_layer* L,
+                                           const uint16_t* x, int32_t T,
+                                           const int32_t* topk_idx,
+                                           const float* topk_w,
+                                           const qsm_grouping* g, uint16_t* y,
+                                           float* y_f32, int32_t* dev_status,
+                                           cudaStream_t stream);
+
 /* ------------------------------------------------------------ dense GEMV */
 
 /* Batch-1 Q8_0 projection y[n] = sum_c q[n,c] * d[n, c/32] * x[c]

@@ -86,6 +86,10 @@ def lib() -> ctypes.CDLL:
                                           P, ctypes.POINTER(GroupingC), P, P,
                                           P, sz, P, P]
             L.moe_ffn_forward.restype = st
+            L.moe_ffn_forward_noalloc.argtypes = [
+                ctypes.POINTER(MoELayerC), P, i32, P, P,
+                ctypes.POINTER(GroupingC), P, P, P, P]
+            L.moe_ffn_forward_noalloc.restype = st
             L.q8_gemv.argtypes = [P, P, P, i32, i32, P, P, P]
             L.q8_gemv.restype = st
             L.qsm_status_str.argtypes = [st]
@@ -263,6 +267,27 @@ def moe_ffn_forward(layer: Layer, x: torch.Tensor, topk_idx: torch.Tensor,
                                  _p(workspace), workspace.numel(),
                                  _p(dev_status), _stream(stream)),
            "moe_ffn_forward")
+    return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None)
+
+
+def moe_ffn_forward_noalloc(layer: Layer, x: torch.Tensor,
+                            topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                            grouping: Grouping, y=None, y_f32=None,
+                            dev_status=None, stream=None):
+    """moe_ffn_forward with the library's built-in scratch (T <= 64): for
+    callers that cannot allocate device memory.  Outputs as moe_ffn_forward."""
+    T, H = x.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if y_f32 is True:
+        y_f32 = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dev_status = _status(dev_status, dev)
+    gc = grouping.c
+    _check(lib().moe_ffn_forward_noalloc(
+        ctypes.byref(layer.c), _p(_u16(x)), T, _p(topk_idx), _p(topk_w),
+        ctypes.byref(gc), _p(y), _p(y_f32 if y_f32 is not False else None),
+        _p(dev_status), _stream(stream)), "moe_ffn_forward_noalloc")
     return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None)
 
 
