@@ -201,22 +201,31 @@ def run_ours(args, wl, rank, world):
     value = world * T * nL / (ms / 1e3)
 
     # dominant launch pair: the expert FFN (gate_up+SwiGLU, down+combine),
-    # timed per layer with events on its stream, outside the graph
-    ffn_ms = []
-    for rep in range(3):
-        evs = [(torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(nL)]
+    # bracketed per layer by event nodes inside a captured graph so the
+    # elapsed times are pure device time on the FFN's stream
+    def graph_event():
+        # an event-record node inside the captured graph (timing enabled)
+        return torch.cuda.Event(enable_timing=True, external=True)
+
+    evs = [(graph_event(), graph_event()) for _ in range(nL)]
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        s2 = torch.cuda.current_stream()
         for (a, b), f, x, L in zip(evs, fwds, xs, layers):
             qsm.moe_route(x, L.w_router, L.k, L.logit_bias, True, f.topk_idx,
-                          f.topk_w, f.route_ws, f.dev_status, stream)
+                          f.topk_w, f.route_ws, f.dev_status, s2)
             qsm.moe_group_tokens(f.topk_idx, L.E, f.grouping.tile_rows,
-                                 f.grouping, f.dev_status, stream)
-            a.record(stream)
+                                 f.grouping, f.dev_status, s2)
+            a.record(s2)
             qsm.moe_ffn_forward(L, x, f.topk_idx, f.topk_w, f.grouping, f.y,
-                                False, f.ffn_ws, f.dev_status, stream)
-            b.record(stream)
-        torch.cuda.synchronize()
-        ffn_ms.append(sum(a.elapsed_time(b) for a, b in evs) / nL)
+                                False, f.ffn_ws, f.dev_status, s2)
+            b.record(s2)
+    ffn_ms = []
+    with torch.cuda.stream(stream):
+        for rep in range(5):
+            g2.replay()
+            torch.cuda.synchronize()
+            ffn_ms.append(sum(a.elapsed_time(b) for a, b in evs) / nL)
     ffn_ms = min(ffn_ms)
     qtype = wl["shape"].qtype
     step_bytes, n_exp = touched_bytes(layers, fwds, qtype)
@@ -359,13 +368,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the layer count (profiling runs only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers:
+        wl["layers"] = args.layers
+        wl["desc"] += f" (layer count overridden: {args.layers})"
     if args.impl == "reference":
         res = run_reference(args, wl, rank, world)
     else:

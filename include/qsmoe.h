@@ -74,6 +74,8 @@ typedef enum {
 #define QSM_DEV_BAD_EXPERT_ID 1 /* topk_idx entry outside [0, E) */
 #define QSM_DEV_NONFINITE 2     /* non-finite router logit */
 #define QSM_DEV_FP16_RANGE 4    /* a value staged in fp16 overflowed */
+#define QSM_DEV_TIMEOUT 8       /* a bounded wait on a copy ran out (the
+                                   kernel skipped its work and returned) */
 
 typedef enum { QSM_Q8_0 = 0, QSM_AFFINE4_G64 = 1 } qsm_qtype;
 
@@ -116,7 +118,8 @@ typedef struct {
  *   inv_perm [T*k]   sorted position of each assignment, -1 if its expert
  *                    id is invalid
  *   tile_map [2*max_tiles]  (expert, first sorted row) of every block of at
- *                    most tile_rows rows of one expert, experts ascending
+ *                    most tile_rows rows of one expert, experts ascending;
+ *                    entries n_tiles .. max_tiles-1 are set to (-1, -1)
  *   n_tiles  [1]     number of blocks written (stays on the device)
  * tile_rows and max_tiles are host values chosen by the caller:
  * max_tiles >= moe_group_max_tiles(T, k, E, tile_rows), tile_rows as

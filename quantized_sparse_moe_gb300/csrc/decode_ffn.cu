@@ -34,7 +34,7 @@ constexpr float kHScale = 1.0f / 16.0f;
 constexpr float kHScaleInv = 16.0f;
 constexpr int kTok = 8;       // tokens per MMA (N = 8) = the path's tile_rows
 constexpr int kD1Split = 4;   // d1: warps splitting K of one 16-row tile
-constexpr int kD2Warps = 16;  // d2: warps per 16-row output tile
+constexpr int kD2Warps = 12;  // d2: max warps per 16-row output tile
 
 using namespace gemv;
 
@@ -61,50 +61,198 @@ __device__ __forceinline__ Slot slot_of(int s, int shared_slots, int T,
     if (tau >= n_tiles) {
       r.e = 0; r.row0 = 0; r.cnt = 0;
     } else {
-      r.e = tile_map[2 * tau];
-      r.row0 = tile_map[2 * tau + 1];
-      r.cnt = min(kTok, offsets[r.e + 1] - r.row0);
+      const int2 te = __ldcg(reinterpret_cast<const int2*>(tile_map) + tau);
+      r.e = te.x;
+      r.row0 = te.y;
+      r.cnt = min(kTok, __ldcg(offsets + r.e + 1) - r.row0);
     }
   }
   return r;
 }
 
+// A warp keeps up to kPre 64-chunks of its weight slice in registers: all of
+// their loads are issued before the first MMA, so each warp pays about one
+// memory round trip per kPre chunks instead of one per chunk.
+constexpr int kPre = 8;
+constexpr int kXPad = 32;  // fp16 padding per staged x row (bank spread)
+
+template <int QT>
+__device__ __forceinline__ void load_batch(RawA (&r)[kPre], const QW& w, int rg,
+                                           int rh, int first, int stride,
+                                           int nch, int q) {
+#pragma unroll
+  for (int c = 0; c < kPre; ++c) {
+    const int ci = first + c * stride;
+    if (ci < nch) load_a<QT>(r[c], w, rg, rh, 64 * ci, q);
+  }
+}
+
 // ----------------------------------------------------------------- d1
+//
+// One CTA = one work slot (an expert and its <= 8 tokens) x 8 intermediate
+// indices: weight rows gate[i0..i0+7] and up[i0..i0+7].  The 16 code rows
+// arrive by TMA bulk copies (one per row, into rows padded by kRowPad bytes
+// so the MMA fragment reads are free of bank conflicts), tracked by one
+// mbarrier; the shared expert's CTAs start their copies before waiting on
+// the routing.  The CTA also asks L2 to prefetch its share of the expert's
+// down-projection rows, which the next launch streams.
+
+constexpr int kRowPad = 32;
+
+template <int QT>
+__device__ __forceinline__ int code_row_bytes(int cols) {
+  return QT == QSM_Q8_0 ? cols : cols / 2;
+}
+
+// RawA of rows g and g + 8 of a staged 16-row tile, for the 64-chunk at k0.
+template <int QT>
+__device__ __forceinline__ void load_a_smem(RawA& r, const unsigned char* wsm,
+                                            int pitch, const uint32_t* ssm,
+                                            int spitch, int g, int k0, int q) {
+  const unsigned char* rg = wsm + g * pitch;
+  const unsigned char* rh = wsm + (g + 8) * pitch;
+  if (QT == QSM_Q8_0) {
+    r.g0 = *reinterpret_cast<const uint2*>(rg + k0 + 8 * q);
+    r.g1 = *reinterpret_cast<const uint2*>(rg + k0 + 32 + 8 * q);
+    r.h0 = *reinterpret_cast<const uint2*>(rh + k0 + 8 * q);
+    r.h1 = *reinterpret_cast<const uint2*>(rh + k0 + 32 + 8 * q);
+  } else {
+    r.g0 = *reinterpret_cast<const uint2*>(rg + k0 / 2 + 8 * q);
+    r.h0 = *reinterpret_cast<const uint2*>(rh + k0 / 2 + 8 * q);
+  }
+  r.sg = ssm[g * spitch + k0 / 64];
+  r.sh = ssm[(g + 8) * spitch + k0 / 64];
+}
 
 template <int QT>
 __global__ void __launch_bounds__(kD1Split * 32)
-d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w,
-                  const uint16_t* __restrict__ x, int T, int H, int I, int k,
-                  const int32_t* __restrict__ perm,
+d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
+                  qsm_qweights sdn_w, const uint16_t* __restrict__ x, int T,
+                  int H, int I, int k, const int32_t* __restrict__ perm,
                   const int32_t* __restrict__ offsets,
-                  const int32_t* __restrict__ tile_map,
-                  const int32_t* __restrict__ n_tiles_p, int shared_slots,
-                  __half* __restrict__ hbuf, int32_t* dev_status) {
+                  const int32_t* __restrict__ tile_map, int shared_slots,
+                  int xrows, __half* __restrict__ hbuf, int32_t* dev_status) {
+  extern __shared__ __align__(128) unsigned char d1_smem[];
+  __shared__ __align__(8) uint64_t bar;
   __shared__ float red[kD1Split][32][4];
-  pdl_launch_dependents();
-  pdl_wait();
+  __shared__ int s_tok[kTok];
   const int lane = threadIdx.x & 31, kw = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int i0 = kTok * blockIdx.x;  // 8 intermediate indices per CTA
-  const Slot sl = slot_of(blockIdx.y, shared_slots, T, offsets, tile_map,
-                          *n_tiles_p);
-  if (sl.cnt <= 0) return;
-  const QW w = sl.e < 0 ? expert_of<QT>(sgu_w, 0) : expert_of<QT>(gu_w, sl.e);
-  // token of B column g, and the h rows of this thread's output columns
-  int tok_g = -1;
-  if (g < sl.cnt) tok_g = sl.e < 0 ? sl.row0 + g : perm[sl.row0 + g] / k;
-  const uint16_t* xrow = x + (size_t)max(tok_g, 0) * H;
+  const int crow = code_row_bytes<QT>(H);
+  const int pitch = crow + kRowPad;
+  const int spitch = H / 64 + 1;     // u32 per staged scale row (+1: banks)
+  unsigned char* wsm = d1_smem;                                   // [16][pitch]
+  uint32_t* ssm = reinterpret_cast<uint32_t*>(d1_smem + 16 * pitch);  // [16][spitch]
+  __half* xs = reinterpret_cast<__half*>(
+      d1_smem + ((16 * pitch + 16 * spitch * 4 + 15) & ~15));     // [xrows][H+kXPad]
+  const bool shared_slot = (int)blockIdx.y < shared_slots;
 
-  // 64-wide chunks are dealt round-robin to the kD1Split warps
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue_copies = [&](const QW& w) {
+    if (kw == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(&bar, 16u * crow);
+      __syncwarp();
+      if (lane < 16) {
+        const int row = lane < 8 ? i0 + lane : I + i0 + (lane - 8);
+        bulk_g2s(wsm + lane * pitch, w.codes + (size_t)row * crow, crow, &bar);
+      }
+    }
+  };
+  // L2 prefetch of this CTA's 1/gridDim.x share of the expert's down rows.
+  auto prefetch_down = [&](const QW& d) {
+    if (kw == 1 && lane == 0) {
+      const int drow = code_row_bytes<QT>(I);
+      const int rows = H / gridDim.x;  // H is a multiple of 16, grid = I/8
+      if (rows > 0 && (rows * drow) % 16 == 0) {
+        const int r0 = blockIdx.x * rows;
+        bulk_prefetch_l2(d.codes + (size_t)r0 * drow, rows * drow);
+        const int sb = (QT == QSM_Q8_0 ? I / 32 : I / 64) * 2;
+        if ((rows * sb) % 16 == 0) {
+          bulk_prefetch_l2(d.scales + (size_t)r0 * (sb / 2), rows * sb);
+          if (QT != QSM_Q8_0) bulk_prefetch_l2(d.biases + (size_t)r0 * (sb / 2), rows * sb);
+        }
+      }
+    }
+  };
+
+  int e = -1, row0, cnt;
+  QW w;
+  if (shared_slot) {  // static weights: start the copies before the wait
+    w = expert_of<QT>(sgu_w, 0);
+    issue_copies(w);
+    prefetch_down(expert_of<QT>(sdn_w, 0));
+  }
+  // The routing comes from the grouping launch: wait for it, then let the
+  // down-projection launch start (it may read the routing right away).
+  pdl_wait();
+  pdl_launch_dependents();
+  if (shared_slot) {
+    row0 = kTok * blockIdx.y;
+    cnt = min(kTok, T - row0);
+  } else {
+    const int tau = blockIdx.y - shared_slots;
+    const int2 te = __ldcg(reinterpret_cast<const int2*>(tile_map) + tau);
+    if (te.x < 0) return;  // no block map entry for this slot
+    e = te.x;
+    row0 = te.y;
+    w = expert_of<QT>(gu_w, e);
+    issue_copies(w);
+    prefetch_down(expert_of<QT>(dn_w, e));
+    cnt = min(kTok, __ldcg(offsets + e + 1) - row0);
+  }
+
+  // block scales (and biases) of the 16 rows -> shared, as u32 per 64-chunk
+  for (int i = threadIdx.x; i < 16 * (H / 64); i += blockDim.x) {
+    const int rr = i / (H / 64), j = i - rr * (H / 64);
+    const int row = rr < 8 ? i0 + rr : I + i0 + (rr - 8);
+    uint32_t v;
+    if (QT == QSM_Q8_0) {
+      v = __ldg(reinterpret_cast<const uint32_t*>(w.scales + (size_t)row * (H / 32)) + j);
+    } else {
+      const size_t gi = (size_t)row * (H / 64) + j;
+      v = (uint32_t)__half_as_ushort(w.scales[gi]) |
+          ((uint32_t)__half_as_ushort(w.biases[gi]) << 16);
+    }
+    ssm[rr * spitch + j] = v;
+  }
+  // this slot's token rows of x, as fp16
+  if (threadIdx.x < kTok)
+    s_tok[threadIdx.x] = threadIdx.x < cnt
+        ? (shared_slot ? row0 + threadIdx.x : __ldcg(perm + row0 + threadIdx.x) / k)
+        : 0;
+  __syncthreads();
+  const int xpitch = H + kXPad;
+  const int v8 = H / 8;
+  for (int i = threadIdx.x; i < cnt * v8; i += blockDim.x) {
+    const int c = i / v8, j = i - c * v8;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)s_tok[c] * H) + j);
+    *reinterpret_cast<uint4*>(xs + c * xpitch + 8 * j) = bf16x8_to_f16x8(v);
+  }
+  __syncthreads();
+  // bounded wait for the weight rows; the CTA agrees on the outcome
+  if (!__syncthreads_and(mbar_wait_bounded(&bar, 0, kWaitIters))) {
+    if (threadIdx.x == 0) set_status(dev_status, QSM_DEV_TIMEOUT);
+    mbar_wait_bounded(&bar, 0, kWaitIters);  // let our copies land first
+    return;
+  }
+
+  const __half* xg = xs + min(g, xrows - 1) * xpitch;
+  const bool has_tok = g < cnt;
+  const int nch = H / 64;  // chunks dealt round-robin to the kD1Split warps
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-  for (int k0 = 64 * kw; k0 < H; k0 += 64 * kD1Split) {
+#pragma unroll 4
+  for (int ci = kw; ci < nch; ci += kD1Split) {
     RawA r;
-    load_a<QT>(r, w, i0 + g, I + i0 + g, k0, q);
+    load_a_smem<QT>(r, wsm, pitch, ssm, spitch, g, 64 * ci, q);
     uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
-    if (tok_g >= 0) {
-      X0 = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(xrow + k0 + b_off0<QT>(q))));
-      X1 = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(xrow + k0 + b_off1<QT>(q))));
+    if (has_tok) {
+      X0 = *reinterpret_cast<const uint4*>(xg + 64 * ci + b_off0<QT>(q));
+      X1 = *reinterpret_cast<const uint4*>(xg + 64 * ci + b_off1<QT>(q));
     }
     chunk_mma<QT>(acc, r, X0, X1);
   }
@@ -123,11 +271,11 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w,
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     const int c = 2 * q + cc;
-    if (c < sl.cnt) {
+    if (c < cnt) {
       const float gate = acc[cc], up = acc[2 + cc];
       const float h = silu(gate) * up * kHScale;
       if (!(fabsf(h) <= 65504.f)) bad = true;
-      const int hrow = sl.e < 0 ? T * k + sl.row0 + c : sl.row0 + c;
+      const int hrow = shared_slot ? T * k + row0 + c : row0 + c;
       hbuf[(size_t)hrow * I + i0 + g] = __float2half_rn(h);
     }
   }
@@ -135,6 +283,33 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w,
 }
 
 // ----------------------------------------------------------------- d2
+//
+// One CTA = 16 output rows n0..n0+15 of y for every token.  Work items are
+// the shared expert's blocks of 8 tokens and the block map's blocks; warp w
+// takes items w, w + warps, ...  Each warp owns one shared-memory slot:
+// the item's 16 down rows (padded), their scales and the item's h rows
+// arrive by bulk copies on the warp's mbarrier.  The weight copies of the
+// first item are issued before waiting on the gate_up launch (the routing
+// was complete before that launch let this one start, and the weights were
+// prefetched into L2 by it); only the h copies wait.  Each warp sums its
+// items into its own [T][16] fp32 slab; the slabs are added in warp order.
+
+struct D2Geo {  // per-slot layout (bytes)
+  int crow, pitch, wbytes, sbytes, hpitch, hoff, slot;
+};
+
+template <int QT>
+__host__ __device__ __forceinline__ D2Geo d2_geo(int I, int hrows) {
+  D2Geo g;
+  g.crow = QT == QSM_Q8_0 ? I : I / 2;          // code bytes per row
+  g.pitch = g.crow + kRowPad;
+  g.wbytes = 16 * g.pitch;
+  g.sbytes = QT == QSM_Q8_0 ? 16 * (I / 32) * 2 : 2 * 16 * (I / 64) * 2;
+  g.hpitch = 2 * I + 32;                        // bytes per staged h row
+  g.hoff = (g.wbytes + g.sbytes + 15) & ~15;
+  g.slot = (g.hoff + hrows * g.hpitch + 127) & ~127;
+  return g;
+}
 
 template <int QT>
 __global__ void __launch_bounds__(kD2Warps * 32)
@@ -144,23 +319,85 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
                 const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ tile_map,
                 const int32_t* __restrict__ n_tiles_p,
-                const float* __restrict__ topk_w, int shared_slots,
-                uint16_t* __restrict__ y, float* __restrict__ y32) {
-  extern __shared__ float slab[];  // [kD2Warps][T][16]
-  pdl_launch_dependents();
-  pdl_wait();
+                const float* __restrict__ topk_w, int shared_slots, int hrows,
+                uint16_t* __restrict__ y, float* __restrict__ y32,
+                int32_t* dev_status) {
+  extern __shared__ __align__(128) unsigned char d2_smem[];
+  __shared__ __align__(8) uint64_t bars[kD2Warps];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int n0 = 16 * blockIdx.x;
-  for (int i = threadIdx.x; i < kD2Warps * T * 16; i += blockDim.x) slab[i] = 0.f;
-  __syncthreads();
-  float* my = slab + (size_t)wid * T * 16;
-  const int items = shared_slots + *n_tiles_p;
-  for (int it = wid; it < items; it += kD2Warps) {
-    const Slot sl = slot_of(it, shared_slots, T, offsets, tile_map, items - shared_slots);
-    if (sl.cnt <= 0) continue;
+  const int nch = I / 64;
+  const D2Geo geo = d2_geo<QT>(I, hrows);
+  unsigned char* slot = d2_smem + (size_t)wid * geo.slot;
+  float* slab = reinterpret_cast<float*>(d2_smem + (size_t)nw * geo.slot);  // [nw][T][16]
+  uint64_t* bar = &bars[wid];
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Routing data and weights need no wait (see above).
+  const int n_tiles = __ldcg(n_tiles_p);
+  const int items = shared_slots + n_tiles;
+  for (int i = threadIdx.x; i < nw * T * 16; i += blockDim.x) slab[i] = 0.f;
+
+  auto issue_weights = [&](const Slot& sl) {
     const QW w = sl.e < 0 ? expert_of<QT>(sdn_w, 0) : expert_of<QT>(dn_w, sl.e);
-    const int hrow_g = g < sl.cnt ? (sl.e < 0 ? T * k + sl.row0 + g : sl.row0 + g) : -1;
+    if (lane == 0) mbar_expect_tx(bar, 16u * geo.crow + geo.sbytes);
+    __syncwarp();
+    if (lane < 16)
+      bulk_g2s(slot + lane * geo.pitch, w.codes + (size_t)(n0 + lane) * geo.crow,
+               geo.crow, bar);
+    if (lane == 16) {
+      if (QT == QSM_Q8_0) {
+        bulk_g2s(slot + geo.wbytes, w.scales + (size_t)n0 * (I / 32), geo.sbytes, bar);
+      } else {
+        bulk_g2s(slot + geo.wbytes, w.scales + (size_t)n0 * (I / 64), geo.sbytes / 2, bar);
+        bulk_g2s(slot + geo.wbytes + geo.sbytes / 2, w.biases + (size_t)n0 * (I / 64),
+                 geo.sbytes / 2, bar);
+      }
+    }
+  };
+  auto h_row_of = [&](const Slot& sl, int c) {
+    return sl.e < 0 ? T * k + sl.row0 + c : sl.row0 + c;
+  };
+  auto issue_h = [&](const Slot& sl) {
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)sl.cnt * (2 * I));
+    __syncwarp();
+    if (lane < sl.cnt)
+      bulk_g2s(slot + geo.hoff + lane * geo.hpitch,
+               hbuf + (size_t)h_row_of(sl, lane) * I, 2 * I, bar);
+  };
+
+  Slot cur;
+  if (wid < items) {
+    cur = slot_of(wid, shared_slots, T, offsets, tile_map, n_tiles);
+    issue_weights(cur);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();  // slab zeroed
+
+  float* my = slab + (size_t)wid * T * 16;
+  uint32_t phase = 0;
+  bool ok_all = true;
+  for (int it = wid; it < items; it += nw) {
+    if (it != wid) {
+      cur = slot_of(it, shared_slots, T, offsets, tile_map, n_tiles);
+      issue_weights(cur);
+    }
+    issue_h(cur);
+    const bool ok = mbar_wait_bounded(bar, phase, kWaitIters);
+    phase ^= 1u;
+    if (!ok) {  // copies did not land: skip, flag, let them finish
+      ok_all = false;
+      mbar_wait_bounded(bar, phase ^ 1u, kWaitIters);
+      break;
+    }
+    // this thread's output columns 2q, 2q+1: token and routing weight
     int tok[2];
     float wt[2];
 #pragma unroll
@@ -168,27 +405,48 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
       const int c = 2 * q + cc;
       tok[cc] = -1;
       wt[cc] = 0.f;
-      if (c < sl.cnt) {
-        if (sl.e < 0) {
-          tok[cc] = sl.row0 + c;
+      if (c < cur.cnt) {
+        if (cur.e < 0) {
+          tok[cc] = cur.row0 + c;
           wt[cc] = 1.f;
         } else {
-          const int a = perm[sl.row0 + c];
+          const int a = __ldcg(perm + cur.row0 + c);
           tok[cc] = a / k;
-          wt[cc] = topk_w[a];
+          wt[cc] = __ldcg(topk_w + a);
         }
       }
     }
-    const __half* hrow = hbuf + (size_t)max(hrow_g, 0) * I;
+    const unsigned char* sc = slot + geo.wbytes;
+    const __half* hg = reinterpret_cast<const __half*>(slot + geo.hoff + min(g, hrows - 1) * geo.hpitch);
+    const bool has_tok = g < cur.cnt;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int k0 = 0; k0 < I; k0 += 64) {
+#pragma unroll 4
+    for (int ci = 0; ci < nch; ++ci) {
+      const int k0 = 64 * ci;
       RawA r;
-      load_a<QT>(r, w, n0 + g, n0 + g + 8, k0, q);
+      const unsigned char* rg = slot + g * geo.pitch;
+      const unsigned char* rh = slot + (g + 8) * geo.pitch;
+      if (QT == QSM_Q8_0) {
+        r.g0 = *reinterpret_cast<const uint2*>(rg + k0 + 8 * q);
+        r.g1 = *reinterpret_cast<const uint2*>(rg + k0 + 32 + 8 * q);
+        r.h0 = *reinterpret_cast<const uint2*>(rh + k0 + 8 * q);
+        r.h1 = *reinterpret_cast<const uint2*>(rh + k0 + 32 + 8 * q);
+        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(sc);
+        r.sg = s32[g * (I / 64) + ci];
+        r.sh = s32[(g + 8) * (I / 64) + ci];
+      } else {
+        r.g0 = *reinterpret_cast<const uint2*>(rg + k0 / 2 + 8 * q);
+        r.h0 = *reinterpret_cast<const uint2*>(rh + k0 / 2 + 8 * q);
+        const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sc);
+        const uint16_t* b16 = s16 + 16 * (I / 64);
+        r.sg = (uint32_t)s16[g * (I / 64) + ci] | ((uint32_t)b16[g * (I / 64) + ci] << 16);
+        r.sh = (uint32_t)s16[(g + 8) * (I / 64) + ci] |
+               ((uint32_t)b16[(g + 8) * (I / 64) + ci] << 16);
+      }
       uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
-      if (hrow_g >= 0) {
-        X0 = __ldg(reinterpret_cast<const uint4*>(hrow + k0 + b_off0<QT>(q)));
-        X1 = __ldg(reinterpret_cast<const uint4*>(hrow + k0 + b_off1<QT>(q)));
+      if (has_tok) {
+        X0 = *reinterpret_cast<const uint4*>(hg + k0 + b_off0<QT>(q));
+        X1 = *reinterpret_cast<const uint4*>(hg + k0 + b_off1<QT>(q));
       }
       chunk_mma<QT>(acc, r, X0, X1);
     }
@@ -200,15 +458,17 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
         my[tok[cc] * 16 + g + 8] += s * acc[2 + cc];
       }
     }
-    __syncwarp();
+    __syncwarp();  // slot and slab free for the next item
   }
-  __syncthreads();
+  if (!__syncthreads_and(ok_all)) {
+    if (threadIdx.x == 0) set_status(dev_status, QSM_DEV_TIMEOUT);
+    return;
+  }
   for (int i = threadIdx.x; i < T * 16; i += blockDim.x) {
     float s = 0.f;
-#pragma unroll 4
-    for (int wv = 0; wv < kD2Warps; ++wv) s += slab[(size_t)wv * T * 16 + i];
-    const int t = i / 16, r = i % 16;
-    const size_t o = (size_t)t * H + n0 + r;
+    for (int wv = 0; wv < nw; ++wv) s += slab[(size_t)wv * T * 16 + i];
+    const int t = i / 16, rr = i % 16;
+    const size_t o = (size_t)t * H + n0 + rr;
     y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
     if (y32) y32[o] = s;
   }
@@ -217,46 +477,57 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
 }  // namespace decode
 
 // Host launcher used by moe_ffn_forward for the decode path.
+template <int QT>
+static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
+                                   int T, const float* topk_w,
+                                   const qsm_grouping* g, uint16_t* y,
+                                   float* y32, __half* hbuf,
+                                   int32_t* dev_status, cudaStream_t stream) {
+  using namespace decode;
+  const int H = L->H, I = L->I, k = L->k;
+  const int shared_slots = (T + kTok - 1) / kTok;
+  const dim3 g1(I / kTok, shared_slots + g->max_tiles);
+  const int xrows = T < kTok ? T : kTok;
+  const int crow = QT == QSM_Q8_0 ? H : H / 2;
+  const size_t smem1 = ((size_t)16 * (crow + kRowPad) + 16 * (H / 64 + 1) * 4 + 15) / 16 * 16 +
+                       (size_t)xrows * (H + kXPad) * sizeof(__half);
+  const int max_items = shared_slots + g->max_tiles;
+  const D2Geo geo = d2_geo<QT>(I, xrows);
+  int w2 = max_items < kD2Warps ? max_items : kD2Warps;
+  const size_t slab_bytes_per_warp = (size_t)T * 16 * sizeof(float);
+  const size_t kSmemBudget = 200 * 1024;
+  while (w2 > 1 && (size_t)w2 * (geo.slot + slab_bytes_per_warp) > kSmemBudget) --w2;
+  const size_t smem2 = (size_t)w2 * (geo.slot + slab_bytes_per_warp);
+  QSM_CUDA_TRY(cudaFuncSetAttribute(d1_gate_up_swiglu<QT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem1));
+  QSM_CUDA_TRY(launch_pdl(d1_gate_up_swiglu<QT>, g1, dim3(kD1Split * 32), smem1,
+                          stream, L->gate_up, L->shared_gate_up, L->down,
+                          L->shared_down, x, T, H, I, k, (const int32_t*)g->perm,
+                          (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
+                          shared_slots, xrows, hbuf, dev_status));
+  QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QT>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem2));
+  QSM_CUDA_TRY(launch_pdl(d2_down_combine<QT>, dim3(H / 16), dim3(w2 * 32), smem2,
+                          stream, L->down, L->shared_down, (const __half*)hbuf, T,
+                          H, I, k, (const int32_t*)g->perm,
+                          (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
+                          (const int32_t*)g->n_tiles, topk_w, shared_slots, xrows,
+                          y, y32, dev_status));
+  return QSM_OK;
+}
+
 qsm_status decode_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
                              const float* topk_w, const qsm_grouping* g,
                              uint16_t* y, float* y32, void* ws,
                              int32_t* dev_status, cudaStream_t stream) {
-  using namespace decode;
-  const int H = L->H, I = L->I, k = L->k;
-  const int shared_slots = (T + kTok - 1) / kTok;
   __half* hbuf = static_cast<__half*>(ws);
-  const dim3 g1(I / kTok, shared_slots + g->max_tiles);
-  const size_t smem2 = (size_t)kD2Warps * T * 16 * sizeof(float);
-  if (L->gate_up.qtype == QSM_Q8_0) {
-    QSM_CUDA_TRY(launch_pdl(d1_gate_up_swiglu<QSM_Q8_0>, g1, dim3(kD1Split * 32), 0,
-                            stream, L->gate_up, L->shared_gate_up, x, T, H, I, k,
-                            (const int32_t*)g->perm, (const int32_t*)g->offsets,
-                            (const int32_t*)g->tile_map, (const int32_t*)g->n_tiles,
-                            shared_slots, hbuf, dev_status));
-    QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QSM_Q8_0>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem2));
-    QSM_CUDA_TRY(launch_pdl(d2_down_combine<QSM_Q8_0>, dim3(H / 16), dim3(kD2Warps * 32),
-                            smem2, stream, L->down, L->shared_down, (const __half*)hbuf,
-                            T, H, I, k, (const int32_t*)g->perm,
-                            (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
-                            (const int32_t*)g->n_tiles, topk_w, shared_slots, y, y32));
-  } else {
-    QSM_CUDA_TRY(launch_pdl(d1_gate_up_swiglu<QSM_AFFINE4_G64>, g1, dim3(kD1Split * 32), 0,
-                            stream, L->gate_up, L->shared_gate_up, x, T, H, I, k,
-                            (const int32_t*)g->perm, (const int32_t*)g->offsets,
-                            (const int32_t*)g->tile_map, (const int32_t*)g->n_tiles,
-                            shared_slots, hbuf, dev_status));
-    QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QSM_AFFINE4_G64>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem2));
-    QSM_CUDA_TRY(launch_pdl(d2_down_combine<QSM_AFFINE4_G64>, dim3(H / 16),
-                            dim3(kD2Warps * 32), smem2, stream, L->down, L->shared_down,
-                            (const __half*)hbuf, T, H, I, k, (const int32_t*)g->perm,
-                            (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
-                            (const int32_t*)g->n_tiles, topk_w, shared_slots, y, y32));
-  }
-  return QSM_OK;
+  if (L->gate_up.qtype == QSM_Q8_0)
+    return decode_launch_qt<QSM_Q8_0>(L, x, T, topk_w, g, y, y32, hbuf,
+                                      dev_status, stream);
+  return decode_launch_qt<QSM_AFFINE4_G64>(L, x, T, topk_w, g, y, y32, hbuf,
+                                           dev_status, stream);
 }
 
 size_t decode_ffn_workspace_bytes(const qsm_moe_layer* L, int T) {

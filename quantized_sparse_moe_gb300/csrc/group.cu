@@ -28,6 +28,7 @@ constexpr size_t kSmemLimit = 227 * 1024 - 1024;  // leave room for static smem
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot,
                                                     int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -37,14 +38,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot,
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_tot[lane];
+    int w = lane < nwarps ? warp_tot[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += n;
     }
-    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane < nwarps) warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
     if (lane == 31) *total = wi;
   }
   __syncthreads();
@@ -120,6 +121,10 @@ group_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
     }
   }
   __syncthreads();
+  for (int i = s_tiles + tid; i < max_tiles; i += kThreads) {
+    tile_map[2 * i] = -1;
+    tile_map[2 * i + 1] = -1;
+  }
 
   // pass 2: stable scatter
   const unsigned lt = (1u << lane) - 1u;
@@ -147,6 +152,72 @@ group_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
   if (stage)
     for (int i = tid; i < valid; i += kThreads) perm[i] = sperm[i];
   for (int i = valid + tid; i < A; i += kThreads) perm[i] = -1;
+}
+
+// Few assignments (decode): the per-warp histogram machinery above costs
+// more than the work.  Thread e owns expert e and walks the (at most
+// kSmallA) assignments in shared memory twice: once to count, once to place
+// its rows in assignment order (stable by construction).
+constexpr int kSmallA = 1024;
+
+template <int NT>  // threads: a multiple of 32 and >= E
+__global__ void __launch_bounds__(NT, 1)
+group_small_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
+                   int max_tiles, int32_t* __restrict__ counts,
+                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                   int32_t* __restrict__ inv_perm,
+                   int32_t* __restrict__ tile_map,
+                   int32_t* __restrict__ n_tiles, int32_t* dev_status) {
+  __shared__ int sidx[kSmallA];
+  __shared__ int warp_tot[32];
+  __shared__ int s_total, s_tiles;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x;
+  bool bad = false;
+  for (int a = tid; a < A; a += NT) {
+    int v = __ldcg(topk_idx + a);
+    if (v < 0 || v >= E) {
+      bad = true;
+      v = -1;
+      inv_perm[a] = -1;
+    }
+    sidx[a] = v;
+  }
+  if (__syncthreads_or(bad) && tid == 0)
+    set_status(dev_status, QSM_DEV_BAD_EXPERT_ID);
+  const int e = tid;
+  int cnt = 0;
+  if (e < E)
+    for (int a = 0; a < A; ++a) cnt += (sidx[a] == e);
+  const int off = block_exclusive_scan(e < E ? cnt : 0, warp_tot, &s_total);
+  const int nt = (e < E) ? (cnt + BM - 1) / BM : 0;
+  const int t0 = block_exclusive_scan(nt, warp_tot, &s_tiles);
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    for (int m = 0; m < nt && t0 + m < max_tiles; ++m) {
+      tile_map[2 * (t0 + m)] = e;
+      tile_map[2 * (t0 + m) + 1] = off + m * BM;
+    }
+    int pos = off;
+    for (int a = 0; a < A && pos < off + cnt; ++a) {
+      if (sidx[a] == e) {
+        perm[pos] = a;
+        inv_perm[a] = pos;
+        ++pos;
+      }
+    }
+  }
+  if (tid == 0) {
+    offsets[E] = s_total;
+    n_tiles[0] = min(s_tiles, max_tiles);
+  }
+  for (int i = s_tiles + tid; i < max_tiles; i += NT) {
+    tile_map[2 * i] = -1;
+    tile_map[2 * i + 1] = -1;
+  }
+  for (int i = s_total + tid; i < A; i += NT) perm[i] = -1;
 }
 
 }  // namespace
@@ -178,6 +249,21 @@ extern "C" qsm_status moe_group_tokens(const int32_t* topk_idx, int32_t T,
     return QSM_ERR_INVALID_ARGUMENT;
   if (g->max_tiles < moe_group_max_tiles(T, k, E, g->tile_rows))
     return QSM_ERR_INVALID_ARGUMENT;
+  if (A <= kSmallA) {
+    if (E <= 256)
+      QSM_CUDA_TRY(launch_pdl(group_small_kernel<256>, dim3(1), dim3(256), 0,
+                              stream, topk_idx, (int)A, (int)E,
+                              (int)g->tile_rows, (int)g->max_tiles, g->counts,
+                              g->offsets, g->perm, g->inv_perm, g->tile_map,
+                              g->n_tiles, dev_status));
+    else
+      QSM_CUDA_TRY(launch_pdl(group_small_kernel<kThreads>, dim3(1), dim3(kThreads),
+                              0, stream, topk_idx, (int)A, (int)E,
+                              (int)g->tile_rows, (int)g->max_tiles, g->counts,
+                              g->offsets, g->perm, g->inv_perm, g->tile_map,
+                              g->n_tiles, dev_status));
+    return QSM_OK;
+  }
   const size_t hist_bytes = (size_t)kWarps * E * sizeof(int);
   const int stage = hist_bytes + (size_t)A * sizeof(int) <= kSmemLimit;
   const size_t smem = hist_bytes + (stage ? (size_t)A * sizeof(int) : 0);

@@ -29,6 +29,9 @@ size_t counters_offset(int T, int E) {
   return (b + 255) & ~size_t(255);
 }
 
+constexpr int kWPer = 4;  // float4 of the router row per thread and batch
+
+template <int kPer>  // candidates per lane in the top-k: ceil(E / 32)
 __global__ void __launch_bounds__(kThreads)
 route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
              const float* __restrict__ bias, int T, int H, int E, int k,
@@ -36,9 +39,10 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
              float* __restrict__ topk_w, float* __restrict__ logits,
              unsigned int* __restrict__ counters, int32_t* dev_status) {
   __shared__ float red[kExpertsPerCta][kThreadsPerExpert / 32][kTokPerCta];
+  __shared__ float sel_l[kThreads / 32][kMaxK];
+  __shared__ int sel_e[kThreads / 32][kMaxK];
   __shared__ int is_last;
 
-  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int sub = tid / kThreadsPerExpert;          // expert within the CTA
@@ -46,37 +50,58 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
   const int e = blockIdx.x * kExpertsPerCta + sub;
   const int t0 = blockIdx.y * kTokPerCta;
   const int nt = min(kTokPerCta, T - t0);
-
-  // Router row slice is read-only model data: fetch before the wait.
-  const float4* wrow = reinterpret_cast<const float4*>(w + (size_t)min(e, E - 1) * H);
   const int H4 = H / 4;
+
+  // The router row is model data no launch writes: fetch it before waiting.
+  const float4* wrow = reinterpret_cast<const float4*>(w + (size_t)min(e, E - 1) * H);
+  float4 wv[kWPer];
+#pragma unroll
+  for (int i = 0; i < kWPer; ++i) {
+    const int h4 = st + i * kThreadsPerExpert;
+    wv[i] = h4 < H4 ? __ldg(wrow + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   pdl_wait();
+  pdl_launch_dependents();
 
   float acc[kTokPerCta];
 #pragma unroll
   for (int i = 0; i < kTokPerCta; ++i) acc[i] = 0.f;
-  if (e < E) {
-    for (int h4 = st; h4 < H4; h4 += kThreadsPerExpert) {
-      const float4 wv = __ldg(wrow + h4);
+  for (int hb = 0; hb < H4; hb += kWPer * kThreadsPerExpert) {
+    if (hb > 0) {
 #pragma unroll
-      for (int i = 0; i < kTokPerCta; ++i) {
-        if (i < nt) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(
-              x + (size_t)(t0 + i) * H + 4 * h4));
-          float a = acc[i];
-          a = fmaf(wv.x, bf16_lo(xv.x), a);
-          a = fmaf(wv.y, bf16_hi(xv.x), a);
-          a = fmaf(wv.z, bf16_lo(xv.y), a);
-          a = fmaf(wv.w, bf16_hi(xv.y), a);
-          acc[i] = a;
+      for (int i = 0; i < kWPer; ++i) {
+        const int h4 = hb + st + i * kThreadsPerExpert;
+        wv[i] = h4 < H4 ? __ldg(wrow + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kTokPerCta; ++tt) {
+      if (tt < nt) {
+        const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)(t0 + tt) * H);
+        uint2 xv[kWPer];
+#pragma unroll
+        for (int i = 0; i < kWPer; ++i) {
+          const int h4 = hb + st + i * kThreadsPerExpert;
+          xv[i] = h4 < H4 ? __ldg(xr + h4) : make_uint2(0u, 0u);
         }
+        float a = acc[tt];
+#pragma unroll
+        for (int i = 0; i < kWPer; ++i) {
+          a = fmaf(wv[i].x, bf16_lo(xv[i].x), a);
+          a = fmaf(wv[i].y, bf16_hi(xv[i].x), a);
+          a = fmaf(wv[i].z, bf16_lo(xv[i].y), a);
+          a = fmaf(wv[i].w, bf16_hi(xv[i].y), a);
+        }
+        acc[tt] = a;
       }
     }
   }
 #pragma unroll
   for (int i = 0; i < kTokPerCta; ++i) {
-    const float s = warp_sum(acc[i]);
-    if (lane == 0) red[sub][st / 32][i] = s;
+    if (i < nt) {
+      const float s2 = warp_sum(acc[i]);
+      if (lane == 0) red[sub][st / 32][i] = s2;
+    }
   }
   __syncthreads();
   if (tid < kExpertsPerCta * kTokPerCta) {
@@ -91,21 +116,22 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
     }
   }
 
-  // Arrival: the last CTA of this token block selects the experts.
-  __threadfence();
+  // Arrival: the last CTA of this token block selects the experts.  The
+  // writers make their logits visible device-wide, one thread per CTA
+  // counts the arrival, and the last arrival reads the others' logits.
+  if (tid < kExpertsPerCta * kTokPerCta) __threadfence();
   __syncthreads();
   if (tid == 0) {
     const unsigned prev = atomicAdd(&counters[blockIdx.y], 1u);
     is_last = (prev == gridDim.x - 1);
+    if (is_last) __threadfence();
   }
   __syncthreads();
   if (!is_last) return;
-  __threadfence();
 
   const int warp = tid / 32;
   if (warp < nt) {
     const int t = t0 + warp;
-    constexpr int kPer = kMaxE / 32;
     float v[kPer];
     bool bad = false;
 #pragma unroll
@@ -123,52 +149,49 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0)
       set_status(dev_status, QSM_DEV_NONFINITE);
+    // Order-preserving integer keys (larger float -> larger key), so each
+    // round is two warp reductions: the largest key, then the lowest expert
+    // index holding it (ties go to the lower index).
+    uint32_t key[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const uint32_t u = __float_as_uint(v[i]);
+      key[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+    }
     uint32_t taken = 0;  // bit i: candidate lane + 32 i already selected
-    float top = 0.f, sel_l[kMaxK];
-    int sel_e[kMaxK];
     for (int j = 0; j < k; ++j) {
-      // local best among this lane's untaken candidates (value desc, index asc)
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+      uint32_t bk = 0u, be = 0xffffffffu;  // best untaken (key desc, index asc)
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        const int ee = lane + 32 * i;
-        if (ee < E && !((taken >> i) & 1u)) {
-          if (v[i] > bv || (v[i] == bv && ee < be)) {
-            bv = v[i];
-            be = ee;
-          }
+        const uint32_t ee = lane + 32 * i;
+        if (ee < (uint32_t)E && !((taken >> i) & 1u) && (key[i] > bk || be == 0xffffffffu)) {
+          bk = key[i];
+          be = ee;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t emin = __reduce_min_sync(0xffffffffu, (bk == kmax) ? be : 0xffffffffu);
+      if ((emin & 31u) == (uint32_t)lane) taken |= 1u << (emin >> 5);
+      if (lane == 0) {
+        const uint32_t u = (kmax & 0x80000000u) ? (kmax & 0x7fffffffu) : ~kmax;
+        sel_l[warp][j] = __uint_as_float(u);
+        sel_e[warp][j] = (int)emin;
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (j == 0) top = bv;
-      sel_l[j < kMaxK ? j : 0] = bv;
-      sel_e[j < kMaxK ? j : 0] = be;
     }
-    float denom = 0.f;
+    __syncwarp();
+    const float top = sel_l[warp][0];
+    float part = 0.f;
     if (renormalize) {
-      for (int j = 0; j < k; ++j) denom += __expf(sel_l[j] - top);
+      if (lane < k) part = __expf(sel_l[warp][lane] - top);
     } else {
-      float part = 0.f;
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
         if (lane + 32 * i < E) part += __expf(v[i] - top);
-      denom = warp_sum(part);
     }
-    const float inv = 1.0f / denom;
-    for (int j = lane; j < k; j += 32) {
-      // sel_l / sel_e are uniform across the warp; index them by j
-      topk_idx[(size_t)t * k + j] = sel_e[j];
-      topk_w[(size_t)t * k + j] = __expf(sel_l[j] - top) * inv;
+    const float inv = 1.0f / warp_sum(part);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = sel_e[warp][lane];
+      topk_w[(size_t)t * k + lane] = __expf(sel_l[warp][lane] - top) * inv;
     }
   }
   if (tid == 0) counters[blockIdx.y] = 0u;  // re-arm for the next call
@@ -207,8 +230,14 @@ extern "C" qsm_status moe_route(const uint16_t* x, const float* w_router,
       static_cast<char*>(workspace) + counters_offset(T, E));
   dim3 grid((E + kExpertsPerCta - 1) / kExpertsPerCta,
             (T + kTokPerCta - 1) / kTokPerCta);
-  QSM_CUDA_TRY(launch_pdl(route_kernel, grid, dim3(kThreads), 0, stream, x,
-                          w_router, logit_bias, T, H, E, k, renormalize,
-                          topk_idx, topk_w, logits, counters, dev_status));
+  if (E <= 256)
+    QSM_CUDA_TRY(launch_pdl(route_kernel<8>, grid, dim3(kThreads), 0, stream, x,
+                            w_router, logit_bias, T, H, E, k, renormalize,
+                            topk_idx, topk_w, logits, counters, dev_status));
+  else
+    QSM_CUDA_TRY(launch_pdl(route_kernel<kMaxE / 32>, grid, dim3(kThreads), 0,
+                            stream, x, w_router, logit_bias, T, H, E, k,
+                            renormalize, topk_idx, topk_w, logits, counters,
+                            dev_status));
   return QSM_OK;
 }
