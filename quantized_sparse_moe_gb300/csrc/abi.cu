@@ -10,22 +10,29 @@ qsm_status decode_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
                              uint16_t* y, float* y32, void* ws,
                              int32_t* dev_status, cudaStream_t stream);
 size_t decode_ffn_workspace_bytes(const qsm_moe_layer* L, int T);
+bool prefill_supported(const qsm_moe_layer* L);
+size_t prefill_ffn_workspace_bytes(const qsm_moe_layer* L, int T);
+qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
+                              const float* topk_w, const qsm_grouping* g,
+                              uint16_t* y, float* y32, void* ws,
+                              int32_t* dev_status, cudaStream_t stream);
 
 namespace {
 
 std::atomic<int> g_force_path{0};
 
 constexpr int kDecodeTileRows = 8;
+constexpr int kPrefillTileRows = 128;
 constexpr int kDecodeMaxT = 128;   // d2 keeps a [T, 16] fp32 slab per warp
 constexpr int kDecodeAutoMaxT = 64;
 
-bool prefill_available() { return false; }
-
+// Path for T tokens: the decode kernels for few tokens, the tensor-core
+// grouped GEMMs for many (the test hook can force either where it applies).
 bool use_decode(int T) {
   const int mode = g_force_path.load();
   if (mode == 1) return T <= kDecodeMaxT;
-  if (mode == 2 && prefill_available()) return false;
-  return T <= kDecodeAutoMaxT || (!prefill_available() && T <= kDecodeMaxT);
+  if (mode == 2) return false;
+  return T <= kDecodeAutoMaxT;
 }
 
 // Shape checks of one quantized tensor (the "same type, same group size,
@@ -61,12 +68,14 @@ qsm_status check_layer(const qsm_moe_layer* L) {
 }  // namespace qsm
 
 extern "C" int32_t moe_ffn_tile_rows(int32_t T) {
-  return qsm::use_decode(T) ? qsm::kDecodeTileRows : qsm::kDecodeTileRows;
+  return qsm::use_decode(T) ? qsm::kDecodeTileRows : qsm::kPrefillTileRows;
 }
 
 extern "C" size_t moe_ffn_workspace_bytes(const qsm_moe_layer* L, int32_t T) {
   if (!L || T < 0 || qsm::check_layer(L) != QSM_OK) return 0;
-  return qsm::decode_ffn_workspace_bytes(L, T);
+  if (qsm::use_decode(T)) return qsm::decode_ffn_workspace_bytes(L, T);
+  if (!qsm::prefill_supported(L)) return 0;
+  return qsm::prefill_ffn_workspace_bytes(L, T);
 }
 
 extern "C" qsm_status moe_ffn_forward(const qsm_moe_layer* L,
@@ -93,12 +102,15 @@ extern "C" qsm_status moe_ffn_forward(const qsm_moe_layer* L,
   if (g->tile_rows != moe_ffn_tile_rows(T) ||
       g->max_tiles < moe_group_max_tiles(T, L->k, L->E, g->tile_rows))
     return QSM_ERR_INVALID_ARGUMENT;
+  const bool decode = use_decode(T);
+  if (!decode && !prefill_supported(L)) return QSM_ERR_UNSUPPORTED;
   if (workspace_bytes < moe_ffn_workspace_bytes(L, T))
     return QSM_ERR_WORKSPACE_TOO_SMALL;
-  if (use_decode(T))
+  if (decode)
     return decode_ffn_launch(L, x, T, topk_w, g, y, y_f32, workspace,
                              dev_status, stream);
-  return QSM_ERR_UNSUPPORTED;
+  return prefill_ffn_launch(L, x, T, topk_w, g, y, y_f32, workspace,
+                            dev_status, stream);
 }
 
 extern "C" const char* qsm_status_str(qsm_status s) {

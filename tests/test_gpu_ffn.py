@@ -124,3 +124,89 @@ def test_invalid_arguments_rejected(qsm):
     with pytest.raises(qsm.QSMError):
         qsm.moe_ffn_forward(L, x, fwd.topk_idx, fwd.topk_w, fwd.grouping,
                             workspace=small)
+
+
+# ------------------------------------------------------------------ prefill
+
+PREFILL_CASES = [65, 128, 200, 1000]
+
+
+@pytest.mark.parametrize("T", PREFILL_CASES)
+def test_qwen_q8_prefill(qsm, T):
+    # full-layer oracle on a token sample (every output of those tokens)
+    rng = np.random.default_rng(T)
+    toks = np.sort(rng.choice(T, min(T, 48), replace=False)).astype(np.int32)
+    _check(qsm, synth.QWEN, T, seed=2, tokens=toks)
+
+
+def test_tiny_layer_forced_prefill(qsm):
+    qsm.force_path("prefill")
+    try:
+        _check(qsm, synth.TINY, 4, seed=0)
+        _check(qsm, synth.TINY, 37, seed=1)
+    finally:
+        qsm.force_path("auto")
+
+
+@pytest.mark.parametrize("T", [1, 16, 64, 100])
+def test_cross_path_same_tokens(qsm, T):
+    """The decode kernels and the prefill kernels both meet the tolerance on
+    the same tokens, and agree with each other within it."""
+    Lg, q, wr, bias = layer(synth.QWEN, 0, None)
+    x = x_for(synth.QWEN, T, 77 + T, Lg, wr, bias)
+    outs = {}
+    for path in ("decode", "prefill"):
+        qsm.force_path(path)
+        try:
+            fwd = run(qsm, Lg, x)
+        finally:
+            qsm.force_path("auto")
+        assert fwd.dev_status.item() == 0
+        outs[path] = fwd.y_f32.cpu().numpy().astype(np.float64)
+    idx_o, w_o = oracle_route(x, wr, bias, synth.QWEN.k)
+    from _helpers import tol_metric
+    import oracle as orc
+    from _helpers import bits16
+    ref = orc.moe_layer(bits16(x), idx_o, w_o, *q)
+    for path, y32 in outs.items():
+        assert tol_metric(y32, ref) <= TOL, path
+    assert tol_metric(outs["decode"], outs["prefill"]) <= TOL
+
+
+def test_prefill_zipf_t4096_sampled(qsm):
+    """The prefill workload at full size: T=4096, Zipf-offset routing (many
+    empty experts, a few very large groups); all routing bit-exact, the
+    layer output checked on sampled tokens."""
+    shape = synth.QWEN
+    Lg, q, wr, bias = layer(shape, 3, "noise")
+    x = x_for(shape, 4096, 4096, Lg, wr, bias)
+    fwd = run(qsm, Lg, x)
+    assert fwd.dev_status.item() == 0
+    idx_o, w_o = oracle_route(x, wr, bias, shape.k)
+    assert np.array_equal(fwd.topk_idx.cpu().numpy(), idx_o)
+    counts = np.bincount(idx_o.ravel(), minlength=shape.E)
+    assert (counts == 0).sum() > 0          # some experts are empty
+    assert np.array_equal(fwd.grouping.counts.cpu().numpy(), counts)
+    # tokens that use the largest and the smallest non-empty groups, plus random
+    big = np.argmax(counts)
+    small = np.where(counts == counts[counts > 0].min())[0][0]
+    pick = {int(np.where((idx_o == big).any(1))[0][0]),
+            int(np.where((idx_o == small).any(1))[0][0])}
+    pick |= set(np.random.default_rng(1).choice(4096, 30, replace=False).tolist())
+    toks = np.array(sorted(pick), np.int32)
+    err, _ = check_layer_output(fwd.y, fwd.y_f32, x, idx_o, w_o, q, toks)
+    assert err <= TOL
+
+
+def test_prefill_repeat_is_stable(qsm):
+    """Two prefill calls in a row give results within one bf16 ulp (the
+    fp32 reduce-add order may differ)."""
+    Lg, _, wr, bias = layer(synth.QWEN, 0, None)
+    x = x_for(synth.QWEN, 300, 5, Lg, wr, bias).cuda()
+    fwd = qsm.MoEForward(qsm.Layer.from_synth(Lg), 300, want_f32=True)
+    fwd(x)
+    a = fwd.y_f32.clone()
+    fwd(x)
+    torch.cuda.synchronize()
+    rel = (a - fwd.y_f32).abs().max().item() / a.abs().max().item()
+    assert rel < 1e-5
