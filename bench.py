@@ -260,6 +260,14 @@ def run_ours(args, wl, rank, world):
         e2e_ms = t.item()
 
     achieved = ffn_bytes_per_layer / (ffn_ms / 1e3) / 1e9
+    # algorithmic FLOPs per layer: expert matmuls (k routed + shared per
+    # token, gate_up 2*2I*H + down 2*H*I) and the router (2*E*H per token)
+    sh = wl["shape"]
+    flops_layer = (2.0 * T * (sh.k + 1) * 3 * sh.H * sh.I + 2.0 * T * sh.E * sh.H)
+    _, tc_peak, _ = peaks()
+    t_hbm = step_bytes / (hbm * 1e9)
+    t_tc = flops_layer * nL / (tc_peak * 1e12)
+    bound = "tensor" if t_tc > t_hbm else "hbm"
     result = {
         "metric": "MoE-layer tokens/s",
         "value": value,
@@ -278,16 +286,25 @@ def run_ours(args, wl, rank, world):
                    "l2": "inputs larger than L2 (touched weights per step "
                          f"{step_bytes / 1e9:.2f} GB)"},
         "layer_roofline": {
-            "bound": "hbm", "touched_bytes_per_step": step_bytes,
-            "floor_ms": step_bytes / (hbm * 1e9) * 1e3,
-            "frac": step_bytes / (hbm * 1e9) / (ms / 1e3),
-            "peak_gbs": hbm, "peak_kind": peak_kind},
-        "roofline": {
+            "bound": bound, "touched_bytes_per_step": step_bytes,
+            "flops_per_step": flops_layer * nL,
+            "floor_ms": max(t_hbm, t_tc) * 1e3,
+            "hbm_frac": t_hbm / (ms / 1e3), "tensor_frac": t_tc / (ms / 1e3),
+            "frac": max(t_hbm, t_tc) / (ms / 1e3),
+            "peak_gbs": hbm, "peak_tflops": tc_peak, "peak_kind": peak_kind},
+        "roofline": ({
             "kernel": "moe_ffn_forward (d1 gate_up+SwiGLU, d2 down+combine)",
             "bound": "hbm", "achieved": achieved, "peak": hbm,
             "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
             "bytes_per_launch": ffn_bytes_per_layer,
-            "launch_ms": ffn_ms, "peak_kind": peak_kind},
+            "launch_ms": ffn_ms, "peak_kind": peak_kind} if T <= 64 else {
+            "kernel": "moe_ffn_forward (prep, gate_up GEMM, down GEMM, finalize)",
+            "bound": "tensor",
+            "achieved": (flops_layer - 2.0 * T * sh.E * sh.H) / (ffn_ms / 1e3) / 1e12,
+            "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": (flops_layer - 2.0 * T * sh.E * sh.H) / (ffn_ms / 1e3) / 1e12 / tc_peak,
+            "traffic": None, "flops_per_launch": flops_layer - 2.0 * T * sh.E * sh.H,
+            "launch_ms": ffn_ms, "peak_kind": peak_kind}),
         "e2e": {"value": world * T * nL / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": e2e_ms},

@@ -137,8 +137,9 @@ typedef struct {
 
 /* ----------------------------------------------------------------- router */
 
-/* Bytes of workspace moe_route needs for T tokens and E experts. */
-QSM_API size_t moe_route_workspace_bytes(int32_t T, int32_t E);
+/* Bytes of workspace moe_route needs for T tokens, hidden size H and E
+ * experts. */
+QSM_API size_t moe_route_workspace_bytes(int32_t T, int32_t H, int32_t E);
 
 /* Router: logits l[t,e] = sum_h x[t,h] * w_router[e,h] + logit_bias[e]
  * (fp32 accumulation), then per token the k largest logits (ties to the
@@ -150,8 +151,12 @@ QSM_API size_t moe_route_workspace_bytes(int32_t T, int32_t E);
  *   w_router   [E, H] fp32
  *   logit_bias [E] fp32 or NULL (added to the logits before selection)
  *   topk_idx   [T, k] int32 (out), topk_w [T, k] fp32 (out)
- *   workspace  >= moe_route_workspace_bytes(T, E) bytes.  It must hold
- *              zeros before its first use; every call leaves it zeroed.
+ *   workspace  >= moe_route_workspace_bytes(T, H, E) bytes.  It must hold
+ *              zeros before its first use; every call leaves the part that
+ *              must start at zero zeroed again.
+ * Few tokens run on CUDA cores (fp32 FMA); many tokens (T > 64, E a multiple
+ * of 16 up to 256, k <= 8) run one tcgen05 GEMM over an exact three-way
+ * bf16 split of w_router, which keeps fp32-accurate logits.
  * Requires H % 64 == 0, 1 <= k <= min(E, 32), E <= 1024, T >= 0.
  * A non-finite logit sets QSM_DEV_NONFINITE. */
 QSM_API qsm_status moe_route(const uint16_t* x, const float* w_router,

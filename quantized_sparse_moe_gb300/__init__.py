@@ -67,7 +67,7 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(_build.build())
             P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
             st = ctypes.c_int
-            L.moe_route_workspace_bytes.argtypes = [i32, i32]
+            L.moe_route_workspace_bytes.argtypes = [i32, i32, i32]
             L.moe_route_workspace_bytes.restype = sz
             L.moe_route.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P,
                                     sz, P, P]
@@ -159,8 +159,8 @@ class Layer:
 
 # ------------------------------------------------------------------ router
 
-def route_workspace_bytes(T: int, E: int) -> int:
-    return int(lib().moe_route_workspace_bytes(T, E))
+def route_workspace_bytes(T: int, H: int, E: int) -> int:
+    return int(lib().moe_route_workspace_bytes(T, H, E))
 
 
 def moe_route(x: torch.Tensor, w_router: torch.Tensor, k: int,
@@ -176,8 +176,8 @@ def moe_route(x: torch.Tensor, w_router: torch.Tensor, k: int,
     if topk_w is None:
         topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.zeros(route_workspace_bytes(T, E), dtype=torch.uint8,
-                                device=dev)
+        workspace = torch.zeros(route_workspace_bytes(T, H, E),
+                                dtype=torch.uint8, device=dev)
     dev_status = _status(dev_status, dev)
     _check(lib().moe_route(_p(_u16(x)), _p(w_router), _p(logit_bias), T, H, E,
                            k, int(bool(renormalize)), _p(topk_idx), _p(topk_w),
@@ -323,7 +323,7 @@ class MoEForward:
         i32 = dict(dtype=torch.int32, device=device)
         self.topk_idx = torch.empty((T, k), **i32)
         self.topk_w = torch.empty((T, k), dtype=torch.float32, device=device)
-        self.route_ws = torch.zeros(max(route_workspace_bytes(T, E), 256),
+        self.route_ws = torch.zeros(max(route_workspace_bytes(T, H, E), 256),
                                     dtype=torch.uint8, device=device)
         self.grouping = Grouping.empty(T, k, E, ffn_tile_rows(T), device)
         self.ffn_ws = torch.empty(max(ffn_workspace_bytes(layer, T), 256),

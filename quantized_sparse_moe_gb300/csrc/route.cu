@@ -24,9 +24,10 @@ constexpr int kTokPerCta = 8;
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 
-size_t counters_offset(int T, int E) {
-  size_t b = (size_t)T * E * sizeof(float);
-  return (b + 255) & ~size_t(255);
+// CUDA-core path workspace: [arrival counters][logits T x E fp32]
+size_t counters_bytes(int T) {
+  const size_t nblk = (size_t)(T + kTokPerCta - 1) / kTokPerCta;
+  return (nblk * 4 + 255) & ~size_t(255);
 }
 
 constexpr int kWPer = 4;  // float4 of the router row per thread and batch
@@ -200,10 +201,20 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
 }  // namespace
 }  // namespace qsm
 
-extern "C" size_t moe_route_workspace_bytes(int32_t T, int32_t E) {
-  if (T < 0 || E <= 0) return 0;
-  const size_t nblk = (size_t)(T + qsm::kTokPerCta - 1) / qsm::kTokPerCta;
-  return qsm::counters_offset(T, E) + ((nblk * 4 + 255) & ~size_t(255));
+namespace qsm {
+bool route_tc_supported(int T, int H, int E, int k);
+size_t route_tc_split_bytes(int H, int E);
+qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
+                           const float* logit_bias, int T, int H, int E, int k,
+                           int renormalize, int32_t* topk_idx, float* topk_w,
+                           void* split_buf, int32_t* dev_status,
+                           cudaStream_t stream);
+}  // namespace qsm
+
+extern "C" size_t moe_route_workspace_bytes(int32_t T, int32_t H, int32_t E) {
+  if (T < 0 || H <= 0 || E <= 0) return 0;
+  if (qsm::route_tc_supported(T, H, E, 1)) return qsm::route_tc_split_bytes(H, E);
+  return qsm::counters_bytes(T) + (((size_t)T * E * sizeof(float) + 255) & ~size_t(255));
 }
 
 extern "C" qsm_status moe_route(const uint16_t* x, const float* w_router,
@@ -223,11 +234,14 @@ extern "C" qsm_status moe_route(const uint16_t* x, const float* w_router,
       !aligned4(topk_idx) || !aligned4(topk_w) || !aligned4(dev_status) ||
       (logit_bias && !aligned4(logit_bias)))
     return QSM_ERR_INVALID_ARGUMENT;
-  if (workspace_bytes < moe_route_workspace_bytes(T, E))
+  if (workspace_bytes < moe_route_workspace_bytes(T, H, E))
     return QSM_ERR_WORKSPACE_TOO_SMALL;
-  float* logits = static_cast<float*>(workspace);
-  unsigned* counters = reinterpret_cast<unsigned*>(
-      static_cast<char*>(workspace) + counters_offset(T, E));
+  if (route_tc_supported(T, H, E, k))  // many tokens: tensor-core logits
+    return route_tc_launch(x, w_router, logit_bias, T, H, E, k, renormalize,
+                           topk_idx, topk_w, workspace, dev_status, stream);
+  unsigned* counters = static_cast<unsigned*>(workspace);
+  float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           counters_bytes(T));
   dim3 grid((E + kExpertsPerCta - 1) / kExpertsPerCta,
             (T + kTokPerCta - 1) / kTokPerCta);
   if (E <= 256)

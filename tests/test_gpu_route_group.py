@@ -20,6 +20,8 @@ ROUTE_CASES = [
     (synth.QWEN, 40, None, True),
     (synth.QWEN, 64, None, False),
     (synth.QWEN, 65, None, True),
+    (synth.TINY, 100, None, False),          # tensor-core router, E = 16
+    (synth.QWEN, 300, None, False),          # tensor-core router, full softmax
     (synth.QWEN, 1000, "noise", True),
     (synth.QWEN, 4096, "noise", True),
 ]
@@ -57,14 +59,14 @@ def test_route_workspace_is_rearmed(qsm):
     shape = synth.QWEN
     wr, bias = _router_only(shape, 7, None)
     x = synth.draw_x(24, shape.H, "cuda", 7)
-    ws = torch.zeros(qsm.route_workspace_bytes(24, shape.E), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.zeros(qsm.route_workspace_bytes(24, shape.H, shape.E),
+                     dtype=torch.uint8, device="cuda")
     a = qsm.moe_route(x, wr.cuda(), 8, workspace=ws)
     a = (a[0].clone(), a[1].clone())
     b = qsm.moe_route(x, wr.cuda(), 8, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
-    counters = ws[qsm.route_workspace_bytes(24, shape.E) - 256:]
+    counters = ws[:256]                     # the arrival counters come first
     assert int(counters.sum().item()) == 0
 
 
