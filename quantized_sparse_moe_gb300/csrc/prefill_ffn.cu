@@ -110,19 +110,22 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
   return false;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int RAW, int AST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_prefill_gemm(const __grid_constant__ Params p) {
-  constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per stage
+  constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per K step
   constexpr int A_BYTES = BM * BK * 2;         // fp16, 128B swizzle
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int C_BYTES = BM * BK;             // int8 codes
-  constexpr int STAGE = NA * A_BYTES + B_BYTES + NA * C_BYTES;
+  constexpr int A_STAGE = NA * A_BYTES;        // dequantised ring
+  constexpr int RAW_STAGE = B_BYTES + NA * C_BYTES;  // TMA ring
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[STAGES], ready_bar[STAGES],
-      empty_bar[STAGES], accf_bar[2], acce_bar[2];
+  unsigned char* aring = smem;                     // [AST][A_STAGE]
+  unsigned char* rring = smem + AST * A_STAGE;     // [RAW][RAW_STAGE]
+  __shared__ __align__(8) uint64_t raw_full[RAW], raw_empty[RAW], a_full[AST],
+      a_empty[AST], accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_tok[2][BN];
   __shared__ float s_w[2][BN];
@@ -130,10 +133,13 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&ready_bar[s], kDeqThreads);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < RAW; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kDeqThreads + 1);  // dequant threads + MMA commit
+    }
+    for (int s = 0; s < AST; ++s) {
+      mbar_init(&a_full[s], kDeqThreads);
+      mbar_init(&a_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], 1);
@@ -163,7 +169,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int s = 0, fill = 0;
+    int r = 0, f = 0;
     for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
@@ -186,33 +192,32 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       const uint32_t bbytes = gather ? (uint32_t)ti.n * (BK * 2) : (uint32_t)B_BYTES;
       for (int ks = 0; ks < ksteps; ++ks) {
         bool ok = true;
-        if (fill >= STAGES && lane == 0)
-          ok = wait_bar(&empty_bar[s], ((fill / STAGES) - 1) & 1, abort_p, p.status);
+        if (f >= RAW && lane == 0)
+          ok = wait_bar(&raw_empty[r], ((f / RAW) - 1) & 1, abort_p, p.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        unsigned char* st = smem + s * STAGE;
-        unsigned char* bdst = st + NA * A_BYTES;
+        unsigned char* bdst = rring + r * RAW_STAGE;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full_bar[s], NA * C_BYTES + bbytes);
+          mbar_arrive_expect_tx(&raw_full[r], NA * C_BYTES + bbytes);
 #pragma unroll
           for (int a = 0; a < NA; ++a)
-            tc::tma_load_2d(bdst + B_BYTES + a * C_BYTES, cm, ks * BK, arow[a], &full_bar[s]);
+            tc::tma_load_2d(bdst + B_BYTES + a * C_BYTES, cm, ks * BK, arow[a], &raw_full[r]);
           if (!gather)
             tc::tma_load_2d(bdst, MODE == kGateUp ? &p.bmap_tile : &p.bmap, ks * BK,
-                            brow, &full_bar[s]);
+                            brow, &raw_full[r]);
         }
         __syncwarp();
         if (gather && lane < ti.n / 4)
           tc::tma_gather4(bdst + lane * 4 * (BK * 2), &p.bmap, ks * BK, tr[0], tr[1],
-                          tr[2], tr[3], &full_bar[s]);
-        ++fill;
-        s = (s + 1 == STAGES) ? 0 : s + 1;
+                          tr[2], tr[3], &raw_full[r]);
+        ++f;
+        r = (r + 1 == RAW) ? 0 : r + 1;
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      int s = 0, fill = 0, j = 0;
+      int r = 0, a = 0, f = 0, j = 0;
       for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x, ++j) {
         const int tau = item / p.nsub;
         const TileInfo ti = tile_info(p, tau);
@@ -223,26 +228,27 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
         const uint32_t dbase = tmem + b * 256;
         bool ok = true;
         for (int ks = 0; ks < ksteps; ++ks) {
-          const uint32_t par = (fill / STAGES) & 1;
-          if (!wait_bar(&full_bar[s], par, abort_p, p.status) ||
-              !wait_bar(&ready_bar[s], par, abort_p, p.status)) {
+          if (!wait_bar(&raw_full[r], (f / RAW) & 1, abort_p, p.status) ||
+              !wait_bar(&a_full[a], (f / AST) & 1, abort_p, p.status)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          unsigned char* st = smem + s * STAGE;
-          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + NA * A_BYTES);
+          const uint32_t a0 = smem_u32(aring + a * A_STAGE);
+          const uint32_t b0 = smem_u32(rring + r * RAW_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
-            for (int a = 0; a < NA; ++a)
-              tc::mma_f16(dbase + a * 128, tc::sw128_desc(a0 + a * A_BYTES + kk * 32),
+            for (int m = 0; m < NA; ++m)
+              tc::mma_f16(dbase + m * 128, tc::sw128_desc(a0 + m * A_BYTES + kk * 32),
                           tc::sw128_desc(b0 + kk * 32), idesc,
                           (ks > 0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit(&empty_bar[s]);
-          ++fill;
-          s = (s + 1 == STAGES) ? 0 : s + 1;
+          tc::mma_commit(&raw_empty[r]);
+          tc::mma_commit(&a_empty[a]);
+          ++f;
+          r = (r + 1 == RAW) ? 0 : r + 1;
+          a = (a + 1 == AST) ? 0 : a + 1;
         }
         if (!ok) break;
         tc::mma_commit(&accf_bar[b]);
@@ -252,54 +258,73 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------- dequant
     const int d = threadIdx.x - 128;
-    const int a = MODE == kGateUp ? (d >> 7) : 0;
-    const int r = MODE == kGateUp ? (d & 127) : (d >> 1);
+    const int am = MODE == kGateUp ? (d >> 7) : 0;
+    const int rw = MODE == kGateUp ? (d & 127) : (d >> 1);
     const int half = MODE == kGateUp ? 0 : (d & 1);
     constexpr int kInChunks = MODE == kGateUp ? 4 : 2;  // 16 codes per chunk
-    int s = 0, fill = 0;
+    int r = 0, a = 0, f = 0;
     for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
       const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
-      const int row = ebase + (a ? p.I : 0) + sub * BM + r;
-      const __half* sc = (ti.e < 0 ? p.scales_sh : p.scales) + (size_t)row * (p.K / 32);
+      const int row = ebase + (am ? p.I : 0) + sub * BM + rw;
+      // this row's block scales: one 4-byte pair per K step (4-byte aligned
+      // for any K % 64 == 0), fetched one group of 8 K steps ahead
+      const uint32_t* sc = reinterpret_cast<const uint32_t*>(
+          (ti.e < 0 ? p.scales_sh : p.scales) + (size_t)row * (p.K / 32));
+      uint32_t nx[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) nx[jj] = jj < ksteps ? __ldg(sc + jj) : 0u;
       bool ok = true;
-      for (int ks = 0; ks < ksteps; ++ks) {
-        const uint32_t sc2 = __ldg(reinterpret_cast<const uint32_t*>(sc) + ks);
-        if (!wait_bar(&full_bar[s], (fill / STAGES) & 1, abort_p, p.status)) {
-          ok = false;
-          break;
+      for (int kg = 0; kg < ksteps && ok; kg += 8) {
+        uint32_t cur[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          cur[jj] = nx[jj];
+          nx[jj] = kg + 8 + jj < ksteps ? __ldg(sc + kg + 8 + jj) : 0u;
         }
-        unsigned char* st = smem + s * STAGE;
-        const unsigned char* codes = st + NA * A_BYTES + B_BYTES + a * C_BYTES + r * BK;
-        unsigned char* arow_s = st + a * A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-        for (int j = 0; j < kInChunks; ++j) {
-          // rotate the chunk order by row to spread shared-memory banks
-          const int ci = half * kInChunks + ((j + r) & (kInChunks - 1));
-          const uint4 v = *reinterpret_cast<const uint4*>(codes + ci * 16);
-          const uint32_t sbits = (ci < 2) ? (sc2 & 0xffffu) : (sc2 >> 16);
-          const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sbits));
-          uint32_t o[8];
-          s8x4_to_f16x2x2(v.x, o[0], o[1]);
-          s8x4_to_f16x2x2(v.y, o[2], o[3]);
-          s8x4_to_f16x2x2(v.z, o[4], o[5]);
-          s8x4_to_f16x2x2(v.w, o[6], o[7]);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            __half2 h = __hmul2(*reinterpret_cast<__half2*>(&o[t]), s2);
-            o[t] = *reinterpret_cast<uint32_t*>(&h);
+        for (int jj = 0; jj < 8; ++jj) {
+          if (kg + jj >= ksteps) break;
+          if (!wait_bar(&raw_full[r], (f / RAW) & 1, abort_p, p.status) ||
+              (f >= AST && !wait_bar(&a_empty[a], ((f / AST) - 1) & 1, abort_p, p.status))) {
+            ok = false;
+            break;
           }
-          const int oc0 = 2 * ci, oc1 = 2 * ci + 1;  // 16-byte output chunks
-          *reinterpret_cast<uint4*>(arow_s + ((oc0 ^ (r & 7)) << 4)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(arow_s + ((oc1 ^ (r & 7)) << 4)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
+          const uint32_t sc2 = cur[jj];
+          const unsigned char* codes = rring + r * RAW_STAGE + B_BYTES + am * C_BYTES + rw * BK;
+          unsigned char* arow_s = aring + a * A_STAGE + am * A_BYTES + (rw >> 3) * 1024 +
+                                  (rw & 7) * 128;
+#pragma unroll
+          for (int j = 0; j < kInChunks; ++j) {
+            // rotate the chunk order by row to spread shared-memory banks
+            const int ci = half * kInChunks + ((j + rw) & (kInChunks - 1));
+            const uint4 v = *reinterpret_cast<const uint4*>(codes + ci * 16);
+            const uint32_t sbits = (ci < 2) ? (sc2 & 0xffffu) : (sc2 >> 16);
+            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sbits));
+            uint32_t o[8];
+            s8x4_to_f16x2x2(v.x, o[0], o[1]);
+            s8x4_to_f16x2x2(v.y, o[2], o[3]);
+            s8x4_to_f16x2x2(v.z, o[4], o[5]);
+            s8x4_to_f16x2x2(v.w, o[6], o[7]);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              __half2 h = __hmul2(*reinterpret_cast<__half2*>(&o[t]), s2);
+              o[t] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            const int oc0 = 2 * ci, oc1 = 2 * ci + 1;  // 16-byte output chunks
+            *reinterpret_cast<uint4*>(arow_s + ((oc0 ^ (rw & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(arow_s + ((oc1 ^ (rw & 7)) << 4)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          tc::fence_async_smem();
+          tc::mbar_arrive(&a_full[a]);
+          tc::mbar_arrive(&raw_empty[r]);
+          ++f;
+          r = (r + 1 == RAW) ? 0 : r + 1;
+          a = (a + 1 == AST) ? 0 : a + 1;
         }
-        tc::fence_async_smem();
-        tc::mbar_arrive(&ready_bar[s]);
-        ++fill;
-        s = (s + 1 == STAGES) ? 0 : s + 1;
       }
       if (!ok) break;
     }
@@ -414,13 +439,15 @@ finalize_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y,
   }
 }
 
-constexpr int kGateUpStages = 3;
-constexpr int kDownStages = 5;
+// (TMA ring, dequantised ring) depths
+constexpr int kGateUpRaw = 4, kGateUpA = 2;
+constexpr int kDownRaw = 6, kDownA = 2;
 
-template <int MODE, int STAGES>
+template <int MODE, int RAW, int AST>
 constexpr size_t gemm_smem() {
-  return (size_t)STAGES * ((MODE == kGateUp ? 2 : 1) * (BM * BK * 2 + BM * BK) +
-                           BN * BK * 2) + 1024;
+  constexpr int NA = MODE == kGateUp ? 2 : 1;
+  return (size_t)AST * NA * BM * BK * 2 + (size_t)RAW * (BN * BK * 2 + NA * BM * BK) +
+         1024;
 }
 
 int sm_count() {
@@ -524,18 +551,16 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   p2.K = I;
   p2.nsub = H / BM;
 
-  constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpStages>();
-  constexpr size_t smem2 = gemm_smem<kDown, kDownStages>();
-  QSM_CUDA_TRY(cudaFuncSetAttribute(moe_prefill_gemm<kGateUp, kGateUpStages>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpRaw, kGateUpA>();
+  constexpr size_t smem2 = gemm_smem<kDown, kDownRaw, kDownA>();
+  auto* k1 = moe_prefill_gemm<kGateUp, kGateUpRaw, kGateUpA>;
+  auto* k2 = moe_prefill_gemm<kDown, kDownRaw, kDownA>;
+  QSM_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem1));
-  QSM_CUDA_TRY(cudaFuncSetAttribute(moe_prefill_gemm<kDown, kDownStages>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+  QSM_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem2));
-  QSM_CUDA_TRY(launch_pdl(moe_prefill_gemm<kGateUp, kGateUpStages>, dim3(nsm),
-                          dim3(kThreads), smem1, stream, p1));
-  QSM_CUDA_TRY(launch_pdl(moe_prefill_gemm<kDown, kDownStages>, dim3(nsm),
-                          dim3(kThreads), smem2, stream, p2));
+  QSM_CUDA_TRY(launch_pdl(k1, dim3(nsm), dim3(kThreads), smem1, stream, p1));
+  QSM_CUDA_TRY(launch_pdl(k2, dim3(nsm), dim3(kThreads), smem2, stream, p2));
   QSM_CUDA_TRY(launch_pdl(finalize_kernel, dim3(2 * nsm), dim3(256), 0, stream,
                           (const float*)yacc, y, y32, (size_t)T * H / 4));
   return QSM_OK;
