@@ -127,7 +127,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------- ours
 
-def build_layers(qsm, wl, device, seed):
+def build_layers(qsm, wl, device, seed, fuse=True):
     shape = wl["shape"]
     layers, xs, fwds, syn = [], [], [], []
     for l in range(wl["layers"]):
@@ -136,7 +136,7 @@ def build_layers(qsm, wl, device, seed):
         L = qsm.Layer.from_synth(Lg)
         layers.append(L)
         xs.append(synth.draw_x(wl["T"], shape.H, device, seed, l))
-        fwds.append(qsm.MoEForward(L, wl["T"], device))
+        fwds.append(qsm.MoEForward(L, wl["T"], device, fuse_route_group=fuse))
     return layers, xs, fwds, syn
 
 
@@ -158,7 +158,8 @@ def run_ours(args, wl, rank, world):
     import quantized_sparse_moe_gb300 as qsm
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    layers, xs, fwds, syn = build_layers(qsm, wl, dev, seed=0)
+    layers, xs, fwds, syn = build_layers(qsm, wl, dev, seed=0,
+                                         fuse=args.route_group == "fused")
     T, nL = wl["T"], wl["layers"]
     stream = torch.cuda.Stream(device=dev)
 
@@ -173,8 +174,10 @@ def run_ours(args, wl, rank, world):
     for f in fwds:
         assert f.dev_status.item() == 0, "device status set"
     graph = torch.cuda.CUDAGraph()
+    n0 = qsm.launch_count()
     with torch.cuda.graph(graph, stream=stream):
         step(torch.cuda.current_stream())
+    launches_per_step = qsm.launch_count() - n0
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
@@ -283,6 +286,7 @@ def run_ours(args, wl, rank, world):
         "data": "synthetic (seeded; random-init weights of the layer shapes)",
         "config": {"workload": wl["desc"], "tokens_per_layer": T,
                    "layers": nL, "parallelism": f"replicas x{world}",
+                   "route_group": args.route_group if T <= 8 else "separate",
                    "l2": "inputs larger than L2 (touched weights per step "
                          f"{step_bytes / 1e9:.2f} GB)"},
         "layer_roofline": {
@@ -308,7 +312,7 @@ def run_ours(args, wl, rank, world):
         "e2e": {"value": world * T * nL / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * nL * 4,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
     }
     return result, (syn, fwds, xs)
@@ -385,6 +389,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route-group", default="fused", choices=["fused", "separate"],
+                    help="for T <= 8: one fused route+group launch, or the two "
+                         "separate launches")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (profiling runs only)")
     args = ap.parse_args()

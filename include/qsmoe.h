@@ -182,6 +182,25 @@ QSM_API qsm_status moe_group_tokens(const int32_t* topk_idx, int32_t T, int32_t 
                             int32_t E, const qsm_grouping* g,
                             int32_t* dev_status, cudaStream_t stream);
 
+/* moe_route followed by moe_group_tokens in one launch, for a few tokens
+ * (decode): topk_idx, topk_w and every array of g are the same bits as the
+ * two calls give.  The router's CTAs split the experts as in moe_route; the
+ * CTA that finishes last selects the top k and then builds the grouping of
+ * the T*k assignments from the ids it holds in shared memory
+ * [Perplexity page, "Qwen creates three distinct workload shapes" and
+ * "Keeping expert routing on the GPU"].
+ *   workspace  as for moe_route (moe_route_workspace_bytes(T, H, E)).
+ * Supported: 1 <= T <= 8, H % 64 == 0, 1 <= E <= 256, 1 <= k <= min(E, 32);
+ * otherwise returns QSM_ERR_UNSUPPORTED and enqueues nothing (use the two
+ * calls).  Argument errors as for the two calls. */
+QSM_API qsm_status moe_route_group(const uint16_t* x, const float* w_router,
+                                   const float* logit_bias, int32_t T, int32_t H,
+                                   int32_t E, int32_t k, int32_t renormalize,
+                                   int32_t* topk_idx, float* topk_w,
+                                   const qsm_grouping* g, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status,
+                                   cudaStream_t stream);
+
 /* -------------------------------------------------------------------- FFN */
 
 /* The tile_rows moe_ffn_forward expects in its grouping for T tokens. */
@@ -259,6 +278,12 @@ QSM_API const char* qsm_status_str(qsm_status s);
 
 /* QSM_ABI_VERSION of the loaded library. */
 QSM_API int32_t qsm_abi_version(void);
+
+/* Kernels this library has launched since it was loaded, process-wide:
+ * every launch of every entry point counts once, including launches
+ * recorded into a CUDA graph under stream capture (a replay of the graph
+ * launches them again without counting).  Never fails. */
+QSM_API uint64_t qsm_launch_count(void);
 
 /* Test hook: 0 = choose the FFN path by T (default), 1 = always the decode
  * kernels, 2 = always the prefill kernels (when T allows).  Process-wide. */

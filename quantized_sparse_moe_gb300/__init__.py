@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
             L.moe_group_tokens.argtypes = [P, i32, i32, i32,
                                            ctypes.POINTER(GroupingC), P, P]
             L.moe_group_tokens.restype = st
+            L.moe_route_group.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P,
+                                          ctypes.POINTER(GroupingC), P, sz, P, P]
+            L.moe_route_group.restype = st
             L.moe_ffn_tile_rows.argtypes = [i32]
             L.moe_ffn_tile_rows.restype = i32
             L.moe_ffn_workspace_bytes.argtypes = [ctypes.POINTER(MoELayerC),
@@ -97,6 +100,8 @@ def lib() -> ctypes.CDLL:
             L.qsm_abi_version.restype = i32
             L.qsm_debug_force_path.argtypes = [i32]
             L.qsm_debug_force_path.restype = st
+            L.qsm_launch_count.argtypes = []
+            L.qsm_launch_count.restype = ctypes.c_uint64
             _lib = L
     return _lib
 
@@ -235,6 +240,36 @@ def moe_group_tokens(topk_idx: torch.Tensor, E: int, tile_rows: int,
     return out
 
 
+def moe_route_group(x: torch.Tensor, w_router: torch.Tensor, k: int,
+                    grouping: Grouping, logit_bias=None, renormalize=True,
+                    topk_idx=None, topk_w=None, workspace=None, dev_status=None,
+                    stream=None, raise_unsupported=True):
+    """Router + grouping in one launch (T <= 8).  Returns (topk_idx, topk_w),
+    or None when the shape is not supported and raise_unsupported is False.
+    The workspace is the router's (route_workspace_bytes, zero-initialised
+    once)."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(max(route_workspace_bytes(T, H, E), 256),
+                                dtype=torch.uint8, device=dev)
+    dev_status = _status(dev_status, dev)
+    gc = grouping.c
+    st = lib().moe_route_group(_p(_u16(x)), _p(w_router), _p(logit_bias), T, H, E,
+                               k, int(bool(renormalize)), _p(topk_idx),
+                               _p(topk_w), ctypes.byref(gc), _p(workspace),
+                               workspace.numel(), _p(dev_status), _stream(stream))
+    if st == 2 and not raise_unsupported:
+        return None
+    _check(st, "moe_route_group")
+    return topk_idx, topk_w
+
+
 # --------------------------------------------------------------------- FFN
 
 def ffn_tile_rows(T: int) -> int:
@@ -297,6 +332,11 @@ def force_path(mode: str | int) -> None:
     _check(lib().qsm_debug_force_path(int(m)), "qsm_debug_force_path")
 
 
+def launch_count() -> int:
+    """Kernels the library has launched (or recorded into a graph) so far."""
+    return int(lib().qsm_launch_count())
+
+
 # -------------------------------------------------------------------- GEMV
 
 def q8_gemv(x: torch.Tensor, q: torch.Tensor, d: torch.Tensor, y=None,
@@ -314,11 +354,13 @@ def q8_gemv(x: torch.Tensor, q: torch.Tensor, d: torch.Tensor, y=None,
 
 class MoEForward:
     """Buffers of one MoE layer call for T tokens, and the call sequence
-    route -> group -> FFN on one stream (nothing is read back)."""
+    route -> group -> FFN on one stream (nothing is read back).  For T <= 8
+    the route and group steps use the fused moe_route_group launch."""
 
     def __init__(self, layer: Layer, T: int, device="cuda", renormalize=True,
-                 want_f32=False):
+                 want_f32=False, fuse_route_group=True):
         self.layer, self.T, self.renormalize = layer, T, renormalize
+        self.fuse_route_group = fuse_route_group
         k, E, H = layer.k, layer.E, layer.H
         i32 = dict(dtype=torch.int32, device=device)
         self.topk_idx = torch.empty((T, k), **i32)
@@ -335,11 +377,19 @@ class MoEForward:
 
     def __call__(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         L = self.layer
-        moe_route(x, L.w_router, L.k, L.logit_bias, self.renormalize,
-                  self.topk_idx, self.topk_w, self.route_ws, self.dev_status,
-                  stream)
-        moe_group_tokens(self.topk_idx, L.E, self.grouping.tile_rows,
-                         self.grouping, self.dev_status, stream)
+        fused = None
+        if self.fuse_route_group and self.T <= 8:
+            fused = moe_route_group(x, L.w_router, L.k, self.grouping,
+                                    L.logit_bias, self.renormalize,
+                                    self.topk_idx, self.topk_w, self.route_ws,
+                                    self.dev_status, stream,
+                                    raise_unsupported=False)
+        if fused is None:
+            moe_route(x, L.w_router, L.k, L.logit_bias, self.renormalize,
+                      self.topk_idx, self.topk_w, self.route_ws,
+                      self.dev_status, stream)
+            moe_group_tokens(self.topk_idx, L.E, self.grouping.tile_rows,
+                             self.grouping, self.dev_status, stream)
         moe_ffn_forward(L, x, self.topk_idx, self.topk_w, self.grouping,
                         self.y, self.y_f32 if self.y_f32 is not None else False,
                         self.ffn_ws, self.dev_status, stream)

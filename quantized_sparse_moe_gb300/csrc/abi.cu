@@ -17,6 +17,8 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
                               uint16_t* y, float* y32, void* ws,
                               int32_t* dev_status, cudaStream_t stream);
 
+std::atomic<unsigned long long> g_launch_count{0};
+
 namespace {
 
 std::atomic<int> g_force_path{0};
@@ -125,6 +127,10 @@ extern "C" const char* qsm_status_str(qsm_status s) {
 }
 
 extern "C" int32_t qsm_abi_version(void) { return QSM_ABI_VERSION; }
+
+extern "C" uint64_t qsm_launch_count(void) {
+  return qsm::g_launch_count.load(std::memory_order_relaxed);
+}
 
 extern "C" qsm_status qsm_debug_force_path(int32_t mode) {
   if (mode < 0 || mode > 2) return QSM_ERR_INVALID_ARGUMENT;

@@ -6,6 +6,11 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+#include <unordered_set>
+#include <utility>
+
 #include "qsmoe.h"
 
 #define QSM_CUDA_TRY(expr)                      \
@@ -25,6 +30,22 @@ inline bool aligned4(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 3u) == 0;
 }
 
+// Every kernel runs with the largest shared-memory carveout, so CTAs of
+// consecutive (overlapping) launches can share an SM without waiting for it
+// to drain and change its L1 / shared-memory split.  Set once per kernel.
+inline void max_smem_carveout(const void* kernel) {
+  static std::mutex mu;
+  static std::unordered_set<const void*> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.insert(kernel).second)
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+}
+
+// Number of kernel launches this library has issued (or recorded into a
+// graph under capture), process-wide.  Read through qsm_launch_count().
+extern std::atomic<unsigned long long> g_launch_count;
+
 // Launch with programmatic dependent launch enabled: the kernel may start
 // while its predecessor on the stream drains; it must execute
 // pdl_wait() before touching anything the predecessor writes (or reads).
@@ -32,6 +53,7 @@ template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
                               size_t smem, cudaStream_t stream,
                               Args&&... args) {
+  max_smem_carveout(reinterpret_cast<const void*>(kernel));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -42,7 +64,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 // ---------------------------------------------------------- device helpers

@@ -12,6 +12,11 @@
 // The logits land in the workspace; the CTA that finishes last for a token
 // block (a per-block arrival counter, no waiting) selects the top k for
 // those tokens, one warp per token, and re-arms the counter to zero.
+//
+// With kGroup (one token block, E <= 256) that same last CTA also groups
+// the T*k assignments ("Keeping expert routing on the GPU": histogram,
+// prefix scan, stable scatter, block map) from the ids it holds in shared
+// memory, so routing plus grouping is one launch for decode batches.
 #include "qsm_common.cuh"
 
 namespace qsm {
@@ -32,17 +37,96 @@ size_t counters_bytes(int T) {
 
 constexpr int kWPer = 4;  // float4 of the router row per thread and batch
 
-template <int kPer>  // candidates per lane in the top-k: ceil(E / 32)
+// Grouping outputs of the fused variant (see qsm_grouping).
+struct GroupOut {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* tile_map;
+  int32_t* n_tiles;
+  int tile_rows;
+  int max_tiles;
+};
+
+// Groups the A = T*k assignments a = t*k + j whose experts sit in
+// sel_e[t][j]: thread e counts expert e, two block scans give the start
+// offsets and first block of every expert, and each thread scatters its
+// expert's assignments in increasing a (a stable sort by expert).  Needs
+// E <= blockDim.x == kThreads.
+__device__ void group_in_cta(const int (*sel_e)[kMaxK], int T, int k, int E,
+                             const GroupOut& g, int* s_cnt, int* s_blk) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int A = T * k, BM = g.tile_rows;
+  int cnt = 0;
+  if (tid < E)
+    for (int a = 0; a < A; ++a) cnt += (sel_e[a / k][a % k] == tid);
+  const int nb = (cnt + BM - 1) / BM;
+  int ic = cnt, ib = nb;  // inclusive warp scans
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int c2 = __shfl_up_sync(0xffffffffu, ic, o);
+    const int b2 = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ic += c2;
+      ib += b2;
+    }
+  }
+  if (lane == 31) {
+    s_cnt[warp] = ic;
+    s_blk[warp] = ib;
+  }
+  __syncthreads();
+  int cbase = 0, bbase = 0, ctot = 0, btot = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < kThreads / 32; ++w2) {
+    if (w2 < warp) {
+      cbase += s_cnt[w2];
+      bbase += s_blk[w2];
+    }
+    ctot += s_cnt[w2];
+    btot += s_blk[w2];
+  }
+  const int off = cbase + ic - cnt, b0 = bbase + ib - nb;
+  if (tid < E) {
+    g.counts[tid] = cnt;
+    g.offsets[tid] = off;
+    for (int m = 0; m < nb && b0 + m < g.max_tiles; ++m) {
+      g.tile_map[2 * (b0 + m)] = tid;
+      g.tile_map[2 * (b0 + m) + 1] = off + m * BM;
+    }
+    int pos = off;
+    for (int a = 0; a < A && pos < off + cnt; ++a) {
+      if (sel_e[a / k][a % k] == tid) {
+        g.perm[pos] = a;
+        g.inv_perm[a] = pos;
+        ++pos;
+      }
+    }
+  }
+  if (tid == 0) {
+    g.offsets[E] = ctot;
+    g.n_tiles[0] = btot < g.max_tiles ? btot : g.max_tiles;
+  }
+  for (int i = btot + tid; i < g.max_tiles; i += kThreads) {  // sentinels
+    g.tile_map[2 * i] = -1;
+    g.tile_map[2 * i + 1] = -1;
+  }
+}
+
+template <int kPer, bool kGroup>  // kPer: top-k candidates per lane, ceil(E/32)
 __global__ void __launch_bounds__(kThreads)
 route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
              const float* __restrict__ bias, int T, int H, int E, int k,
              int renormalize, int32_t* __restrict__ topk_idx,
              float* __restrict__ topk_w, float* __restrict__ logits,
-             unsigned int* __restrict__ counters, int32_t* dev_status) {
+             unsigned int* __restrict__ counters, int32_t* dev_status,
+             GroupOut gout) {
   __shared__ float red[kExpertsPerCta][kThreadsPerExpert / 32][kTokPerCta];
   __shared__ float sel_l[kThreads / 32][kMaxK];
   __shared__ int sel_e[kThreads / 32][kMaxK];
   __shared__ int is_last;
+  __shared__ int s_cnt[kThreads / 32], s_blk[kThreads / 32];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -196,6 +280,10 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
     }
   }
   if (tid == 0) counters[blockIdx.y] = 0u;  // re-arm for the next call
+  if constexpr (kGroup) {
+    __syncthreads();
+    group_in_cta(sel_e, nt, k, E, gout, s_cnt, s_blk);
+  }
 }
 
 }  // namespace
@@ -244,14 +332,49 @@ extern "C" qsm_status moe_route(const uint16_t* x, const float* w_router,
                                            counters_bytes(T));
   dim3 grid((E + kExpertsPerCta - 1) / kExpertsPerCta,
             (T + kTokPerCta - 1) / kTokPerCta);
+  const GroupOut none = {};
   if (E <= 256)
-    QSM_CUDA_TRY(launch_pdl(route_kernel<8>, grid, dim3(kThreads), 0, stream, x,
-                            w_router, logit_bias, T, H, E, k, renormalize,
-                            topk_idx, topk_w, logits, counters, dev_status));
+    QSM_CUDA_TRY(launch_pdl(route_kernel<8, false>, grid, dim3(kThreads), 0, stream,
+                            x, w_router, logit_bias, T, H, E, k, renormalize,
+                            topk_idx, topk_w, logits, counters, dev_status, none));
   else
-    QSM_CUDA_TRY(launch_pdl(route_kernel<kMaxE / 32>, grid, dim3(kThreads), 0,
+    QSM_CUDA_TRY(launch_pdl(route_kernel<kMaxE / 32, false>, grid, dim3(kThreads), 0,
                             stream, x, w_router, logit_bias, T, H, E, k,
                             renormalize, topk_idx, topk_w, logits, counters,
-                            dev_status));
+                            dev_status, none));
+  return QSM_OK;
+}
+
+extern "C" qsm_status moe_route_group(const uint16_t* x, const float* w_router,
+                                      const float* logit_bias, int32_t T,
+                                      int32_t H, int32_t E, int32_t k,
+                                      int32_t renormalize, int32_t* topk_idx,
+                                      float* topk_w, const qsm_grouping* g,
+                                      void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, cudaStream_t stream) {
+  using namespace qsm;
+  if (T < 1 || T > kTokPerCta || H <= 0 || H % 64 || E < 1 || E > kThreads ||
+      k < 1 || k > E || k > kMaxK)
+    return QSM_ERR_UNSUPPORTED;
+  if (!x || !w_router || !topk_idx || !topk_w || !workspace || !dev_status || !g ||
+      !g->counts || !g->offsets || !g->perm || !g->inv_perm || !g->tile_map ||
+      !g->n_tiles || g->tile_rows < 1 ||
+      g->max_tiles < moe_group_max_tiles(T, k, E, g->tile_rows))
+    return QSM_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace) ||
+      !aligned4(topk_idx) || !aligned4(topk_w) || !aligned4(dev_status) ||
+      (logit_bias && !aligned4(logit_bias)))
+    return QSM_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < moe_route_workspace_bytes(T, H, E))
+    return QSM_ERR_WORKSPACE_TOO_SMALL;
+  unsigned* counters = static_cast<unsigned*>(workspace);
+  float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           counters_bytes(T));
+  const GroupOut gout = {g->counts, g->offsets, g->perm, g->inv_perm,
+                         g->tile_map, g->n_tiles, g->tile_rows, g->max_tiles};
+  const dim3 grid((E + kExpertsPerCta - 1) / kExpertsPerCta, 1);
+  QSM_CUDA_TRY(launch_pdl(route_kernel<8, true>, grid, dim3(kThreads), 0, stream, x,
+                          w_router, logit_bias, T, H, E, k, renormalize, topk_idx,
+                          topk_w, logits, counters, dev_status, gout));
   return QSM_OK;
 }

@@ -120,3 +120,74 @@ def test_group_flags_bad_expert_id(qsm):
     valid = idx.ravel().copy()
     ok = (valid >= 0) & (valid < E)
     assert int(g.counts.sum().item()) == ok.sum()
+
+
+@pytest.mark.parametrize("shape,T,zipf,renorm", [
+    (synth.QWEN, 1, None, True), (synth.QWEN, 2, None, True),
+    (synth.QWEN, 3, "noise", True), (synth.QWEN, 8, None, False),
+    (synth.TINY, 4, None, True), (synth.TINY, 8, None, False)])
+def test_fused_route_group_matches_separate_calls(qsm, shape, T, zipf, renorm):
+    """moe_route_group gives the routing and grouping of moe_route +
+    moe_group_tokens bit for bit, and the oracle's routing and grouping."""
+    seed = 300 + T
+    wr, bias = _router_only(shape, seed, zipf)
+    L = synth.MoELayer(shape, wr, bias, None, None, None, None)
+    from _helpers import tie_free_x
+    x = tie_free_x(L, T, seed=seed).cuda()
+    wrc, bc = wr.cuda(), None if bias is None else bias.cuda()
+    BM = 8
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g1 = qsm.Grouping.empty(T, shape.k, shape.E, BM, "cuda")
+    i1, w1 = qsm.moe_route_group(x, wrc, shape.k, g1, bc, renorm, dev_status=st)
+    i2, w2 = qsm.moe_route(x, wrc, shape.k, bc, renorm, dev_status=st)
+    g2 = qsm.moe_group_tokens(i2, shape.E, BM, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(i1, i2)
+    assert torch.equal(w1, w2)
+    for name in ("counts", "offsets", "perm", "inv_perm", "n_tiles"):
+        assert torch.equal(getattr(g1, name), getattr(g2, name)), name
+    nt = int(g1.n_tiles.item())
+    assert torch.equal(g1.tile_map[:2 * nt], g2.tile_map[:2 * nt])
+    idx_o, w_o = oracle_route(x.cpu(), wr, bias, shape.k, renorm)
+    assert np.array_equal(i1.cpu().numpy(), idx_o)
+    np.testing.assert_allclose(w1.cpu().numpy(), w_o, rtol=0, atol=TOPK_W_ATOL)
+    _check_grouping(g1, idx_o, shape.E, BM)
+
+
+def test_fused_route_group_rejects_unsupported(qsm):
+    shape = synth.QWEN
+    x = synth.draw_x(9, shape.H, "cuda", 1)
+    g = qsm.Grouping.empty(9, shape.k, shape.E, 8, "cuda")
+    assert qsm.moe_route_group(x, synth.draw_router(shape.E, shape.H, "cuda", 1),
+                               shape.k, g, raise_unsupported=False) is None
+    x = synth.draw_x(2, shape.H, "cuda", 1)            # E > 256
+    g = qsm.Grouping.empty(2, shape.k, 512, 8, "cuda")
+    assert qsm.moe_route_group(x, synth.draw_router(512, shape.H, "cuda", 1),
+                               shape.k, g, raise_unsupported=False) is None
+
+
+def test_fused_route_group_repeat_and_bias(qsm):
+    """Back-to-back calls on one workspace (the arrival counter re-arms) with
+    a logit bias that sends several tokens to the same experts, so groups
+    hold more than one row and span blocks of 2 rows."""
+    shape = synth.QWEN
+    T, BM = 8, 2
+    wr = synth.draw_router(shape.E, shape.H, "cpu", 11)
+    bias = torch.zeros(shape.E)
+    bias[[3, 17, 200]] = torch.tensor([40.0, 60.0, 80.0])
+    from _helpers import tie_free_x
+    x = tie_free_x(synth.MoELayer(shape, wr, bias, None, None, None, None), T, seed=11)
+    ws = torch.zeros(max(qsm.route_workspace_bytes(T, shape.H, shape.E), 256),
+                     dtype=torch.uint8, device="cuda")
+    g = qsm.Grouping.empty(T, shape.k, shape.E, BM, "cuda")
+    for _ in range(2):
+        i1, w1 = qsm.moe_route_group(x.cuda(), wr.cuda(), shape.k, g, bias.cuda(),
+                                     True, workspace=ws)
+    torch.cuda.synchronize()
+    idx_o, w_o = oracle_route(x, wr, bias, shape.k, True)
+    assert (idx_o[:, :3] == np.array([200, 17, 3])).all()
+    assert np.array_equal(i1.cpu().numpy(), idx_o)
+    np.testing.assert_allclose(w1.cpu().numpy(), w_o, rtol=0, atol=TOPK_W_ATOL)
+    _check_grouping(g, idx_o, shape.E, BM)
+    assert int(ws[:256].sum().item()) == 0
