@@ -11,27 +11,36 @@
 // one pass over the fused [gate; up] weight.
 //
 // Launch sequence (stream ordered, programmatic dependent launch):
-//   prep      x -> fp16 copy (exact for the bf16 inputs), zero the fp32
-//             output accumulator
+//   prep      the token operand of gate_up as one fp16 matrix (exact for
+//             the bf16 inputs): the routed rows in grouped order (sorted
+//             row r holds the token of assignment perm[r]), then the T
+//             tokens in order for the shared expert; zero the fp32 output
+//             accumulator
 //   gate_up   per work item (block of <= 128 token rows of one expert,
 //             128 intermediate indices): D_gate, D_up (128 x N fp32 each, in
 //             tensor memory) += W_gate/up tile x token rows; epilogue
 //             h = silu(gate) * up, stored fp16 (scaled by 1/16) per sorted row
 //   down      per work item (same token block, 128 output rows):
-//             D (128 x N) = W_down tile x h rows; epilogue
-//             y_acc[token] += routing weight * D (fp32 reduce-add)
+//             D (128 token rows x 128) = h rows x W_down tile^T; epilogue
+//             y_acc[token] += routing weight * D row (16-byte fp32
+//             reduce-adds, one token per thread)
 //   finalize  y = bf16(y_acc) (and the fp32 copy)
 //
 // Roles in a persistent CTA (one per SM, 16 warps):
-//   warp 0       TMA producer: int8 code tiles (2D tensor map) and the token
-//                rows (tile::gather4 from the fp16 x copy, or 2D tiles of h)
+//   warp 0       TMA producer of the int8 code tiles (2D tensor map)
 //   warp 1       allocates tensor memory; lane 0 issues the MMAs
+//   warp 2       TMA producer of the token-row tiles: 2D boxes of the
+//                grouped fp16 x (gate_up) or of h (down), 128 rows or a
+//                64/32/16-row decomposition of a short tile's rows
 //   warps 4-11   dequantise the code tiles: fp16(code * block scale) written
 //                in the 128-byte-swizzled K-major layout the MMA reads
 //   warps 12-15  epilogue, one warp per quarter of the tensor-memory lanes
-// A ring of shared-memory stages (mbarriers: full / dequantised / empty)
-// connects producer, dequant and MMA; two accumulator buffers in tensor
-// memory (mbarriers: full / empty) connect MMA and epilogue.
+// Three shared-memory rings, each with full / empty mbarriers: code tiles
+// (freed as soon as the dequantising warps have read them), token tiles
+// (freed by the MMA commit) and dequantised weight tiles (freed by the MMA
+// commit).  Keeping the rings apart lets each run as many stages ahead as
+// its own latency needs.  Two accumulator buffers in tensor memory
+// (mbarriers: full / empty) connect MMA and epilogue.
 //
 // Precision: weights are fp16(code * scale) (relative rounding 2^-11),
 // tokens are exact; products are accumulated in fp32.
@@ -53,9 +62,8 @@ enum { kGateUp = 1, kDown = 2 };
 struct Params {
   CUtensorMap codes;      // routed experts' codes [E*R, K] u8, box {64, 128}
   CUtensorMap codes_sh;   // shared expert's codes [R, K] u8, box {64, 128}
-  CUtensorMap bmap;       // gate_up: x16 [T, H] box {64, 1} (gather4)
-                          // down:    h [rows, I] box {64, 128}
-  CUtensorMap bmap_tile;  // gate_up: x16 [T, H] box {64, 128} (shared tiles)
+  CUtensorMap bmap[4];    // token rows [T*k + T, K] fp16 (gate_up: grouped
+                          // x; down: h), boxes {64, 128 / 64 / 32 / 16}
   const __half* scales;   // [E*R, K/32]
   const __half* scales_sh;
   int R, K;               // rows per expert and reduction length
@@ -110,7 +118,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
   return false;
 }
 
-template <int MODE, int RAW, int AST>
+// y[0..3] += v0..v3 in one 16-byte reduction (16-byte aligned address).
+__device__ __forceinline__ void red_add_v4(float* y, float v0, float v1, float v2,
+                                           float v3) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(y), "f"(v0),
+               "f"(v1), "f"(v2), "f"(v3)
+               : "memory");
+}
+
+template <int MODE, int CR, int BR, int AST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_prefill_gemm(const __grid_constant__ Params p) {
   constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per K step
@@ -118,24 +134,27 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int C_BYTES = BM * BK;             // int8 codes
   constexpr int A_STAGE = NA * A_BYTES;        // dequantised ring
-  constexpr int RAW_STAGE = B_BYTES + NA * C_BYTES;  // TMA ring
+  constexpr int C_STAGE = NA * C_BYTES;        // code ring
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* aring = smem;                     // [AST][A_STAGE]
-  unsigned char* rring = smem + AST * A_STAGE;     // [RAW][RAW_STAGE]
-  __shared__ __align__(8) uint64_t raw_full[RAW], raw_empty[RAW], a_full[AST],
-      a_empty[AST], accf_bar[2], acce_bar[2];
+  unsigned char* bring = aring + AST * A_STAGE;    // [BR][B_BYTES]
+  unsigned char* cring = bring + BR * B_BYTES;     // [CR][C_STAGE]
+  __shared__ __align__(8) uint64_t c_full[CR], c_empty[CR], b_full[BR], b_empty[BR],
+      a_full[AST], a_empty[AST], accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_base;
-  __shared__ int s_tok[2][BN];
-  __shared__ float s_w[2][BN];
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RAW; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kDeqThreads + 1);  // dequant threads + MMA commit
+    for (int s = 0; s < CR; ++s) {
+      mbar_init(&c_full[s], 1);
+      mbar_init(&c_empty[s], kDeqThreads);
+    }
+    for (int s = 0; s < BR; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);  // MMA commit
     }
     for (int s = 0; s < AST; ++s) {
       mbar_init(&a_full[s], kDeqThreads);
@@ -151,8 +170,8 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   if (warp == 0 && lane == 0) {
     tc::prefetch_map(&p.codes);
     tc::prefetch_map(&p.codes_sh);
-    tc::prefetch_map(&p.bmap);
-    if (MODE == kGateUp) tc::prefetch_map(&p.bmap_tile);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) tc::prefetch_map(&p.bmap[m]);
   }
   if (warp == 1) tc::tmem_alloc(&tmem_base, 512);
   tc::tc_fence_before();
@@ -168,90 +187,120 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   volatile int* abort_p = &abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    int r = 0, f = 0;
-    for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
-      const int tau = item / p.nsub, sub = item - tau * p.nsub;
-      const TileInfo ti = tile_info(p, tau);
-      const bool gather = MODE == kGateUp && ti.e >= 0;
-      int tr[4] = {0, 0, 0, 0};
-      if (gather) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rr = min(4 * lane + j, ti.cnt - 1);
-          tr[j] = __ldcg(p.perm + ti.row0 + rr) / p.k;
-        }
-      }
-      const CUtensorMap* cm = ti.e < 0 ? &p.codes_sh : &p.codes;
-      const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
-      int arow[2];
-      arow[0] = ebase + sub * BM;
-      arow[1] = ebase + p.I + sub * BM;  // gate_up: the up rows
-      const int brow = MODE == kGateUp ? ti.row0
-                                       : (ti.e < 0 ? p.T * p.k + ti.row0 : ti.row0);
-      const uint32_t bbytes = gather ? (uint32_t)ti.n * (BK * 2) : (uint32_t)B_BYTES;
-      for (int ks = 0; ks < ksteps; ++ks) {
+    // ------------------------------------------------- producer: code tiles
+    if (lane == 0) {
+      int c = 0;
+      uint32_t f = 0;
+      for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
+        const int tau = item / p.nsub, sub = item - tau * p.nsub;
+        const TileInfo ti = tile_info(p, tau);
+        const CUtensorMap* cm = ti.e < 0 ? &p.codes_sh : &p.codes;
+        const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
+        int arow[2];
+        arow[0] = ebase + sub * BM;
+        arow[1] = ebase + p.I + sub * BM;  // gate_up: the up rows
         bool ok = true;
-        if (f >= RAW && lane == 0)
-          ok = wait_bar(&raw_empty[r], ((f / RAW) - 1) & 1, abort_p, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        unsigned char* bdst = rring + r * RAW_STAGE;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&raw_full[r], NA * C_BYTES + bbytes);
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (f >= CR && !wait_bar(&c_empty[c], ((f / CR) - 1) & 1, abort_p, p.status)) {
+            ok = false;
+            break;
+          }
+          unsigned char* cdst = cring + c * C_STAGE;
+          mbar_arrive_expect_tx(&c_full[c], C_STAGE);
 #pragma unroll
           for (int a = 0; a < NA; ++a)
-            tc::tma_load_2d(bdst + B_BYTES + a * C_BYTES, cm, ks * BK, arow[a], &raw_full[r]);
-          if (!gather)
-            tc::tma_load_2d(bdst, MODE == kGateUp ? &p.bmap_tile : &p.bmap, ks * BK,
-                            brow, &raw_full[r]);
+            tc::tma_load_2d(cdst + a * C_BYTES, cm, ks * BK, arow[a], &c_full[c]);
+          ++f;
+          c = (c + 1 == CR) ? 0 : c + 1;
         }
-        __syncwarp();
-        if (gather && lane < ti.n / 4)
-          tc::tma_gather4(bdst + lane * 4 * (BK * 2), &p.bmap, ks * BK, tr[0], tr[1],
-                          tr[2], tr[3], &raw_full[r]);
-        ++f;
-        r = (r + 1 == RAW) ? 0 : r + 1;
+        if (!ok) break;
       }
     }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------ producer: token tiles
+    if (lane == 0) {
+      int b = 0;
+      uint32_t f = 0;
+      for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
+        const int tau = item / p.nsub;
+        const TileInfo ti = tile_info(p, tau);
+        const int brow = (ti.e < 0 ? p.T * p.k : 0) + ti.row0;
+        bool ok = true;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (f >= BR && !wait_bar(&b_empty[b], ((f / BR) - 1) & 1, abort_p, p.status)) {
+            ok = false;
+            break;
+          }
+          unsigned char* bdst = bring + b * B_BYTES;
+          mbar_arrive_expect_tx(&b_full[b], (uint32_t)ti.n * (BK * 2));
+          if (ti.n == BN) {
+            tc::tma_load_2d(bdst, &p.bmap[0], ks * BK, brow, &b_full[b]);
+          } else {  // n = 16 * (4a + 2b + c): boxes of 64, 32 and 16 rows
+            int r0 = 0;
+#pragma unroll
+            for (int m = 1; m < 4; ++m) {
+              const int rows = BN >> m;
+              if (ti.n & rows) {
+                tc::tma_load_2d(bdst + r0 * (BK * 2), &p.bmap[m], ks * BK, brow + r0,
+                                &b_full[b]);
+                r0 += rows;
+              }
+            }
+          }
+          ++f;
+          b = (b + 1 == BR) ? 0 : b + 1;
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      int r = 0, a = 0, f = 0, j = 0;
+      int b = 0, a = 0, j = 0;
+      uint32_t f = 0;
       for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x, ++j) {
         const int tau = item / p.nsub;
         const TileInfo ti = tile_info(p, tau);
-        const int b = j & 1;
-        if (j >= 2 && !wait_bar(&acce_bar[b], ((j >> 1) - 1) & 1, abort_p, p.status)) break;
+        const int ab = j & 1;  // accumulator buffer
+        if (j >= 2 && !wait_bar(&acce_bar[ab], ((j >> 1) - 1) & 1, abort_p, p.status)) break;
         tc::tc_fence_after();
-        const uint32_t idesc = tc::idesc_f16_m128(ti.n);
-        const uint32_t dbase = tmem + b * 256;
+        // gate_up: D[weight row, token] (N = the tile's rows rounded up to
+        // 16); down: D[token, output row] (M = 128 token rows, N = 128)
+        const uint32_t idesc = tc::idesc_f16_m128(MODE == kGateUp ? ti.n : BM);
+        const uint32_t dbase = tmem + ab * 256;
         bool ok = true;
         for (int ks = 0; ks < ksteps; ++ks) {
-          if (!wait_bar(&raw_full[r], (f / RAW) & 1, abort_p, p.status) ||
+          if (!wait_bar(&b_full[b], (f / BR) & 1, abort_p, p.status) ||
               !wait_bar(&a_full[a], (f / AST) & 1, abort_p, p.status)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
           const uint32_t a0 = smem_u32(aring + a * A_STAGE);
-          const uint32_t b0 = smem_u32(rring + r * RAW_STAGE);
+          const uint32_t b0 = smem_u32(bring + b * B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (MODE == kGateUp) {
 #pragma unroll
-            for (int m = 0; m < NA; ++m)
-              tc::mma_f16(dbase + m * 128, tc::sw128_desc(a0 + m * A_BYTES + kk * 32),
-                          tc::sw128_desc(b0 + kk * 32), idesc,
-                          (ks > 0 || kk > 0) ? 1u : 0u);
+              for (int m = 0; m < NA; ++m)
+                tc::mma_f16(dbase + m * 128, tc::sw128_desc(a0 + m * A_BYTES + kk * 32),
+                            tc::sw128_desc(b0 + kk * 32), idesc,
+                            (ks > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              tc::mma_f16(dbase, tc::sw128_desc(b0 + kk * 32), tc::sw128_desc(a0 + kk * 32),
+                          idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            }
           }
-          tc::mma_commit(&raw_empty[r]);
+          tc::mma_commit(&b_empty[b]);
           tc::mma_commit(&a_empty[a]);
           ++f;
-          r = (r + 1 == RAW) ? 0 : r + 1;
+          b = (b + 1 == BR) ? 0 : b + 1;
           a = (a + 1 == AST) ? 0 : a + 1;
         }
         if (!ok) break;
-        tc::mma_commit(&accf_bar[b]);
+        tc::mma_commit(&accf_bar[ab]);
       }
     }
     __syncwarp();
@@ -262,7 +311,8 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
     const int rw = MODE == kGateUp ? (d & 127) : (d >> 1);
     const int half = MODE == kGateUp ? 0 : (d & 1);
     constexpr int kInChunks = MODE == kGateUp ? 4 : 2;  // 16 codes per chunk
-    int r = 0, a = 0, f = 0;
+    int c = 0, a = 0;
+    uint32_t f = 0;
     for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
@@ -286,13 +336,13 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           if (kg + jj >= ksteps) break;
-          if (!wait_bar(&raw_full[r], (f / RAW) & 1, abort_p, p.status) ||
+          if (!wait_bar(&c_full[c], (f / CR) & 1, abort_p, p.status) ||
               (f >= AST && !wait_bar(&a_empty[a], ((f / AST) - 1) & 1, abort_p, p.status))) {
             ok = false;
             break;
           }
           const uint32_t sc2 = cur[jj];
-          const unsigned char* codes = rring + r * RAW_STAGE + B_BYTES + am * C_BYTES + rw * BK;
+          const unsigned char* codes = cring + c * C_STAGE + am * C_BYTES + rw * BK;
           unsigned char* arow_s = aring + a * A_STAGE + am * A_BYTES + (rw >> 3) * 1024 +
                                   (rw & 7) * 128;
 #pragma unroll
@@ -318,11 +368,11 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
             *reinterpret_cast<uint4*>(arow_s + ((oc1 ^ (rw & 7)) << 4)) =
                 make_uint4(o[4], o[5], o[6], o[7]);
           }
+          tc::mbar_arrive(&c_empty[c]);
           tc::fence_async_smem();
           tc::mbar_arrive(&a_full[a]);
-          tc::mbar_arrive(&raw_empty[r]);
           ++f;
-          r = (r + 1 == RAW) ? 0 : r + 1;
+          c = (c + 1 == CR) ? 0 : c + 1;
           a = (a + 1 == AST) ? 0 : a + 1;
         }
       }
@@ -338,18 +388,18 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
       const int b = j & 1;
-      if (MODE == kDown) {
-        if (et < ti.cnt) {
-          if (ti.e < 0) {
-            s_tok[b][et] = ti.row0 + et;
-            s_w[b][et] = kHScaleInv;
-          } else {
-            const int asg = __ldcg(p.perm + ti.row0 + et);
-            s_tok[b][et] = asg / p.k;
-            s_w[b][et] = __ldcg(p.topk_w + asg) * kHScaleInv;
-          }
+      // down: this thread's token row of the tile, its token and weight
+      int tok = -1;
+      float wt = 0.f;
+      if (MODE == kDown && et < ti.cnt) {
+        if (ti.e < 0) {
+          tok = ti.row0 + et;
+          wt = kHScaleInv;
+        } else {
+          const int asg = __ldcg(p.perm + ti.row0 + et);
+          tok = asg / p.k;
+          wt = __ldcg(p.topk_w + asg) * kHScaleInv;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
       }
       if (!wait_bar(&accf_bar[b], (j >> 1) & 1, abort_p, p.status)) break;
       tc::tc_fence_after();
@@ -372,21 +422,21 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
           }
         }
       } else {
-        const int n = sub * BM + 32 * q4 + lane;  // output row
-        for (int c0 = 0; c0 < ti.n; c0 += 16) {
+        // 16 consecutive output rows per load: four 16-byte reduce-adds
+        float* dst = p.yacc + (size_t)(tok < 0 ? 0 : tok) * p.H + sub * BM;
+        for (int c0 = 0; c0 < BM; c0 += 16) {
           float dv[16];
           tc::tmem_ld16(taddr + c0, dv);
+          if (tok >= 0) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = c0 + c;
-            if (col < ti.cnt)
-              atomicAdd(p.yacc + (size_t)s_tok[b][col] * p.H + n, s_w[b][col] * dv[c]);
+            for (int v = 0; v < 4; ++v)
+              red_add_v4(dst + c0 + 4 * v, wt * dv[4 * v], wt * dv[4 * v + 1],
+                         wt * dv[4 * v + 2], wt * dv[4 * v + 3]);
           }
         }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&acce_bar[b]);
-      if (MODE == kDown) asm volatile("bar.sync 1, 128;" ::: "memory");
     }
     if (bad) set_status(p.status, QSM_DEV_FP16_RANGE);
   }
@@ -397,27 +447,56 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
-// x (bf16) -> fp16 copy; zero the fp32 output accumulator.
+// The token operand of gate_up, fp16 [A + T, H] with A = T*k: row r < A
+// holds the token of assignment perm[r] (zero if that assignment has no
+// valid expert), row A + t holds token t.  One warp per row, its 16-byte
+// chunks loaded four at a time before they are converted and stored.  Also
+// zeroes the fp32 output accumulator.
 __global__ void __launch_bounds__(256)
-prep_kernel(const uint16_t* __restrict__ x, __half* __restrict__ x16,
-            float* __restrict__ yacc, size_t n8, int32_t* status) {
+prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int T,
+            int k, int H, __half* __restrict__ xall, float* __restrict__ yacc,
+            int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   bool bad = false;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
-    const uint4 h = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
-                               bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-    const uint32_t* hw = reinterpret_cast<const uint32_t*>(&h);
+  const int A = T * k, rows = A + T;
+  const int cpr = H / 8;  // 16-byte chunks per row
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    int t = r - A;
+    if (r < A) {
+      const int a = __ldcg(perm + r);
+      t = a >= 0 ? a / k : -1;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t < 0 ? 0 : t) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xall + (size_t)r * H);
+    for (int c0 = lane; c0 < cpr; c0 += 4 * 32) {
+      uint4 v[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t)  // an all-ones exponent: out of fp16 range
-      if ((hw[t] & 0x7c00u) == 0x7c00u || (hw[t] & 0x7c000000u) == 0x7c000000u)
-        bad = true;
-    reinterpret_cast<uint4*>(x16)[i] = h;
-    reinterpret_cast<float4*>(yacc)[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    reinterpret_cast<float4*>(yacc)[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        v[u] = (c < cpr && t >= 0) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= cpr) break;
+        const uint4 h = make_uint4(bf16x2_to_f16x2(v[u].x), bf16x2_to_f16x2(v[u].y),
+                                   bf16x2_to_f16x2(v[u].z), bf16x2_to_f16x2(v[u].w));
+        const uint32_t* hw = reinterpret_cast<const uint32_t*>(&h);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)  // an all-ones exponent: out of fp16 range
+          if ((hw[q] & 0x7c00u) == 0x7c00u || (hw[q] & 0x7c000000u) == 0x7c000000u)
+            bad = true;
+        dst[c] = h;
+      }
+    }
   }
+  const size_t ny = (size_t)T * H / 4;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < ny; i += stride)
+    reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (bad) set_status(status, QSM_DEV_FP16_RANGE);
 }
 
@@ -439,15 +518,15 @@ finalize_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y,
   }
 }
 
-// (TMA ring, dequantised ring) depths
-constexpr int kGateUpRaw = 4, kGateUpA = 2;
-constexpr int kDownRaw = 6, kDownA = 2;
+// (code ring, token ring, dequantised ring) depths
+constexpr int kGateUpC = 4, kGateUpB = 5, kGateUpA = 2;
+constexpr int kDownC = 6, kDownB = 6, kDownA = 3;
 
-template <int MODE, int RAW, int AST>
+template <int MODE, int CR, int BR, int AST>
 constexpr size_t gemm_smem() {
   constexpr int NA = MODE == kGateUp ? 2 : 1;
-  return (size_t)AST * NA * BM * BK * 2 + (size_t)RAW * (BN * BK * 2 + NA * BM * BK) +
-         1024;
+  return (size_t)AST * NA * BM * BK * 2 + (size_t)BR * BN * BK * 2 +
+         (size_t)CR * NA * BM * BK + 1024;
 }
 
 int sm_count() {
@@ -464,16 +543,17 @@ int sm_count() {
 }
 
 struct WsLayout {
-  size_t x16, hbuf, yacc, total;
+  size_t xall, hbuf, yacc, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
 WsLayout ws_layout(const qsm_moe_layer* L, int T) {
   WsLayout w;
-  w.x16 = 0;
-  w.hbuf = up256((size_t)T * L->H * 2);
-  w.yacc = w.hbuf + up256(((size_t)T * L->k + T) * L->I * 2);
+  const size_t rows = (size_t)T * L->k + T;  // grouped rows, then shared
+  w.xall = 0;
+  w.hbuf = up256(rows * L->H * 2);
+  w.yacc = w.hbuf + up256(rows * L->I * 2);
   w.total = w.yacc + up256((size_t)T * L->H * 4);
   return w;
 }
@@ -496,14 +576,14 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   const int H = L->H, I = L->I, E = L->E, k = L->k;
   const WsLayout wl = ws_layout(L, T);
   char* wsb = static_cast<char*>(ws);
-  __half* x16 = reinterpret_cast<__half*>(wsb + wl.x16);
+  __half* xall = reinterpret_cast<__half*>(wsb + wl.xall);
   __half* hbuf = reinterpret_cast<__half*>(wsb + wl.hbuf);
   float* yacc = reinterpret_cast<float*>(wsb + wl.yacc);
   const int nsm = sm_count();
   const size_t rows_h = (size_t)T * k + T;
 
-  QSM_CUDA_TRY(launch_pdl(prep_kernel, dim3(2 * nsm), dim3(256), 0, stream, x, x16,
-                          yacc, (size_t)T * H / 8, dev_status));
+  QSM_CUDA_TRY(launch_pdl(prep_kernel, dim3(4 * nsm), dim3(256), 0, stream, x,
+                          (const int32_t*)g->perm, T, k, H, xall, yacc, dev_status));
 
   Params p1 = {};
   bool ok = true;
@@ -512,10 +592,9 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   ok &= tc::make_map_2d(&p1.codes_sh, L->shared_gate_up.codes,
                         CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, H, BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok &= tc::make_map_2d(&p1.bmap, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, T, H, BK, 1,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-  ok &= tc::make_map_2d(&p1.bmap_tile, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, T, H,
-                        BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  for (int m = 0; m < 4; ++m)
+    ok &= tc::make_map_2d(&p1.bmap[m], xall, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, H,
+                          BK, BN >> m, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QSM_ERR_CUDA;
   p1.scales = reinterpret_cast<const __half*>(L->gate_up.scales);
   p1.scales_sh = reinterpret_cast<const __half*>(L->shared_gate_up.scales);
@@ -542,8 +621,9 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   ok &= tc::make_map_2d(&p2.codes_sh, L->shared_down.codes,
                         CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, I, BK, BM,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok &= tc::make_map_2d(&p2.bmap, hbuf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, I,
-                        BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  for (int m = 0; m < 4; ++m)
+    ok &= tc::make_map_2d(&p2.bmap[m], hbuf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, I,
+                          BK, BN >> m, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return QSM_ERR_CUDA;
   p2.scales = reinterpret_cast<const __half*>(L->down.scales);
   p2.scales_sh = reinterpret_cast<const __half*>(L->shared_down.scales);
@@ -551,10 +631,11 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   p2.K = I;
   p2.nsub = H / BM;
 
-  constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpRaw, kGateUpA>();
-  constexpr size_t smem2 = gemm_smem<kDown, kDownRaw, kDownA>();
-  auto* k1 = moe_prefill_gemm<kGateUp, kGateUpRaw, kGateUpA>;
-  auto* k2 = moe_prefill_gemm<kDown, kDownRaw, kDownA>;
+  constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpC, kGateUpB, kGateUpA>();
+  constexpr size_t smem2 = gemm_smem<kDown, kDownC, kDownB, kDownA>();
+  static_assert(smem1 <= 220 * 1024 && smem2 <= 220 * 1024, "shared memory");
+  auto* k1 = moe_prefill_gemm<kGateUp, kGateUpC, kGateUpB, kGateUpA>;
+  auto* k2 = moe_prefill_gemm<kDown, kDownC, kDownB, kDownA>;
   QSM_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem1));
   QSM_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -153,8 +153,11 @@ __device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
   return r;
 }
 
+// silu(g) = g / (1 + e^-g) with an approximate reciprocal (a few ulp of
+// fp32).  For g below about -88, e^-g overflows and the quotient is 0, the
+// limit of silu; an IEEE division would take its slow path there.
 __device__ __forceinline__ float silu(float g) {
-  return g / (1.0f + __expf(-g));
+  return __fdividef(g, 1.0f + __expf(-g));
 }
 
 
