@@ -8,13 +8,15 @@
 // Reading: inside an expert the rows keep assignment order (stable), so the
 // permutation is unique.
 //
-// One CTA of 1024 threads does it all (T*k is at most a few ten thousand on
-// this path).  Warp w owns a contiguous range of assignments; a pass with
-// __match_any_sync counts its per-expert histogram without atomics, the CTA
-// turns the 32 histograms into per-(warp, expert) start positions, and a
-// second pass scatters with in-warp ranks, which keeps the order stable.
-// The permutation is staged in shared memory when it fits and written out
-// coalesced.
+// Many assignments: CTA c of the grid owns a contiguous chunk of them.  It
+// histograms ALL the ids (shared-memory atomics; the ids are few and stay in
+// L2), which gives it the global counts, offsets and block map and the
+// counts of the chunks before its own, with no scratch memory and no
+// waiting on other CTAs.  Warp w of the CTA owns a contiguous run of groups
+// of 32 inside the chunk; per-(warp, expert) start positions follow from a
+// scan, and each group is scattered with in-group ranks (the number of
+// lower lanes holding the same expert, from 31 shuffles), which keeps the
+// order stable.  CTA 0 writes the counts, offsets and block map.
 #include "qsm_common.cuh"
 
 namespace qsm {
@@ -23,7 +25,8 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 1024;
-constexpr size_t kSmemLimit = 227 * 1024 - 1024;  // leave room for static smem
+constexpr int kBatch = 8;
+constexpr int kMaxCtas = 64;
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot,
                                                     int* total) {
@@ -55,103 +58,111 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-group_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
-             int max_tiles, int stage, int32_t* __restrict__ counts,
-             int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-             int32_t* __restrict__ inv_perm, int32_t* __restrict__ tile_map,
-             int32_t* __restrict__ n_tiles, int32_t* dev_status) {
+group_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM, int max_tiles,
+             int G, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+             int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
+             int32_t* __restrict__ tile_map, int32_t* __restrict__ n_tiles,
+             int32_t* dev_status) {
   extern __shared__ int smem[];
-  int* hist = smem;                       // [kWarps][E]
-  int* sperm = smem + kWarps * E;         // [A] when staged
+  int* tot = smem;          // [E] all assignments per expert
+  int* bef = smem + E;      // [E] those before this CTA's chunk
+  int* wh = smem + 2 * E;   // [kWarps][E] this CTA's groups, per warp
   __shared__ int warp_tot[32];
   __shared__ int s_total, s_tiles;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
+  for (int i = tid; i < (2 + kWarps) * E; i += kThreads) smem[i] = 0;
   __syncthreads();
-
-  const int chunk = ((A + kWarps - 1) / kWarps + 31) & ~31;
-  const int beg = min(A, warp * chunk), end = min(A, beg + chunk);
-  int* myhist = hist + warp * E;
-  bool bad = false;
-  // pass 1: per-warp histogram
-  for (int base = beg; base < end; base += 32) {
-    const int a = base + lane;
-    int key = -1;
-    if (a < end) {
-      const int e = topk_idx[a];
-      if (e >= 0 && e < E) key = e; else bad = true;
+  const int c0 = blockIdx.x * G * kThreads;  // first assignment of the chunk
+  for (int b = 0; b < A; b += kThreads * kBatch) {
+    int ids[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int a = b + u * kThreads + tid;
+      ids[u] = a < A ? __ldcg(topk_idx + a) : -1;
     }
-    const unsigned m = __match_any_sync(0xffffffffu, key);
-    if (key >= 0 && lane == __ffs(m) - 1) myhist[key] += __popc(m);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int a = b + u * kThreads + tid;
+      if (ids[u] >= 0 && ids[u] < E) {
+        atomicAdd(&tot[ids[u]], 1);
+        if (a < c0) atomicAdd(&bef[ids[u]], 1);
+      }
+    }
   }
-  if (__any_sync(0xffffffffu, bad) && lane == 0)
-    set_status(dev_status, QSM_DEV_BAD_EXPERT_ID);
-  __syncthreads();
+  const int wbeg = c0 + warp * G * 32;  // this warp's G groups of 32
+  bool bad = false;
+  for (int g = 0; g < G; ++g) {
+    const int a = wbeg + 32 * g + lane;
+    if (a < A) {
+      const int e = __ldcg(topk_idx + a);
+      if (e >= 0 && e < E) atomicAdd(&wh[warp * E + e], 1);
+      else bad = true;
+    }
+  }
+  if (__syncthreads_or(bad) && tid == 0) set_status(dev_status, QSM_DEV_BAD_EXPERT_ID);
 
-  // counts, offsets, per-(warp, expert) bases, block map
+  // offsets and block map (thread e owns expert e), per-(warp, expert) starts
   {
     const int e = tid;
-    int cnt = 0;
-    if (e < E)
-      for (int w = 0; w < kWarps; ++w) cnt += hist[w * E + e];
-    const int off = block_exclusive_scan(e < E ? cnt : 0, warp_tot, &s_total);
+    const int cnt = e < E ? tot[e] : 0;
+    const int off = block_exclusive_scan(cnt, warp_tot, &s_total);
     const int nt = (e < E) ? (cnt + BM - 1) / BM : 0;
     const int t0 = block_exclusive_scan(nt, warp_tot, &s_tiles);
     if (e < E) {
-      counts[e] = cnt;
-      offsets[e] = off;
-      int run = off;
+      int run = off + bef[e];
       for (int w = 0; w < kWarps; ++w) {
-        const int c = hist[w * E + e];
-        hist[w * E + e] = run;
+        const int c = wh[w * E + e];
+        wh[w * E + e] = run;
         run += c;
       }
-      for (int m = 0; m < nt && t0 + m < max_tiles; ++m) {
-        tile_map[2 * (t0 + m)] = e;
-        tile_map[2 * (t0 + m) + 1] = off + m * BM;
+      if (blockIdx.x == 0) {
+        counts[e] = cnt;
+        offsets[e] = off;
+        for (int m = 0; m < nt && t0 + m < max_tiles; ++m) {
+          tile_map[2 * (t0 + m)] = e;
+          tile_map[2 * (t0 + m) + 1] = off + m * BM;
+        }
       }
     }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
     if (tid == 0) {
       offsets[E] = s_total;
       n_tiles[0] = min(s_tiles, max_tiles);
     }
-  }
-  __syncthreads();
-  for (int i = s_tiles + tid; i < max_tiles; i += kThreads) {
-    tile_map[2 * i] = -1;
-    tile_map[2 * i + 1] = -1;
+    for (int i = s_tiles + tid; i < max_tiles; i += kThreads) {
+      tile_map[2 * i] = -1;
+      tile_map[2 * i + 1] = -1;
+    }
+    for (int i = s_total + tid; i < A; i += kThreads) perm[i] = -1;
   }
 
-  // pass 2: stable scatter
-  const unsigned lt = (1u << lane) - 1u;
-  for (int base = beg; base < end; base += 32) {
-    const int a = base + lane;
-    int key = -1;
-    if (a < end) {
-      const int e = topk_idx[a];
-      if (e >= 0 && e < E) key = e;
+  // stable scatter of this warp's groups
+  for (int g = 0; g < G; ++g) {
+    const int a = wbeg + 32 * g + lane;
+    int key = a < A ? __ldcg(topk_idx + a) : -1;
+    if (key >= E) key = -1;
+    int rank = 0;  // lower lanes of this group with the same expert
+#pragma unroll
+    for (int d = 1; d < 32; ++d) {
+      const int o = __shfl_up_sync(0xffffffffu, key, d);
+      rank += (lane >= d && o == key) ? 1 : 0;
     }
-    const unsigned m = __match_any_sync(0xffffffffu, key);
     if (key >= 0) {
-      const int pos = myhist[key] + __popc(m & lt);
-      if (stage) sperm[pos] = a; else perm[pos] = a;
+      const int pos = wh[warp * E + key] + rank;
+      perm[pos] = a;
       inv_perm[a] = pos;
-    } else if (a < end) {
+    } else if (a < A) {
       inv_perm[a] = -1;
     }
     __syncwarp();
-    if (key >= 0 && lane == __ffs(m) - 1) myhist[key] += __popc(m);
+    if (key >= 0) atomicAdd(&wh[warp * E + key], 1);
     __syncwarp();
   }
-  __syncthreads();
-  const int valid = s_total;
-  if (stage)
-    for (int i = tid; i < valid; i += kThreads) perm[i] = sperm[i];
-  for (int i = valid + tid; i < A; i += kThreads) perm[i] = -1;
 }
 
 // Few assignments (decode): the per-warp histogram machinery above costs
@@ -264,16 +275,16 @@ extern "C" qsm_status moe_group_tokens(const int32_t* topk_idx, int32_t T,
                               g->n_tiles, dev_status));
     return QSM_OK;
   }
-  const size_t hist_bytes = (size_t)kWarps * E * sizeof(int);
-  const int stage = hist_bytes + (size_t)A * sizeof(int) <= kSmemLimit;
-  const size_t smem = hist_bytes + (stage ? (size_t)A * sizeof(int) : 0);
+  // chunks of G groups of 32 per warp, at most kMaxCtas CTAs
+  const int G = (int)((A + (int64_t)kThreads * kMaxCtas - 1) / ((int64_t)kThreads * kMaxCtas));
+  const int nblk = (int)((A + (int64_t)G * kThreads - 1) / ((int64_t)G * kThreads));
+  const size_t smem = (size_t)(2 + kWarps) * E * sizeof(int);
   QSM_CUDA_TRY(cudaFuncSetAttribute(group_kernel,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemLimit));
-  QSM_CUDA_TRY(launch_pdl(group_kernel, dim3(1), dim3(kThreads), smem, stream,
+                                    (int)smem));
+  QSM_CUDA_TRY(launch_pdl(group_kernel, dim3(nblk), dim3(kThreads), smem, stream,
                           topk_idx, (int)A, (int)E, (int)g->tile_rows,
-                          (int)g->max_tiles, stage, g->counts, g->offsets,
-                          g->perm, g->inv_perm, g->tile_map, g->n_tiles,
-                          dev_status));
+                          (int)g->max_tiles, G, g->counts, g->offsets, g->perm,
+                          g->inv_perm, g->tile_map, g->n_tiles, dev_status));
   return QSM_OK;
 }

@@ -17,13 +17,17 @@
 //             tokens in order for the shared expert; zero the fp32 output
 //             accumulator
 //   gate_up   per work item (block of <= 128 token rows of one expert,
-//             128 intermediate indices): D_gate, D_up (128 x N fp32 each, in
-//             tensor memory) += W_gate/up tile x token rows; epilogue
-//             h = silu(gate) * up, stored fp16 (scaled by 1/16) per sorted row
-//   down      per work item (same token block, 128 output rows):
-//             D (128 token rows x 128) = h rows x W_down tile^T; epilogue
+//             128 intermediate indices): D (128 token rows x 256, fp32 in
+//             tensor memory) += token rows x [W_gate tile; W_up tile]^T, one
+//             N = 256 MMA per 16-wide K step; epilogue (one token row per
+//             thread) h = silu(gate) * up, stored fp16 (scaled by 1/16) in
+//             16-byte pieces per sorted row
+//   down      per work item (same token block, 256 output rows):
+//             D (128 token rows x 256) = h rows x W_down tiles^T; epilogue
 //             y_acc[token] += routing weight * D row (16-byte fp32
 //             reduce-adds, one token per thread)
+// Rows of a short tile beyond its tokens hold stale data: their D rows are
+// never read.
 //   finalize  y = bf16(y_acc) (and the fp32 copy)
 //
 // Roles in a persistent CTA (one per SM, 16 warps):
@@ -74,7 +78,7 @@ struct Params {
   const int32_t* n_tiles;
   const float* topk_w;
   int shared_tiles;       // ceil(T / BN)
-  int nsub;               // 128-row sub-blocks per tile
+  int nsub;               // weight blocks (two 128-row tiles each) per tile
   __half* hbuf;           // [T*k + T, I]
   float* yacc;            // [T, H]
   int32_t* status;
@@ -118,6 +122,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// First row (within the expert) of weight tile a in {0, 1} of work item sub:
+// gate_up pairs the gate rows and the up rows of intermediates sub*128..,
+// down takes output rows sub*256 + a*128...
+__device__ __forceinline__ int weight_row0(const Params& p, int mode, int sub, int a) {
+  return mode == kGateUp ? a * p.I + sub * BM : (2 * sub + a) * BM;
+}
+
 // y[0..3] += v0..v3 in one 16-byte reduction (16-byte aligned address).
 __device__ __forceinline__ void red_add_v4(float* y, float v0, float v1, float v2,
                                            float v3) {
@@ -129,7 +140,7 @@ __device__ __forceinline__ void red_add_v4(float* y, float v0, float v1, float v
 template <int MODE, int CR, int BR, int AST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_prefill_gemm(const __grid_constant__ Params p) {
-  constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per K step
+  constexpr int NA = 2;                        // weight tiles per K step
   constexpr int A_BYTES = BM * BK * 2;         // fp16, 128B swizzle
   constexpr int B_BYTES = BN * BK * 2;
   constexpr int C_BYTES = BM * BK;             // int8 codes
@@ -197,8 +208,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
         const CUtensorMap* cm = ti.e < 0 ? &p.codes_sh : &p.codes;
         const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
         int arow[2];
-        arow[0] = ebase + sub * BM;
-        arow[1] = ebase + p.I + sub * BM;  // gate_up: the up rows
+        for (int a = 0; a < NA; ++a) arow[a] = ebase + weight_row0(p, MODE, sub, a);
         bool ok = true;
         for (int ks = 0; ks < ksteps; ++ks) {
           if (f >= CR && !wait_bar(&c_empty[c], ((f / CR) - 1) & 1, abort_p, p.status)) {
@@ -266,9 +276,8 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
         const int ab = j & 1;  // accumulator buffer
         if (j >= 2 && !wait_bar(&acce_bar[ab], ((j >> 1) - 1) & 1, abort_p, p.status)) break;
         tc::tc_fence_after();
-        // gate_up: D[weight row, token] (N = the tile's rows rounded up to
-        // 16); down: D[token, output row] (M = 128 token rows, N = 128)
-        const uint32_t idesc = tc::idesc_f16_m128(MODE == kGateUp ? ti.n : BM);
+        // D[token row, weight row]: M = 128 token rows, N = 256 weight rows
+        const uint32_t idesc = tc::idesc_f16_m128(NA * BM);
         const uint32_t dbase = tmem + ab * 256;
         bool ok = true;
         for (int ks = 0; ks < ksteps; ++ks) {
@@ -280,19 +289,11 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
           tc::tc_fence_after();
           const uint32_t a0 = smem_u32(aring + a * A_STAGE);
           const uint32_t b0 = smem_u32(bring + b * B_BYTES);
+          // the two weight tiles of a stage are one 256-row K-major operand
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            if (MODE == kGateUp) {
-#pragma unroll
-              for (int m = 0; m < NA; ++m)
-                tc::mma_f16(dbase + m * 128, tc::sw128_desc(a0 + m * A_BYTES + kk * 32),
-                            tc::sw128_desc(b0 + kk * 32), idesc,
-                            (ks > 0 || kk > 0) ? 1u : 0u);
-            } else {
-              tc::mma_f16(dbase, tc::sw128_desc(b0 + kk * 32), tc::sw128_desc(a0 + kk * 32),
-                          idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16(dbase, tc::sw128_desc(b0 + kk * 32), tc::sw128_desc(a0 + kk * 32),
+                        idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&b_empty[b]);
           tc::mma_commit(&a_empty[a]);
           ++f;
@@ -307,17 +308,16 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------- dequant
     const int d = threadIdx.x - 128;
-    const int am = MODE == kGateUp ? (d >> 7) : 0;
-    const int rw = MODE == kGateUp ? (d & 127) : (d >> 1);
-    const int half = MODE == kGateUp ? 0 : (d & 1);
-    constexpr int kInChunks = MODE == kGateUp ? 4 : 2;  // 16 codes per chunk
+    const int am = d >> 7;   // weight tile
+    const int rw = d & 127;  // row of the tile
+    constexpr int kInChunks = 4;  // 16 codes per chunk
     int c = 0, a = 0;
     uint32_t f = 0;
     for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
       const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
-      const int row = ebase + (am ? p.I : 0) + sub * BM + rw;
+      const int row = ebase + weight_row0(p, MODE, sub, am) + rw;
       // this row's block scales: one 4-byte pair per K step (4-byte aligned
       // for any K % 64 == 0), fetched one group of 8 K steps ahead
       const uint32_t* sc = reinterpret_cast<const uint32_t*>(
@@ -347,8 +347,10 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
                                   (rw & 7) * 128;
 #pragma unroll
           for (int j = 0; j < kInChunks; ++j) {
-            // rotate the chunk order by row to spread shared-memory banks
-            const int ci = half * kInChunks + ((j + rw) & (kInChunks - 1));
+            // chunk order per row: conflict-free shared-memory banks for the
+            // code reads (8 rows per quarter warp, 64-byte row pitch) and the
+            // swizzled fp16 writes alike
+            const int ci = j ^ (int)((0x5FA0u >> (2 * (rw & 7))) & 3u);
             const uint4 v = *reinterpret_cast<const uint4*>(codes + ci * 16);
             const uint32_t sbits = (ci < 2) ? (sc2 & 0xffffu) : (sc2 >> 16);
             const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sbits));
@@ -388,10 +390,13 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
       const int b = j & 1;
-      // down: this thread's token row of the tile, its token and weight
-      int tok = -1;
+      // this thread's token row of the tile: its sorted row (gate_up) or
+      // its token and routing weight (down)
+      const bool live = et < ti.cnt;
+      const int srow = (ti.e < 0 ? p.T * p.k : 0) + ti.row0 + et;
+      int tok = 0;
       float wt = 0.f;
-      if (MODE == kDown && et < ti.cnt) {
+      if (MODE == kDown && live) {
         if (ti.e < 0) {
           tok = ti.row0 + et;
           wt = kHScaleInv;
@@ -405,29 +410,34 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       tc::tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + b * 256;
       if (MODE == kGateUp) {
-        const int i = sub * BM + 32 * q4 + lane;  // intermediate index
-        for (int c0 = 0; c0 < ti.n; c0 += 16) {
+        // columns 0..127 gate, 128..255 up of intermediates sub*128 + c
+        __half* dst = p.hbuf + (size_t)srow * p.I + sub * BM;
+        for (int c0 = 0; c0 < BM; c0 += 16) {
           float gv[16], uv[16];
           tc::tmem_ld16(taddr + c0, gv);
-          tc::tmem_ld16(taddr + 128 + c0, uv);
+          tc::tmem_ld16(taddr + BM + c0, uv);
+          if (live) {
+            uint32_t hw[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = c0 + c;
-            if (col < ti.cnt) {
-              const float h = silu(gv[c]) * uv[c] * kHScale;
-              if (!(fabsf(h) <= 65504.f)) bad = true;
-              const int hrow = ti.e < 0 ? p.T * p.k + ti.row0 + col : ti.row0 + col;
-              p.hbuf[(size_t)hrow * p.I + i] = __float2half_rn(h);
+            for (int c = 0; c < 16; c += 2) {
+              const float h0 = silu(gv[c]) * uv[c] * kHScale;
+              const float h1 = silu(gv[c + 1]) * uv[c + 1] * kHScale;
+              if (!(fabsf(h0) <= 65504.f) || !(fabsf(h1) <= 65504.f)) bad = true;
+              const __half2 hh = __floats2half2_rn(h0, h1);
+              hw[c / 2] = *reinterpret_cast<const uint32_t*>(&hh);
             }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+            d4[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            d4[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
       } else {
         // 16 consecutive output rows per load: four 16-byte reduce-adds
-        float* dst = p.yacc + (size_t)(tok < 0 ? 0 : tok) * p.H + sub * BM;
-        for (int c0 = 0; c0 < BM; c0 += 16) {
+        float* dst = p.yacc + (size_t)tok * p.H + sub * (NA * BM);
+        for (int c0 = 0; c0 < NA * BM; c0 += 16) {
           float dv[16];
           tc::tmem_ld16(taddr + c0, dv);
-          if (tok >= 0) {
+          if (live) {
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               red_add_v4(dst + c0 + 4 * v, wt * dv[4 * v], wt * dv[4 * v + 1],
@@ -519,12 +529,12 @@ finalize_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y,
 }
 
 // (code ring, token ring, dequantised ring) depths
-constexpr int kGateUpC = 4, kGateUpB = 5, kGateUpA = 2;
-constexpr int kDownC = 6, kDownB = 6, kDownA = 3;
+constexpr int kGateUpC = 4, kGateUpB = 3, kGateUpA = 3;
+constexpr int kDownC = 4, kDownB = 3, kDownA = 3;
 
 template <int MODE, int CR, int BR, int AST>
 constexpr size_t gemm_smem() {
-  constexpr int NA = MODE == kGateUp ? 2 : 1;
+  constexpr int NA = 2;
   return (size_t)AST * NA * BM * BK * 2 + (size_t)BR * BN * BK * 2 +
          (size_t)CR * NA * BM * BK + 1024;
 }
@@ -561,7 +571,7 @@ WsLayout ws_layout(const qsm_moe_layer* L, int T) {
 }  // namespace prefill
 
 bool prefill_supported(const qsm_moe_layer* L) {
-  return L->gate_up.qtype == QSM_Q8_0 && L->H % 128 == 0 && L->I % 128 == 0;
+  return L->gate_up.qtype == QSM_Q8_0 && L->H % 256 == 0 && L->I % 128 == 0;
 }
 
 size_t prefill_ffn_workspace_bytes(const qsm_moe_layer* L, int T) {
@@ -629,7 +639,7 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   p2.scales_sh = reinterpret_cast<const __half*>(L->shared_down.scales);
   p2.R = H;
   p2.K = I;
-  p2.nsub = H / BM;
+  p2.nsub = H / (2 * BM);
 
   constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpC, kGateUpB, kGateUpA>();
   constexpr size_t smem2 = gemm_smem<kDown, kDownC, kDownB, kDownA>();

@@ -91,6 +91,49 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Top k of the values a warp holds, v[i] at index lane + 32 i (i < KPER,
+// indices >= E ignored), in descending order with ties to the lower index.
+// Lane j < k receives the j-th value and its index.  Each round takes every
+// lane's best untaken candidate, packed as (order-preserving key << 32 |
+// ~index), and a butterfly of 64-bit maxima over the warp.  Non-finite
+// values must be mapped to -inf by the caller.
+template <int KPER>
+__device__ __forceinline__ void warp_topk(const float (&v)[KPER], int E, int k,
+                                          float& out_v, int& out_e) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[KPER];
+#pragma unroll
+  for (int i = 0; i < KPER; ++i) {
+    const uint32_t u = __float_as_uint(v[i]);
+    key[i] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  uint32_t taken = 0;
+  out_v = 0.f;
+  out_e = 0;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < KPER; ++i) {
+      const int e = lane + 32 * i;
+      const unsigned long long c =
+          ((unsigned long long)key[i] << 32) | (unsigned long long)(~(uint32_t)e);
+      if (e < E && !((taken >> i) & 1u) && c > best) best = c;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    const uint32_t e = ~(uint32_t)best;
+    const uint32_t kv = (uint32_t)(best >> 32);
+    if ((e & 31u) == (uint32_t)lane) taken |= 1u << (e >> 5);
+    if (lane == j) {
+      out_v = __uint_as_float((kv & 0x80000000u) ? (kv & 0x7fffffffu) : ~kv);
+      out_e = (int)e;
+    }
+  }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) {
   return __uint_as_float(v << 16);
 }

@@ -234,34 +234,12 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0)
       set_status(dev_status, QSM_DEV_NONFINITE);
-    // Order-preserving integer keys (larger float -> larger key), so each
-    // round is two warp reductions: the largest key, then the lowest expert
-    // index holding it (ties go to the lower index).
-    uint32_t key[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const uint32_t u = __float_as_uint(v[i]);
-      key[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-    }
-    uint32_t taken = 0;  // bit i: candidate lane + 32 i already selected
-    for (int j = 0; j < k; ++j) {
-      uint32_t bk = 0u, be = 0xffffffffu;  // best untaken (key desc, index asc)
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const uint32_t ee = lane + 32 * i;
-        if (ee < (uint32_t)E && !((taken >> i) & 1u) && (key[i] > bk || be == 0xffffffffu)) {
-          bk = key[i];
-          be = ee;
-        }
-      }
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-      const uint32_t emin = __reduce_min_sync(0xffffffffu, (bk == kmax) ? be : 0xffffffffu);
-      if ((emin & 31u) == (uint32_t)lane) taken |= 1u << (emin >> 5);
-      if (lane == 0) {
-        const uint32_t u = (kmax & 0x80000000u) ? (kmax & 0x7fffffffu) : ~kmax;
-        sel_l[warp][j] = __uint_as_float(u);
-        sel_e[warp][j] = (int)emin;
-      }
+    float my_l;
+    int my_e;
+    warp_topk<kPer>(v, E, k, my_l, my_e);
+    if (lane < k) {
+      sel_l[warp][lane] = my_l;
+      sel_e[warp][lane] = my_e;
     }
     __syncwarp();
     const float top = sel_l[warp][0];
@@ -291,7 +269,7 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
 
 namespace qsm {
 bool route_tc_supported(int T, int H, int E, int k);
-size_t route_tc_split_bytes(int H, int E);
+size_t route_tc_workspace_bytes(int T, int H, int E);
 qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
                            const float* logit_bias, int T, int H, int E, int k,
                            int renormalize, int32_t* topk_idx, float* topk_w,
@@ -301,7 +279,7 @@ qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
 
 extern "C" size_t moe_route_workspace_bytes(int32_t T, int32_t H, int32_t E) {
   if (T < 0 || H <= 0 || E <= 0) return 0;
-  if (qsm::route_tc_supported(T, H, E, 1)) return qsm::route_tc_split_bytes(H, E);
+  if (qsm::route_tc_supported(T, H, E, 1)) return qsm::route_tc_workspace_bytes(T, H, E);
   return qsm::counters_bytes(T) + (((size_t)T * E * sizeof(float) + 255) & ~size_t(255));
 }
 

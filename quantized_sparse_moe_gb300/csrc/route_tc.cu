@@ -10,15 +10,19 @@
 // every product x * part is exact in fp32 and the tensor core's fp32
 // accumulation gives fp32-accurate logits.
 //
-// One CTA computes a tile of 128 tokens x all E experts (E <= 256) in tensor
-// memory: D[token][expert], in two accumulators, one per half of H, each
-// summing the lo, mid and hi parts (small ones first); the epilogue adds the
-// halves in fp32.  Fewer tensor-core accumulation steps per accumulator keep
-// the logit error near plain fp32 accumulation.  Warp 0 streams x tiles and split-weight tiles
-// by TMA (128-byte swizzle), lane 0 of warp 1 issues the MMAs over K =
-// 3 * H, and warps 4-7 (one tensor-memory lane = one token each) read the
-// E logits of their token, keep the top k in registers and write the
-// routing weights.
+// The reduction over H is split in KS slices: CTA (tile, q) computes a tile
+// of 128 tokens x all E experts (E <= 256) over slice q of H in tensor
+// memory, D[token][expert], summing the lo, mid and hi parts (small ones
+// first).  Few tensor-core accumulation steps per accumulator keep the logit
+// error near plain fp32 accumulation, and the KS CTAs of a tile run on KS
+// SMs.  Warp 0 streams x tiles and split-weight tiles by TMA (128-byte
+// swizzle), lane 0 of warp 1 issues the MMAs, and warps 4-7 (one
+// tensor-memory lane = one token each) write the partial logits to the
+// workspace.  The CTA that finishes a tile last (a per-tile arrival counter,
+// no waiting) adds the KS partials of each token in slice order plus the
+// bias into a shared-memory tile (all its threads, coalesced), then one
+// thread per token keeps the top k in registers and writes the routing
+// weights; it re-arms the counter.
 #include "tc_common.cuh"
 
 namespace qsm {
@@ -34,27 +38,40 @@ struct Params {
   CUtensorMap xa;  // x [T, H] bf16, box {64, 128}
   CUtensorMap wb;  // split router weight [3E, H] bf16, box {64, E}
   const float* bias;
-  int T, H, E, k, renorm, ntiles;
+  int T, H, E, k, renorm, ntiles, ks;
+  float* part;          // partial logits [ks][T][E] fp32
+  unsigned* counters;   // [ntiles] arrival counters, zero between calls
   int32_t* topk_idx;
   float* topk_w;
   int32_t* status;
 };
 
-// out[p*E*H + i] = part p of w[i] (hi, mid, lo).
+__device__ __forceinline__ uint32_t bf16_split3(float v, uint32_t& mid, uint32_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h);
+  const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(m);
+  mid = __bfloat16_as_ushort(m);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(r2));
+  return __bfloat16_as_ushort(h);
+}
+
+// out[p*n + i] = part p of w[i] (hi, mid, lo); n % 4 == 0.
 __global__ void __launch_bounds__(256)
 split_kernel(const float* __restrict__ w, __nv_bfloat16* __restrict__ out, size_t n) {
   pdl_wait();
   pdl_launch_dependents();
+  const size_t n4 = n / 4;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += stride) {
-    const float v = __ldg(w + i);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    out[i] = hi;
-    out[n + i] = mid;
-    out[2 * n + i] = __float2bfloat16_rn(r2);
+  uint2* o = reinterpret_cast<uint2*>(out);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(w) + i);
+    uint32_t m0, m1, m2, m3, l0, l1, l2, l3;
+    const uint32_t h0 = bf16_split3(v.x, m0, l0), h1 = bf16_split3(v.y, m1, l1);
+    const uint32_t h2 = bf16_split3(v.z, m2, l2), h3 = bf16_split3(v.w, m3, l3);
+    o[i] = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+    o[n4 + i] = make_uint2(m0 | (m1 << 16), m2 | (m3 << 16));
+    o[2 * n4 + i] = make_uint2(l0 | (l1 << 16), l2 | (l3 << 16));
   }
 }
 
@@ -64,6 +81,7 @@ __device__ __forceinline__ uint32_t idesc_bf16_m128(int n) {
          ((uint32_t)(128 >> 4) << 24);
 }
 
+template <int KS>  // slices of H (p.ks == KS)
 __global__ void __launch_bounds__(kThreads, 1)
 route_tc_kernel(const __grid_constant__ Params p) {
   constexpr int A_BYTES = BM * BK * 2;
@@ -72,18 +90,17 @@ route_tc_kernel(const __grid_constant__ Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar,
-      acce_bar;
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  __shared__ int abort_flag, is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x / KS, q = blockIdx.x - tile * KS;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&accf_bar, 1);
-    mbar_init(&acce_bar, 128);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -91,7 +108,7 @@ route_tc_kernel(const __grid_constant__ Params p) {
     tc::prefetch_map(&p.xa);
     tc::prefetch_map(&p.wb);
   }
-  if (warp == 1) tc::tmem_alloc(&tmem_base, 512);
+  if (warp == 1) tc::tmem_alloc(&tmem_base, 256);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -99,8 +116,8 @@ route_tc_kernel(const __grid_constant__ Params p) {
   pdl_wait();
   pdl_launch_dependents();
   volatile int* abort_p = &abort_flag;
-  const int kh = p.H / BK;
-  const int steps = 3 * kh;
+  const int kq = p.H / BK / KS;  // K steps of 64 per slice and part
+  const int steps = 3 * kq;
   auto wait = [&](uint64_t* bar, uint32_t par) {
     for (uint32_t i = 0; i < kWaitIters; ++i) {
       if (mbar_try_wait(bar, par)) return true;
@@ -113,65 +130,130 @@ route_tc_kernel(const __grid_constant__ Params p) {
 
   if (warp == 0) {
     if (lane == 0) {
-      int s = 0, fill = 0;
       const uint32_t bytes = A_BYTES + (uint32_t)p.E * BK * 2;
-      for (int tile = blockIdx.x; tile < p.ntiles && !*abort_p; tile += gridDim.x) {
-        for (int st = 0; st < steps; ++st) {
-          if (fill >= kStages && !wait(&empty_bar[s], ((fill / kStages) - 1) & 1)) break;
-          const int pi = st / kh, ks = st - pi * kh;
-          const int part = 2 - pi;  // lo, mid, hi
-          unsigned char* sb = smem + s * STAGE;
-          mbar_arrive_expect_tx(&full_bar[s], bytes);
-          tc::tma_load_2d(sb, &p.xa, ks * BK, tile * BM, &full_bar[s]);
-          tc::tma_load_2d(sb + A_BYTES, &p.wb, ks * BK, part * p.E, &full_bar[s]);
-          ++fill;
-          s = (s + 1 == kStages) ? 0 : s + 1;
-        }
+      for (int st = 0, s = 0; st < steps && !*abort_p; ++st) {
+        if (st >= kStages && !wait(&empty_bar[s], ((st / kStages) - 1) & 1)) break;
+        const int pi = st / kq, kk = q * kq + (st - pi * kq);
+        const int part = 2 - pi;  // lo, mid, hi
+        unsigned char* sb = smem + s * STAGE;
+        mbar_arrive_expect_tx(&full_bar[s], bytes);
+        tc::tma_load_2d(sb, &p.xa, kk * BK, tile * BM, &full_bar[s]);
+        tc::tma_load_2d(sb + A_BYTES, &p.wb, kk * BK, part * p.E, &full_bar[s]);
+        s = (s + 1 == kStages) ? 0 : s + 1;
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      int s = 0, fill = 0, j = 0;
       const uint32_t idesc = idesc_bf16_m128(p.E);
-      for (int tile = blockIdx.x; tile < p.ntiles && !*abort_p; tile += gridDim.x, ++j) {
-        if (j > 0 && !wait(&acce_bar, (j - 1) & 1)) break;
-        tc::tc_fence_after();
-        bool ok = true;
-        for (int st = 0; st < steps; ++st) {
-          if (!wait(&full_bar[s], (fill / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + s * STAGE);
-          const uint32_t b0 = a0 + A_BYTES;
-          const int pi = st / kh, ks = st - pi * kh;
-          const int acc = ks < kh / 2 ? 0 : 1;  // accumulator of this half of H
-          const bool first = pi == 0 && (ks == 0 || ks == kh / 2);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_f16(tmem + acc * 256, tc::sw128_desc(a0 + kk * 32),
-                        tc::sw128_desc(b0 + kk * 32), idesc,
-                        (!first || kk > 0) ? 1u : 0u);
-          tc::mma_commit(&empty_bar[s]);
-          ++fill;
-          s = (s + 1 == kStages) ? 0 : s + 1;
+      bool ok = true;
+      for (int st = 0, s = 0; st < steps; ++st) {
+        if (!wait(&full_bar[s], (st / kStages) & 1)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc::mma_commit(&accf_bar);
+        tc::tc_fence_after();
+        const uint32_t a0 = smem_u32(smem + s * STAGE);
+        const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc::mma_f16(tmem, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32),
+                      idesc, (st > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&empty_bar[s]);
+        s = (s + 1 == kStages) ? 0 : s + 1;
       }
+      if (ok) tc::mma_commit(&accf_bar);
     }
     __syncwarp();
   } else if (warp >= 4) {
     const int q4 = warp & 3;
-    int j = 0;
-    bool bad = false;
-    for (int tile = blockIdx.x; tile < p.ntiles && !*abort_p; tile += gridDim.x, ++j) {
-      if (!wait(&accf_bar, j & 1)) break;
-      tc::tc_fence_after();
-      const int t = tile * BM + 32 * q4 + lane;
-      const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16);
+    const int row = 32 * q4 + lane;  // token row of the tile = TMEM lane
+    const int t = tile * BM + row;
+    const bool ok = wait(&accf_bar, 0);
+    tc::tc_fence_after();
+    // partial logits of this slice: the token's E values, 64 bytes at a time
+    const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16);
+    float* prow = p.part + ((size_t)q * p.T + (t < p.T ? t : 0)) * p.E;
+    if (ok) {
+      for (int c0 = 0; c0 < p.E; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(taddr + c0, v);
+        if (t < p.T) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            __stcg(reinterpret_cast<float4*>(prow + c0) + u,
+                   make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+        }
+      }
+    }
+    __threadfence();  // this thread's partial logits, before the arrival
+  }
+
+  // arrival: the last of the tile's ks CTAs selects the experts, one token
+  // per warp at a time
+  tc::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(p.counters + tile, 1u);
+    is_last = prev == (unsigned)(KS - 1);
+    if (is_last) __threadfence();
+  }
+  __syncthreads();
+  if (is_last && !*abort_p) {
+    // the pipeline stages are free: the tile's logits go to shared memory,
+    // [row][E + 4] fp32 (the pad spreads a column over the banks)
+    float* lg = reinterpret_cast<float*>(smem);
+    const int ld = p.E + 4;
+    const int rows = min(BM, p.T - tile * BM);
+    const size_t pstride = (size_t)p.T * p.E;
+    const int e4 = p.E / 4;  // float4 columns
+    const int n4 = rows * e4;
+    // the slices in order, then the bias; 8 positions per thread in flight
+    for (int b0 = threadIdx.x; b0 < n4; b0 += kThreads * 8) {
+      float4 sl[8][KS];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int pos = b0 + u * kThreads;
+        if (pos < n4) {
+          const int r = pos / e4, c = pos - r * e4;
+          const float4* src = reinterpret_cast<const float4*>(
+                                  p.part + (size_t)(tile * BM + r) * p.E) + c;
+#pragma unroll
+          for (int s2 = 0; s2 < KS; ++s2)
+            sl[u][s2] = __ldcg(src + s2 * (pstride / 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int pos = b0 + u * kThreads;
+        if (pos < n4) {
+          const int r = pos / e4, c = pos - r * e4;
+          float4 a = sl[u][0];
+#pragma unroll
+          for (int s2 = 1; s2 < KS; ++s2) {
+            a.x += sl[u][s2].x;
+            a.y += sl[u][s2].y;
+            a.z += sl[u][s2].z;
+            a.w += sl[u][s2].w;
+          }
+          if (p.bias) {
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias) + c);
+            a.x += bb.x;
+            a.y += bb.y;
+            a.z += bb.z;
+            a.w += bb.w;
+          }
+          *reinterpret_cast<float4*>(lg + r * ld + 4 * c) = a;
+        }
+      }
+    }
+    __syncthreads();
+    // one thread per token: the best kMaxTopK in registers (value desc,
+    // index asc; indices arrive in ascending order, so an equal value never
+    // displaces)
+    const int r = threadIdx.x;
+    if (r < rows) {
+      const float* row = lg + r * ld;
       float val[kMaxTopK];
       int idx[kMaxTopK];
 #pragma unroll
@@ -179,20 +261,18 @@ route_tc_kernel(const __grid_constant__ Params p) {
         val[i] = -INFINITY;
         idx[i] = 0x7fffffff;
       }
-      for (int c0 = 0; c0 < p.E; c0 += 16) {
-        float v[16], v2[16];
-        tc::tmem_ld16(taddr + c0, v);
-        tc::tmem_ld16(taddr + 256 + c0, v2);
+      bool bad = false;
+      for (int c0 = 0; c0 < p.E; c0 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(row + c0);
+        const float l4[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float l = v[c] + v2[c] + (p.bias ? __ldg(p.bias + c0 + c) : 0.f);
+        for (int c = 0; c < 4; ++c) {
+          float l = l4[c];
           if (!isfinite(l)) {
-            bad = bad || t < p.T;
+            bad = true;
             l = -INFINITY;
           }
           int ci = c0 + c;
-          // keep the best kMaxTopK (value desc, index asc); indices arrive
-          // in ascending order, so an equal value never displaces
           if (l > val[kMaxTopK - 1] || (l == val[kMaxTopK - 1] && ci < idx[kMaxTopK - 1])) {
 #pragma unroll
             for (int i = 0; i < kMaxTopK; ++i) {
@@ -215,36 +295,31 @@ route_tc_kernel(const __grid_constant__ Params p) {
         for (int i = 0; i < kMaxTopK; ++i)
           if (i < p.k) denom += __expf(val[i] - top);
       } else {
-        for (int c0 = 0; c0 < p.E; c0 += 16) {
-          float v[16], v2[16];
-          tc::tmem_ld16(taddr + c0, v);
-          tc::tmem_ld16(taddr + 256 + c0, v2);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float l = v[c] + v2[c] + (p.bias ? __ldg(p.bias + c0 + c) : 0.f);
-            if (isfinite(l)) denom += __expf(l - top);
-          }
+        for (int c0 = 0; c0 < p.E; c0 += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(row + c0);
+          if (isfinite(a.x)) denom += __expf(a.x - top);
+          if (isfinite(a.y)) denom += __expf(a.y - top);
+          if (isfinite(a.z)) denom += __expf(a.z - top);
+          if (isfinite(a.w)) denom += __expf(a.w - top);
         }
       }
       const float inv = 1.0f / denom;
-      if (t < p.T) {
+      const size_t t = (size_t)tile * BM + r;
 #pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i) {
-          if (i < p.k) {
-            p.topk_idx[(size_t)t * p.k + i] = idx[i];
-            p.topk_w[(size_t)t * p.k + i] = __expf(val[i] - top) * inv;
-          }
+      for (int i = 0; i < kMaxTopK; ++i) {
+        if (i < p.k) {
+          p.topk_idx[t * p.k + i] = idx[i];
+          p.topk_w[t * p.k + i] = __expf(val[i] - top) * inv;
         }
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&acce_bar);
+      if (bad) set_status(p.status, QSM_DEV_NONFINITE);
     }
-    if (bad) set_status(p.status, QSM_DEV_NONFINITE);
+    if (threadIdx.x == 0) p.counters[tile] = 0u;  // re-arm for the next call
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+  if (warp == 1) tc::tmem_dealloc(tmem, 256);
 }
 
 int sm_count_route() {
@@ -260,7 +335,19 @@ bool route_tc_supported(int T, int H, int E, int k) {
   return T > 64 && H % 128 == 0 && E % 16 == 0 && E >= 16 && E <= 256 && k <= 8;
 }
 
-size_t route_tc_split_bytes(int H, int E) { return (size_t)3 * E * H * 2; }
+namespace route_tc {
+// H slices: 4 when H allows it (every slice a whole number of 64-wide steps)
+int k_slices(int H) { return H % (4 * BK) == 0 ? 4 : (H % (2 * BK) == 0 ? 2 : 1); }
+inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+}  // namespace route_tc
+
+// [arrival counters][split router weight 3*E*H bf16][partials ks*T*E fp32]
+size_t route_tc_workspace_bytes(int T, int H, int E) {
+  using namespace route_tc;
+  const size_t ntiles = (size_t)(T + BM - 1) / BM;
+  return up256(ntiles * 4) + up256((size_t)3 * E * H * 2) +
+         (size_t)k_slices(H) * T * E * 4;
+}
 
 qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
                            const float* logit_bias, int T, int H, int E, int k,
@@ -269,7 +356,11 @@ qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
                            cudaStream_t stream) {
   using namespace route_tc;
   const size_t n = (size_t)E * H;
-  __nv_bfloat16* split = static_cast<__nv_bfloat16*>(split_buf);
+  const int ntiles = (T + BM - 1) / BM;
+  char* ws = static_cast<char*>(split_buf);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws);
+  __nv_bfloat16* split = reinterpret_cast<__nv_bfloat16*>(ws + up256((size_t)ntiles * 4));
+  float* part = reinterpret_cast<float*>(ws + up256((size_t)ntiles * 4) + up256(n * 2 * 3));
   const int nsm = sm_count_route();
   QSM_CUDA_TRY(launch_pdl(split_kernel, dim3(nsm), dim3(256), 0, stream, w_router,
                           split, n));
@@ -285,16 +376,19 @@ qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
   p.E = E;
   p.k = k;
   p.renorm = renormalize;
-  p.ntiles = (T + BM - 1) / BM;
+  p.ntiles = ntiles;
+  p.ks = k_slices(H);
+  p.part = part;
+  p.counters = counters;
   p.topk_idx = topk_idx;
   p.topk_w = topk_w;
   p.status = dev_status;
   const size_t smem = (size_t)kStages * (BM * BK * 2 + 256 * BK * 2) + 1024;
-  QSM_CUDA_TRY(cudaFuncSetAttribute(route_tc_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto* kern = p.ks == 4 ? route_tc_kernel<4>
+                         : (p.ks == 2 ? route_tc_kernel<2> : route_tc_kernel<1>);
+  QSM_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem));
-  const int grid = p.ntiles < nsm ? p.ntiles : nsm;
-  QSM_CUDA_TRY(launch_pdl(route_tc_kernel, dim3(grid), dim3(kThreads), smem, stream, p));
+  QSM_CUDA_TRY(launch_pdl(kern, dim3(ntiles * p.ks), dim3(kThreads), smem, stream, p));
   return QSM_OK;
 }
 
