@@ -58,6 +58,23 @@ WORKLOADS = {
 }
 
 
+def measured_traffic(workload):
+    """DRAM bytes per expert-FFN call from the committed ncu capture, or None
+    when the kernel sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "ffn_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    ent = json.load(open(p)).get("prefill" if workload == "prefill" else "decode")
+    if not ent or workload not in ("decode", "prefill"):
+        return None
+    m = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_sparse_moe_gb300", "csrc")
+    for f in ent["sources"]:
+        m.update(open(os.path.join(csrc, f), "rb").read())
+    return ent["bytes_per_launch"] if m.hexdigest() == ent["sources_sha256"] else None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -235,6 +252,7 @@ def run_ours(args, wl, rank, world):
     gu, dn = Q8_EXPERT_BYTES[qtype]
     ffn_bytes_per_layer = (n_exp / nL + 1) * (gu + dn) + 2 * T * 2048 * 2
     hbm, _, peak_kind = peaks()
+    traffic = measured_traffic(args.workload)  # DRAM bytes per FFN call (ncu)
 
     # end to end through the public API: pinned host x in, host y out
     xh = torch.stack(xs).cpu().pin_memory()
@@ -299,7 +317,7 @@ def run_ours(args, wl, rank, world):
         "roofline": ({
             "kernel": "moe_ffn_forward (d1 gate_up+SwiGLU, d2 down+combine)",
             "bound": "hbm", "achieved": achieved, "peak": hbm,
-            "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+            "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
             "bytes_per_launch": ffn_bytes_per_layer,
             "launch_ms": ffn_ms, "peak_kind": peak_kind} if T <= 64 else {
             "kernel": "moe_ffn_forward (prep, gate_up GEMM, down GEMM, finalize)",
@@ -307,7 +325,7 @@ def run_ours(args, wl, rank, world):
             "achieved": (flops_layer - 2.0 * T * sh.E * sh.H) / (ffn_ms / 1e3) / 1e12,
             "peak": tc_peak, "unit": "TFLOP/s",
             "frac": (flops_layer - 2.0 * T * sh.E * sh.H) / (ffn_ms / 1e3) / 1e12 / tc_peak,
-            "traffic": None, "flops_per_launch": flops_layer - 2.0 * T * sh.E * sh.H,
+            "traffic": traffic, "flops_per_launch": flops_layer - 2.0 * T * sh.E * sh.H,
             "launch_ms": ffn_ms, "peak_kind": peak_kind}),
         "e2e": {"value": world * T * nL / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": xh.numel() * 2,
@@ -320,50 +338,71 @@ def run_ours(args, wl, rank, world):
 
 # ----------------------------------------------------------- CPU oracle
 
-def oracle_sample(wl, layers_dev, xs_dev, budget_s=12.0, reps_max=1000):
+class OracleSampler:
     """The fp64 oracle on the host cores over a bounded sample of the
-    workload's layers; returns (tokens/s, description, cores)."""
-    import oracle
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from _helpers import bits16, oracle_q
-    T = wl["T"]
-    done_tokens, t_used, n_layers = 0, 0.0, 0
-    for Lg, x in zip(layers_dev, xs_dev):
-        q = [oracle_q(t) for t in (Lg.gate_up, Lg.down, Lg.shared_gate_up,
-                                   Lg.shared_down)]
-        xb = bits16(x)
-        wr = Lg.w_router.cpu().numpy()
-        bias = None if Lg.logit_bias is None else Lg.logit_bias.cpu().numpy()
-        toks = np.arange(T, dtype=np.int32)
-        if T > 64:  # prefill: a token sample of the full routing
-            toks = np.random.default_rng(0).choice(T, 64, replace=False).astype(np.int32)
-        t0 = time.perf_counter()
-        idx, w = oracle.route(xb, wr, Lg.shape.k, bias)
-        oracle.group(idx, Lg.shape.E, 8)
-        oracle.moe_layer(xb, idx, w, *q, tokens=toks)
-        t_used += time.perf_counter() - t0
-        done_tokens += len(toks)
-        n_layers += 1
-        del q
-        if t_used > budget_s:
-            break
-    return done_tokens / t_used, n_layers, oracle.max_threads(), t_used
+    workload: up to max_layers of its layers (weights copied to the host
+    once), each call one full layer (route, group, expert FFNs, combine) for
+    the layer's tokens (prefill: a fixed sample of 64 tokens of the full
+    routing)."""
+
+    def __init__(self, wl, layers_dev, xs_dev, max_layers=4):
+        import oracle
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from _helpers import bits16, oracle_q
+        self.oracle = oracle
+        self.layers = []
+        T = wl["T"]
+        for Lg, x in list(zip(layers_dev, xs_dev))[:max_layers]:
+            toks = np.arange(T, dtype=np.int32)
+            if T > 64:
+                toks = np.random.default_rng(0).choice(T, 64, replace=False).astype(np.int32)
+            self.layers.append(dict(
+                q=[oracle_q(t) for t in (Lg.gate_up, Lg.down, Lg.shared_gate_up,
+                                         Lg.shared_down)],
+                x=bits16(x), wr=Lg.w_router.cpu().numpy(),
+                bias=None if Lg.logit_bias is None else Lg.logit_bias.cpu().numpy(),
+                k=Lg.shape.k, E=Lg.shape.E, toks=toks))
+
+    def run(self, budget_s):
+        """Calls cycling over the sampled layers until budget_s seconds of
+        oracle time; returns (tokens/s, seconds, calls)."""
+        orc = self.oracle
+        tokens, t_used, calls = 0, 0.0, 0
+        while t_used < budget_s:
+            L = self.layers[calls % len(self.layers)]
+            t0 = time.perf_counter()
+            idx, w = orc.route(L["x"], L["wr"], L["k"], L["bias"])
+            orc.group(idx, L["E"], 8)
+            orc.moe_layer(L["x"], idx, w, *L["q"], tokens=L["toks"])
+            t_used += time.perf_counter() - t0
+            tokens += len(L["toks"])
+            calls += 1
+        return tokens / t_used, t_used, calls
+
+    def describe(self, seconds, calls):
+        return (f"{len(self.layers)} layer(s) of the workload, {calls} call(s) cycling "
+                f"over them, {seconds:.1f} s of fp64 oracle (route, group, expert "
+                f"FFNs, combine; {len(self.layers[0]['toks'])} token(s) per call)")
 
 
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    vals = []
-    n_l = 0
-    # each step: a bounded sample (the first layers of the workload)
+    Ls = [synth.draw_layer(wl["shape"], dev, seed=0, layer=l, zipf=wl["zipf"])
+          for l in range(min(wl["layers"], 2))]
+    xs = [synth.draw_x(wl["T"], wl["shape"].H, dev, 0, l) for l in range(len(Ls))]
+    sampler = OracleSampler(wl, Ls, xs, max_layers=2)
+    del Ls
+    # each step a bounded sample: the whole run stays within about 90 s
+    step_s = min(6.0, max(0.05, 90.0 / (args.warmup + args.steps)))
+    vals, secs, calls = [], 0.0, 0
     for s in range(args.warmup + args.steps):
-        Ls = [synth.draw_layer(wl["shape"], dev, seed=0, layer=l, zipf=wl["zipf"])
-              for l in range(min(wl["layers"], 2))]
-        xs = [synth.draw_x(wl["T"], wl["shape"].H, dev, 0, l) for l in range(len(Ls))]
-        v, n_l, cores, t = oracle_sample(wl, Ls, xs, budget_s=6.0)
+        v, t, c = sampler.run(step_s)
         if s >= args.warmup:
             vals.append(v)
+            secs += t
+            calls += c
     value = statistics.median(vals)
     return {
         "impl": "reference", "metric": "MoE-layer tokens/s", "value": value,
@@ -372,10 +411,10 @@ def run_reference(args, wl, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl["desc"], "tokens_per_layer": wl["T"],
                    "layers": wl["layers"]},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
-                         "kind": "oracle",
-                         "sample": f"{n_l} layer(s) per step of the workload "
-                                   "(route, group, expert FFNs, combine; fp64)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s",
+                         "cores": sampler.oracle.max_threads(), "kind": "oracle",
+                         "sample": sampler.describe(secs, calls) +
+                                   f"; {step_s:.2f} s per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -409,11 +448,11 @@ def main():
     else:
         res, (syn, fwds, xs) = run_ours(args, wl, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
-            v, n_l, cores, t = oracle_sample(wl, syn, xs, budget_s=10.0)
+            sampler = OracleSampler(wl, syn, xs, max_layers=4)
+            v, t, calls = sampler.run(12.0)
             res["cpu_baseline"] = {
-                "value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                "sample": f"{n_l} of {wl['layers']} layers, {t:.1f} s of fp64 "
-                          "oracle (route, group, expert FFNs, combine)"}
+                "value": v, "unit": "tokens/s", "cores": sampler.oracle.max_threads(),
+                "kind": "oracle", "sample": sampler.describe(t, calls)}
     if rank == 0 and res is not None:
         print(json.dumps(res))
     if world > 1:

@@ -643,7 +643,7 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
 
   constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpC, kGateUpB, kGateUpA>();
   constexpr size_t smem2 = gemm_smem<kDown, kDownC, kDownB, kDownA>();
-  static_assert(smem1 <= 220 * 1024 && smem2 <= 220 * 1024, "shared memory");
+  static_assert(smem1 <= 225 * 1024 && smem2 <= 225 * 1024, "shared memory");
   auto* k1 = moe_prefill_gemm<kGateUp, kGateUpC, kGateUpB, kGateUpA>;
   auto* k2 = moe_prefill_gemm<kDown, kDownC, kDownB, kDownA>;
   QSM_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
