@@ -55,6 +55,8 @@ WORKLOADS = {
                       desc="batched decode T=64, 40 layers, affine-4 g64"),
     "prefill": dict(shape=synth.QWEN, T=4096, layers=1, zipf="noise",
                     desc="prefill T=4096, 1 layer, Zipf-offset routing, Q8_0"),
+    "prefill_a4": dict(shape=synth.QWEN_A4, T=4096, layers=1, zipf="noise",
+                       desc="prefill T=4096, 1 layer, Zipf-offset routing, affine-4 g64"),
 }
 
 

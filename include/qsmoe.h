@@ -226,7 +226,9 @@ QSM_API size_t moe_ffn_workspace_bytes(const qsm_moe_layer* L, int32_t T);
  *              moe_ffn_tile_rows(T)
  *   workspace  >= moe_ffn_workspace_bytes(L, T) bytes, no initial content.
  * T <= 64 runs the decode kernels (weight streaming GEMV), larger T the
- * grouped-GEMM prefill kernels. */
+ * grouped-GEMM prefill kernels (tcgen05, weights of either type expanded to
+ * fp16 tile by tile on chip; they need H % 256 == 0 and I % 128 == 0, else
+ * QSM_ERR_UNSUPPORTED). */
 QSM_API qsm_status moe_ffn_forward(const qsm_moe_layer* L, const uint16_t* x,
                            int32_t T, const int32_t* topk_idx,
                            const float* topk_w, const qsm_grouping* g,

@@ -46,8 +46,14 @@
 // its own latency needs.  Two accumulator buffers in tensor memory
 // (mbarriers: full / empty) connect MMA and epilogue.
 //
-// Precision: weights are fp16(code * scale) (relative rounding 2^-11),
-// tokens are exact; products are accumulated in fp32.
+// Weights: Q8_0 (int8 codes, an fp16 scale per 32) or affine-4 (8 codes
+// per 32-bit word, lowest nibble first along K, fp16 scale and bias per 64:
+// "Dequantizing weights during matrix multiplication").  A 64-wide K step
+// is 64 bytes of Q8_0 codes or 32 bytes of affine-4 codes per row.
+//
+// Precision: weights are fp16(code * scale) or fp16(code * scale + bias)
+// (one rounding, relative 2^-11), tokens are exact; products are
+// accumulated in fp32.
 #include "tc_common.cuh"
 
 namespace qsm {
@@ -68,8 +74,10 @@ struct Params {
   CUtensorMap codes_sh;   // shared expert's codes [R, K] u8, box {64, 128}
   CUtensorMap bmap[4];    // token rows [T*k + T, K] fp16 (gate_up: grouped
                           // x; down: h), boxes {64, 128 / 64 / 32 / 16}
-  const __half* scales;   // [E*R, K/32]
+  const __half* scales;   // [E*R, K/32] (Q8_0) or [E*R, K/64] (affine-4)
   const __half* scales_sh;
+  const __half* biases;   // [E*R, K/64] (affine-4)
+  const __half* biases_sh;
   int R, K;               // rows per expert and reduction length
   int T, k, I, H;
   const int32_t* perm;
@@ -137,13 +145,34 @@ __device__ __forceinline__ void red_add_v4(float* y, float v0, float v1, float v
                : "memory");
 }
 
-template <int MODE, int CR, int BR, int AST>
+// One 32-bit word of affine-4 codes (K order k..k+7, lowest nibble first)
+// -> eight fp16 s*q + b in K order (one rounding each: q is exact in fp16).
+__device__ __forceinline__ uint4 a4_word_to_f16x8(uint32_t w, __half2 s2, __half2 b2) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;         // q0 q2 q4 q6
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // q1 q3 q5 q7
+  const uint32_t t0 = __byte_perm(lo, hi, 0x5140);  // q0 q1 q2 q3
+  const uint32_t t1 = __byte_perm(lo, hi, 0x7362);  // q4 q5 q6 q7
+  // each code under the fp16 exponent of 1024: 1024 + q
+  uint32_t v[4] = {__byte_perm(t0, 0x64646464u, 0x4140), __byte_perm(t0, 0x64646464u, 0x4342),
+                   __byte_perm(t1, 0x64646464u, 0x4140), __byte_perm(t1, 0x64646464u, 0x4342)};
+  const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v[i]), k1024);
+    h = __hfma2(h, s2, b2);
+    v[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+template <int MODE, int QT, int CR, int BR, int AST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_prefill_gemm(const __grid_constant__ Params p) {
   constexpr int NA = 2;                        // weight tiles per K step
   constexpr int A_BYTES = BM * BK * 2;         // fp16, 128B swizzle
   constexpr int B_BYTES = BN * BK * 2;
-  constexpr int C_BYTES = BM * BK;             // int8 codes
+  constexpr int KB = QT == QSM_Q8_0 ? BK : BK / 2;  // code bytes per row and K step
+  constexpr int C_BYTES = BM * KB;
   constexpr int A_STAGE = NA * A_BYTES;        // dequantised ring
   constexpr int C_STAGE = NA * C_BYTES;        // code ring
   extern __shared__ unsigned char smem_raw[];
@@ -219,7 +248,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
           mbar_arrive_expect_tx(&c_full[c], C_STAGE);
 #pragma unroll
           for (int a = 0; a < NA; ++a)
-            tc::tma_load_2d(cdst + a * C_BYTES, cm, ks * BK, arow[a], &c_full[c]);
+            tc::tma_load_2d(cdst + a * C_BYTES, cm, ks * KB, arow[a], &c_full[c]);
           ++f;
           c = (c + 1 == CR) ? 0 : c + 1;
         }
@@ -318,20 +347,29 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       const TileInfo ti = tile_info(p, tau);
       const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
       const int row = ebase + weight_row0(p, MODE, sub, am) + rw;
-      // this row's block scales: one 4-byte pair per K step (4-byte aligned
-      // for any K % 64 == 0), fetched one group of 8 K steps ahead
-      const uint32_t* sc = reinterpret_cast<const uint32_t*>(
-          (ti.e < 0 ? p.scales_sh : p.scales) + (size_t)row * (p.K / 32));
+      // this row's block constants, one 32-bit word per K step, fetched one
+      // group of 8 K steps ahead: Q8_0 the two block scales (4-byte aligned
+      // for any K % 64 == 0), affine-4 the group's scale | bias << 16
+      const __half* scb = (ti.e < 0 ? p.scales_sh : p.scales) +
+                          (size_t)row * (p.K / (QT == QSM_Q8_0 ? 32 : 64));
+      const __half* bib = QT == QSM_Q8_0 ? nullptr
+                                         : (ti.e < 0 ? p.biases_sh : p.biases) +
+                                               (size_t)row * (p.K / 64);
+      auto consts = [&](int ks) -> uint32_t {
+        if (QT == QSM_Q8_0) return __ldg(reinterpret_cast<const uint32_t*>(scb) + ks);
+        return (uint32_t)__half_as_ushort(__ldg(scb + ks)) |
+               ((uint32_t)__half_as_ushort(__ldg(bib + ks)) << 16);
+      };
       uint32_t nx[8];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) nx[jj] = jj < ksteps ? __ldg(sc + jj) : 0u;
+      for (int jj = 0; jj < 8; ++jj) nx[jj] = jj < ksteps ? consts(jj) : 0u;
       bool ok = true;
       for (int kg = 0; kg < ksteps && ok; kg += 8) {
         uint32_t cur[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           cur[jj] = nx[jj];
-          nx[jj] = kg + 8 + jj < ksteps ? __ldg(sc + kg + 8 + jj) : 0u;
+          nx[jj] = kg + 8 + jj < ksteps ? consts(kg + 8 + jj) : 0u;
         }
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
@@ -342,9 +380,21 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
             break;
           }
           const uint32_t sc2 = cur[jj];
-          const unsigned char* codes = cring + c * C_STAGE + am * C_BYTES + rw * BK;
+          const unsigned char* codes = cring + c * C_STAGE + am * C_BYTES + rw * KB;
           unsigned char* arow_s = aring + a * A_STAGE + am * A_BYTES + (rw >> 3) * 1024 +
                                   (rw & 7) * 128;
+          if (QT == QSM_AFFINE4_G64) {
+            // word i holds K 8i..8i+7: one 16-byte output chunk each
+            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(sc2 & 0xffffu)));
+            const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(sc2 >> 16)));
+            const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(codes + 16);
+            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(arow_s + ((i ^ (rw & 7)) << 4)) =
+                  a4_word_to_f16x8(wv[i], s2, b2);
+          } else {
 #pragma unroll
           for (int j = 0; j < kInChunks; ++j) {
             // chunk order per row: conflict-free shared-memory banks for the
@@ -369,6 +419,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
                 make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(arow_s + ((oc1 ^ (rw & 7)) << 4)) =
                 make_uint4(o[4], o[5], o[6], o[7]);
+          }
           }
           tc::mbar_arrive(&c_empty[c]);
           tc::fence_async_smem();
@@ -532,12 +583,15 @@ finalize_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y,
 constexpr int kGateUpC = 4, kGateUpB = 3, kGateUpA = 3;
 constexpr int kDownC = 4, kDownB = 3, kDownA = 3;
 
-template <int MODE, int CR, int BR, int AST>
+template <int QT, int CR, int BR, int AST>
 constexpr size_t gemm_smem() {
   constexpr int NA = 2;
+  constexpr int KB = QT == QSM_Q8_0 ? BK : BK / 2;
   return (size_t)AST * NA * BM * BK * 2 + (size_t)BR * BN * BK * 2 +
-         (size_t)CR * NA * BM * BK + 1024;
+         (size_t)CR * NA * BM * KB + 1024;
 }
+
+
 
 int sm_count() {
   static int n[64] = {0};
@@ -550,6 +604,23 @@ int sm_count() {
     n[dev] = v > 0 ? v : 148;
   }
   return n[dev];
+}
+
+template <int QT>
+qsm_status launch_gemms(const Params& p1, const Params& p2, cudaStream_t stream) {
+  constexpr size_t smem1 = gemm_smem<QT, kGateUpC, kGateUpB, kGateUpA>();
+  constexpr size_t smem2 = gemm_smem<QT, kDownC, kDownB, kDownA>();
+  static_assert(smem1 <= 225 * 1024 && smem2 <= 225 * 1024, "shared memory");
+  auto* k1 = moe_prefill_gemm<kGateUp, QT, kGateUpC, kGateUpB, kGateUpA>;
+  auto* k2 = moe_prefill_gemm<kDown, QT, kDownC, kDownB, kDownA>;
+  QSM_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem1));
+  QSM_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem2));
+  const int nsm = sm_count();
+  QSM_CUDA_TRY(launch_pdl(k1, dim3(nsm), dim3(kThreads), smem1, stream, p1));
+  QSM_CUDA_TRY(launch_pdl(k2, dim3(nsm), dim3(kThreads), smem2, stream, p2));
+  return QSM_OK;
 }
 
 struct WsLayout {
@@ -571,7 +642,8 @@ WsLayout ws_layout(const qsm_moe_layer* L, int T) {
 }  // namespace prefill
 
 bool prefill_supported(const qsm_moe_layer* L) {
-  return L->gate_up.qtype == QSM_Q8_0 && L->H % 256 == 0 && L->I % 128 == 0;
+  return (L->gate_up.qtype == QSM_Q8_0 || L->gate_up.qtype == QSM_AFFINE4_G64) &&
+         L->H % 256 == 0 && L->I % 128 == 0;
 }
 
 size_t prefill_ffn_workspace_bytes(const qsm_moe_layer* L, int T) {
@@ -595,12 +667,16 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   QSM_CUDA_TRY(launch_pdl(prep_kernel, dim3(4 * nsm), dim3(256), 0, stream, x,
                           (const int32_t*)g->perm, T, k, H, xall, yacc, dev_status));
 
+  // code tiles: 64 K per step = 64 bytes (Q8_0) or 32 bytes (affine-4) a row
+  const bool a4 = L->gate_up.qtype == QSM_AFFINE4_G64;
+  const int kb = a4 ? BK / 2 : BK;
+  auto code_cols = [&](int K) { return (uint64_t)(a4 ? K / 2 : K); };
   Params p1 = {};
   bool ok = true;
   ok &= tc::make_map_2d(&p1.codes, L->gate_up.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                        (uint64_t)E * 2 * I, H, BK, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        (uint64_t)E * 2 * I, code_cols(H), kb, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok &= tc::make_map_2d(&p1.codes_sh, L->shared_gate_up.codes,
-                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, H, BK, BM,
+                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, code_cols(H), kb, BM,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
   for (int m = 0; m < 4; ++m)
     ok &= tc::make_map_2d(&p1.bmap[m], xall, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, H,
@@ -608,6 +684,8 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   if (!ok) return QSM_ERR_CUDA;
   p1.scales = reinterpret_cast<const __half*>(L->gate_up.scales);
   p1.scales_sh = reinterpret_cast<const __half*>(L->shared_gate_up.scales);
+  p1.biases = reinterpret_cast<const __half*>(L->gate_up.biases);
+  p1.biases_sh = reinterpret_cast<const __half*>(L->shared_gate_up.biases);
   p1.R = 2 * I;
   p1.K = H;
   p1.T = T;
@@ -627,9 +705,9 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
 
   Params p2 = p1;
   ok &= tc::make_map_2d(&p2.codes, L->down.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                        (uint64_t)E * H, I, BK, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                        (uint64_t)E * H, code_cols(I), kb, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok &= tc::make_map_2d(&p2.codes_sh, L->shared_down.codes,
-                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, I, BK, BM,
+                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, code_cols(I), kb, BM,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
   for (int m = 0; m < 4; ++m)
     ok &= tc::make_map_2d(&p2.bmap[m], hbuf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, I,
@@ -637,21 +715,15 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   if (!ok) return QSM_ERR_CUDA;
   p2.scales = reinterpret_cast<const __half*>(L->down.scales);
   p2.scales_sh = reinterpret_cast<const __half*>(L->shared_down.scales);
+  p2.biases = reinterpret_cast<const __half*>(L->down.biases);
+  p2.biases_sh = reinterpret_cast<const __half*>(L->shared_down.biases);
   p2.R = H;
   p2.K = I;
   p2.nsub = H / (2 * BM);
 
-  constexpr size_t smem1 = gemm_smem<kGateUp, kGateUpC, kGateUpB, kGateUpA>();
-  constexpr size_t smem2 = gemm_smem<kDown, kDownC, kDownB, kDownA>();
-  static_assert(smem1 <= 225 * 1024 && smem2 <= 225 * 1024, "shared memory");
-  auto* k1 = moe_prefill_gemm<kGateUp, kGateUpC, kGateUpB, kGateUpA>;
-  auto* k2 = moe_prefill_gemm<kDown, kDownC, kDownB, kDownA>;
-  QSM_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem1));
-  QSM_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem2));
-  QSM_CUDA_TRY(launch_pdl(k1, dim3(nsm), dim3(kThreads), smem1, stream, p1));
-  QSM_CUDA_TRY(launch_pdl(k2, dim3(nsm), dim3(kThreads), smem2, stream, p2));
+  const qsm_status st = a4 ? launch_gemms<QSM_AFFINE4_G64>(p1, p2, stream)
+                           : launch_gemms<QSM_Q8_0>(p1, p2, stream);
+  if (st != QSM_OK) return st;
   QSM_CUDA_TRY(launch_pdl(finalize_kernel, dim3(2 * nsm), dim3(256), 0, stream,
                           (const float*)yacc, y, y32, (size_t)T * H / 4));
   return QSM_OK;

@@ -210,3 +210,61 @@ def test_prefill_repeat_is_stable(qsm):
     torch.cuda.synchronize()
     rel = (a - fwd.y_f32).abs().max().item() / a.abs().max().item()
     assert rel < 1e-5
+
+
+# ------------------------------------------------- affine-4 prefill (NEXT-1)
+
+@pytest.mark.parametrize("T", [65, 300, 1000])
+def test_qwen_affine4_prefill(qsm, T):
+    """The grouped tcgen05 GEMMs with affine-4 weights (fp16(s*q + b) tiles
+    expanded on chip) against the fp64 oracle on sampled tokens."""
+    rng = np.random.default_rng(T + 7)
+    toks = np.sort(rng.choice(T, min(T, 48), replace=False)).astype(np.int32)
+    _check(qsm, synth.QWEN_A4, T, seed=4, tokens=toks)
+
+
+@pytest.mark.parametrize("T", [16, 100])
+def test_affine4_cross_path(qsm, T):
+    """Affine-4: the decode and the prefill kernels both meet the tolerance
+    on the same tokens and agree with each other within it."""
+    from _helpers import bits16, tol_metric
+    import oracle as orc
+    shape = synth.QWEN_A4
+    Lg, q, wr, bias = layer(shape, 5, None)
+    x = x_for(shape, T, 91 + T, Lg, wr, bias)
+    outs = {}
+    for path in ("decode", "prefill"):
+        qsm.force_path(path)
+        try:
+            fwd = run(qsm, Lg, x)
+        finally:
+            qsm.force_path("auto")
+        assert fwd.dev_status.item() == 0
+        outs[path] = fwd.y_f32.cpu().numpy().astype(np.float64)
+    idx_o, w_o = oracle_route(x, wr, bias, shape.k)
+    ref = orc.moe_layer(bits16(x), idx_o, w_o, *q)
+    for path, y32 in outs.items():
+        assert tol_metric(y32, ref) <= TOL, path
+    assert tol_metric(outs["decode"], outs["prefill"]) <= TOL
+
+
+def test_affine4_prefill_zipf_t2048_sampled(qsm):
+    """Affine-4 prefill with uneven groups (Zipf offset): routing bit-exact,
+    the output checked on tokens of the largest and smallest groups."""
+    shape = synth.QWEN_A4
+    Lg, q, wr, bias = layer(shape, 6, "noise")
+    T = 2048
+    x = x_for(shape, T, 2048, Lg, wr, bias)
+    fwd = run(qsm, Lg, x)
+    assert fwd.dev_status.item() == 0
+    idx_o, w_o = oracle_route(x, wr, bias, shape.k)
+    assert np.array_equal(fwd.topk_idx.cpu().numpy(), idx_o)
+    counts = np.bincount(idx_o.ravel(), minlength=shape.E)
+    big = np.argmax(counts)
+    small = np.where(counts == counts[counts > 0].min())[0][0]
+    pick = {int(np.where((idx_o == big).any(1))[0][0]),
+            int(np.where((idx_o == small).any(1))[0][0])}
+    pick |= set(np.random.default_rng(2).choice(T, 24, replace=False).tolist())
+    toks = np.array(sorted(pick), np.int32)
+    err, _ = check_layer_output(fwd.y, fwd.y_f32, x, idx_o, w_o, q, toks)
+    assert err <= TOL
