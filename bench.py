@@ -159,6 +159,26 @@ def build_layers(qsm, wl, device, seed, fuse=True):
     return layers, xs, fwds, syn
 
 
+class ChunkedLayer:
+    """One layer through moe_layer_forward in chunks, outputs and workspace
+    allocated once."""
+
+    def __init__(self, qsm, L, T, chunk, device):
+        self.qsm, self.L, self.chunk = qsm, L, chunk
+        self.y = torch.empty((T, L.H), dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty((T, L.k), dtype=torch.int32, device=device)
+        self.w = torch.empty((T, L.k), dtype=torch.float32, device=device)
+        self.ws = torch.zeros(qsm.layer_workspace_bytes(L, T, chunk), dtype=torch.uint8,
+                              device=device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def __call__(self, x, stream=None):
+        self.qsm.moe_layer_forward(self.L, x, self.chunk, y=self.y, topk_idx=self.idx,
+                                   topk_w=self.w, workspace=self.ws,
+                                   dev_status=self.dev_status, stream=stream)
+        return self.y
+
+
 def touched_bytes(layers, fwds, qtype):
     """Distinct touched experts (from the device routing) + shared +
     router + x + y, per step."""
@@ -182,15 +202,23 @@ def run_ours(args, wl, rank, world):
     T, nL = wl["T"], wl["layers"]
     stream = torch.cuda.Stream(device=dev)
 
+    calls = fwds
+    if args.chunk:  # the whole layer per call, in chunks of args.chunk tokens
+        calls = [ChunkedLayer(qsm, L, T, args.chunk, dev) for L in layers]
+
     def step(s):
-        for f, x in zip(fwds, xs):
+        for f, x in zip(calls, xs):
             f(x, stream=s)
 
     # warm-up (also builds the library and fixes the routing)
     with torch.cuda.stream(stream):
         step(stream)
+    if args.chunk:  # the unchunked calls give the routing counts for the bytes
+        with torch.cuda.stream(stream):
+            for f, x in zip(fwds, xs):
+                f(x, stream=stream)
     torch.cuda.synchronize()
-    for f in fwds:
+    for f in list(fwds) + (list(calls) if args.chunk else []):
         assert f.dev_status.item() == 0, "device status set"
     graph = torch.cuda.CUDAGraph()
     n0 = qsm.launch_count()
@@ -255,6 +283,10 @@ def run_ours(args, wl, rank, world):
     ffn_bytes_per_layer = (n_exp / nL + 1) * (gu + dn) + 2 * T * 2048 * 2
     hbm, _, peak_kind = peaks()
     traffic = measured_traffic(args.workload)  # DRAM bytes per FFN call (ncu)
+    if args.chunk:
+        # the dominant launch group is the whole chunked layer call
+        ffn_ms = ms / nL
+        traffic = None
 
     # end to end through the public API: pinned host x in, host y out
     xh = torch.stack(xs).cpu().pin_memory()
@@ -268,7 +300,7 @@ def run_ours(args, wl, rank, world):
         e0.record(stream)
         with torch.cuda.stream(stream):
             xd.copy_(xh, non_blocking=True)
-            for l, f in enumerate(fwds):
+            for l, f in enumerate(calls):
                 f(xd[l], stream=stream)
                 yh[l].copy_(f.y, non_blocking=True)
         e1.record(stream)
@@ -307,6 +339,10 @@ def run_ours(args, wl, rank, world):
         "config": {"workload": wl["desc"], "tokens_per_layer": T,
                    "layers": nL, "parallelism": f"replicas x{world}",
                    "route_group": args.route_group if T <= 8 else "separate",
+                   "chunk_tokens": args.chunk or None,
+                   "workspace_bytes_per_layer": int(
+                       calls[0].ws.numel() if args.chunk else
+                       fwds[0].route_ws.numel() + fwds[0].ffn_ws.numel()),
                    "l2": "inputs larger than L2 (touched weights per step "
                          f"{step_bytes / 1e9:.2f} GB)"},
         "layer_roofline": {
@@ -322,7 +358,10 @@ def run_ours(args, wl, rank, world):
             "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
             "bytes_per_launch": ffn_bytes_per_layer,
             "launch_ms": ffn_ms, "peak_kind": peak_kind} if T <= 64 else {
-            "kernel": "moe_ffn_forward (prep, gate_up GEMM, down GEMM, finalize)",
+            "kernel": ("moe_ffn_forward (prep, gate_up GEMM, down GEMM, finalize)"
+                       if not args.chunk else
+                       f"moe_layer_forward in chunks of {args.chunk} tokens "
+                       "(route, group, FFN per chunk)"),
             "bound": "tensor",
             "achieved": (flops_layer - 2.0 * T * sh.E * sh.H) / (ffn_ms / 1e3) / 1e12,
             "peak": tc_peak, "unit": "TFLOP/s",
@@ -433,6 +472,9 @@ def main():
     ap.add_argument("--route-group", default="fused", choices=["fused", "separate"],
                     help="for T <= 8: one fused route+group launch, or the two "
                          "separate launches")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="run each layer through moe_layer_forward in chunks of "
+                         "this many tokens (chunked prefill)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (profiling runs only)")
     args = ap.parse_args()
@@ -445,6 +487,8 @@ def main():
     if args.layers:
         wl["layers"] = args.layers
         wl["desc"] += f" (layer count overridden: {args.layers})"
+    if args.chunk:
+        wl["desc"] += f", chunks of {args.chunk} tokens"
     if args.impl == "reference":
         res = run_reference(args, wl, rank, world)
     else:

@@ -236,6 +236,37 @@ QSM_API qsm_status moe_ffn_forward(const qsm_moe_layer* L, const uint16_t* x,
                            size_t workspace_bytes, int32_t* dev_status,
                            cudaStream_t stream);
 
+/* ------------------------------------------------------------ whole layer */
+
+/* Bytes of workspace moe_layer_forward needs for T tokens in chunks of at
+ * most `chunk` tokens (sized for one chunk: the router's, the grouping's
+ * and the FFN's workspaces of the largest chunk).  0 if the layer is
+ * unsupported or an argument is invalid. */
+QSM_API size_t moe_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T,
+                                         int32_t chunk);
+
+/* The whole layer: moe_route -> moe_group_tokens -> moe_ffn_forward over the
+ * tokens in consecutive chunks of at most `chunk` tokens, all enqueued on
+ * `stream` [Perplexity page, "Qwen creates three distinct workload shapes"
+ * (long prompts in chunks) and "Keeping expert routing on the GPU"].  A
+ * token's routing does not depend on the chunking; its output differs
+ * between chunkings at most by the order of the prefill combine's fp32
+ * additions (or by the decode / prefill kernel choice of its chunk's size).
+ *   x [T, H] bf16;  w_router [E, H] fp32;  logit_bias [E] fp32 or NULL;
+ *   topk_idx [T, k] int32 and topk_w [T, k] fp32 (out);  y [T, H] bf16 (out);
+ *   y_f32 [T, H] fp32 (out) or NULL;
+ *   workspace  >= moe_layer_workspace_bytes(L, T, chunk) bytes; it must hold
+ *              zeros before its first use, and every call leaves it so.
+ * Errors as for the three calls. */
+QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
+                                     int32_t T, int32_t chunk,
+                                     const float* w_router,
+                                     const float* logit_bias, int32_t renormalize,
+                                     int32_t* topk_idx, float* topk_w,
+                                     uint16_t* y, float* y_f32, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_status,
+                                     cudaStream_t stream);
+
 /* moe_ffn_forward without a workspace argument, for callers that cannot
  * allocate device memory (code running inside another runtime's memory
  * pool, latency-critical threads where an allocation and the device

@@ -100,6 +100,11 @@ def lib() -> ctypes.CDLL:
             L.qsm_abi_version.restype = i32
             L.qsm_debug_force_path.argtypes = [i32]
             L.qsm_debug_force_path.restype = st
+            L.moe_layer_workspace_bytes.argtypes = [ctypes.POINTER(MoELayerC), i32, i32]
+            L.moe_layer_workspace_bytes.restype = sz
+            L.moe_layer_forward.argtypes = [ctypes.POINTER(MoELayerC), P, i32, i32, P,
+                                            P, i32, P, P, P, P, P, sz, P, P]
+            L.moe_layer_forward.restype = st
             L.qsm_launch_count.argtypes = []
             L.qsm_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -324,6 +329,39 @@ def moe_ffn_forward_noalloc(layer: Layer, x: torch.Tensor,
         ctypes.byref(gc), _p(y), _p(y_f32 if y_f32 is not False else None),
         _p(dev_status), _stream(stream)), "moe_ffn_forward_noalloc")
     return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None)
+
+
+def layer_workspace_bytes(layer: Layer, T: int, chunk: int) -> int:
+    return int(lib().moe_layer_workspace_bytes(ctypes.byref(layer.c), T, chunk))
+
+
+def moe_layer_forward(layer: Layer, x: torch.Tensor, chunk: int, renormalize=True,
+                      y=None, y_f32=None, topk_idx=None, topk_w=None,
+                      workspace=None, dev_status=None, stream=None):
+    """The whole layer (route -> group -> FFN) in chunks of at most `chunk`
+    tokens on one workspace sized for a chunk (zero-initialised once).
+    Returns (y, y_f32 or None, topk_idx, topk_w)."""
+    T, H = x.shape
+    dev = x.device
+    k = layer.k
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if y_f32 is True:
+        y_f32 = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(max(layer_workspace_bytes(layer, T, chunk), 256),
+                                dtype=torch.uint8, device=dev)
+    dev_status = _status(dev_status, dev)
+    _check(lib().moe_layer_forward(
+        ctypes.byref(layer.c), _p(_u16(x)), T, chunk, _p(layer.w_router),
+        _p(layer.logit_bias), int(bool(renormalize)), _p(topk_idx), _p(topk_w),
+        _p(y), _p(y_f32 if y_f32 is not False else None), _p(workspace),
+        workspace.numel(), _p(dev_status), _stream(stream)), "moe_layer_forward")
+    return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None), topk_idx, topk_w
 
 
 def force_path(mode: str | int) -> None:
