@@ -70,6 +70,8 @@ def _load():
                                         P, P]
             lib.orc_router_logits.argtypes = [P, P, P, i32, i32, i32, P]
             lib.orc_topk.argtypes = [P, i32, i32, i32, i32, P, P]
+            lib.orc_topk_sel.argtypes = [P, P, i32, i32, i32, i32, P, P]
+            lib.orc_shared_gate.argtypes = [P, P, i32, i32, P]
             lib.orc_group.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P]
             lib.orc_group.restype = ctypes.c_int
             lib.orc_silu.argtypes = [ctypes.c_double]
@@ -82,6 +84,11 @@ def _load():
                                           ctypes.POINTER(_QMat),
                                           ctypes.POINTER(_QMat),
                                           ctypes.POINTER(_QMat), P, i32, P]
+            lib.orc_moe_layer_ex.argtypes = [P, i32, P, P, i32,
+                                             ctypes.POINTER(_QMat),
+                                             ctypes.POINTER(_QMat),
+                                             ctypes.POINTER(_QMat),
+                                             ctypes.POINTER(_QMat), P, P, i32, P]
             lib.orc_q8_gemv.argtypes = [P, P, P, i32, i32, P]
             lib.orc_max_threads.restype = ctypes.c_int
             lib.orc_set_threads.argtypes = [ctypes.c_int]
@@ -192,8 +199,38 @@ def topk(logits, k: int, renormalize: bool = True):
     return idx, w
 
 
-def route(x_bf16, w_router, k: int, bias=None, renormalize: bool = True):
-    return topk(router_logits(x_bf16, w_router, bias), k, renormalize)
+def topk_sel(sel_logits, weight_logits, k: int, renormalize: bool = True):
+    """Top k by sel_logits, routing weights from weight_logits."""
+    s = np.ascontiguousarray(sel_logits, dtype=np.float64)
+    w = np.ascontiguousarray(weight_logits, dtype=np.float64)
+    T, E = s.shape
+    assert w.shape == (T, E)
+    idx = np.empty((T, k), np.int32)
+    out = np.empty((T, k), np.float64)
+    _load().orc_topk_sel(_ptr(s), _ptr(w), T, E, k, int(bool(renormalize)), _ptr(idx),
+                         _ptr(out))
+    return idx, out
+
+
+def route(x_bf16, w_router, k: int, bias=None, renormalize: bool = True,
+          bias_select_only: bool = False):
+    """Router: logits + bias select the experts; the weights come from the
+    same logits, or from the logits without the bias (bias_select_only)."""
+    sel = router_logits(x_bf16, w_router, bias)
+    if bias is None or not bias_select_only:
+        return topk(sel, k, renormalize)
+    return topk_sel(sel, router_logits(x_bf16, w_router, None), k, renormalize)
+
+
+def shared_gate(x_bf16, w_sg) -> np.ndarray:
+    """g[t] = sigmoid(x[t] . w_sg) in fp64."""
+    x = _u16(x_bf16)
+    T, H = x.shape
+    w = np.ascontiguousarray(w_sg, dtype=np.float32)
+    assert w.shape == (H,)
+    g = np.empty(T, np.float64)
+    _load().orc_shared_gate(_ptr(x), _ptr(w), T, H, _ptr(g))
+    return g
 
 
 def group(topk_idx, E: int, tile_rows: int):
@@ -235,8 +272,9 @@ def expert_ffn(gate_up: QWeights, down: QWeights, e: int, x: np.ndarray):
 
 def moe_layer(x_bf16, topk_idx, topk_w, gate_up: QWeights, down: QWeights,
               shared_gate_up: QWeights, shared_down: QWeights,
-              tokens=None) -> np.ndarray:
-    """fp64 layer output for `tokens` (default: all), shape [len(tokens), H]."""
+              tokens=None, shared_w=None) -> np.ndarray:
+    """fp64 layer output for `tokens` (default: all), shape [len(tokens), H];
+    shared_w [T] scales the shared expert per token (default 1)."""
     x = _u16(x_bf16)
     T, H = x.shape
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
@@ -245,9 +283,17 @@ def moe_layer(x_bf16, topk_idx, topk_w, gate_up: QWeights, down: QWeights,
     toks = np.arange(T, dtype=np.int32) if tokens is None else \
         np.ascontiguousarray(tokens, dtype=np.int32)
     y = np.empty((len(toks), H), np.float64)
-    _load().orc_moe_layer(_ptr(x), H, _ptr(idx), _ptr(w), k, gate_up.struct,
-                          down.struct, shared_gate_up.struct,
-                          shared_down.struct, _ptr(toks), len(toks), _ptr(y))
+    if shared_w is None:
+        _load().orc_moe_layer(_ptr(x), H, _ptr(idx), _ptr(w), k, gate_up.struct,
+                              down.struct, shared_gate_up.struct,
+                              shared_down.struct, _ptr(toks), len(toks), _ptr(y))
+    else:
+        sw = np.ascontiguousarray(shared_w, dtype=np.float64)
+        assert sw.shape == (T,)
+        _load().orc_moe_layer_ex(_ptr(x), H, _ptr(idx), _ptr(w), k, gate_up.struct,
+                                 down.struct, shared_gate_up.struct,
+                                 shared_down.struct, _ptr(sw), _ptr(toks), len(toks),
+                                 _ptr(y))
     return y
 
 

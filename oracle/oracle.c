@@ -161,30 +161,68 @@ static int orc_cmp_scored(const void* pa, const void* pb) {
   return (a->e < b->e) ? -1 : (a->e > b->e);
 }
 
-/* Select the k highest-scoring experts of every token (full sort by logit
- * descending, ties to the lower index) and their routing weights:
- *   renormalize=1: w_j = exp(l_j) / sum_{j'<k} exp(l_j')  (softmax over the
- *                  selected logits, equal to the full softmax renormalised
- *                  to sum 1 over the selection);
- *   renormalize=0: w_j = exp(l_j) / sum_{e<E} exp(l_e). */
-void orc_topk(const double* logits, int32_t T, int32_t E, int32_t k,
-              int32_t renormalize, int32_t* topk_idx, double* topk_w) {
+/* Select the k experts of every token with the highest selection logits
+ * sel (full sort descending, ties to the lower index), and their routing
+ * weights from the weight logits wl:
+ *   renormalize=1: w_j = exp(wl_j) / sum_{j'<k} exp(wl_j')  (softmax over
+ *                  the selected experts);
+ *   renormalize=0: w_j = exp(wl_j) / sum_{e<E} exp(wl_e).
+ * sel == wl is the plain router [P1: the router scores the experts and keeps
+ * eight].  sel = l + bias with wl = l is the selection-only bias variant: a
+ * per-expert offset that changes which experts are chosen but not how their
+ * outputs are weighted. */
+void orc_topk_sel(const double* sel, const double* wl, int32_t T, int32_t E,
+                  int32_t k, int32_t renormalize, int32_t* topk_idx,
+                  double* topk_w) {
 #pragma omp parallel for schedule(static)
   for (int t = 0; t < T; ++t) {
     orc_scored* s = (orc_scored*)malloc(sizeof(orc_scored) * (size_t)E);
     for (int e = 0; e < E; ++e) {
-      s[e].v = logits[(size_t)t * E + e];
+      s[e].v = sel[(size_t)t * E + e];
       s[e].e = e;
     }
     qsort(s, (size_t)E, sizeof(orc_scored), orc_cmp_scored);
-    double top = s[0].v, denom = 0.0;
-    int nd = renormalize ? k : E;
-    for (int j = 0; j < nd; ++j) denom += exp(s[j].v - top);
+    const double* w = wl + (size_t)t * E;
+    double top = w[s[0].e];
+    if (renormalize) {
+      for (int j = 1; j < k; ++j)
+        if (w[s[j].e] > top) top = w[s[j].e];
+    } else {
+      for (int e = 1; e < E; ++e)
+        if (w[e] > top) top = w[e];
+    }
+    double denom = 0.0;
+    if (renormalize) {
+      for (int j = 0; j < k; ++j) denom += exp(w[s[j].e] - top);
+    } else {
+      for (int e = 0; e < E; ++e) denom += exp(w[e] - top);
+    }
     for (int j = 0; j < k; ++j) {
       topk_idx[(size_t)t * k + j] = s[j].e;
-      topk_w[(size_t)t * k + j] = exp(s[j].v - top) / denom;
+      topk_w[(size_t)t * k + j] = exp(w[s[j].e] - top) / denom;
     }
     free(s);
+  }
+}
+
+/* The plain router: selection and weights from the same logits. */
+void orc_topk(const double* logits, int32_t T, int32_t E, int32_t k,
+              int32_t renormalize, int32_t* topk_idx, double* topk_w) {
+  orc_topk_sel(logits, logits, T, E, k, renormalize, topk_idx, topk_w);
+}
+
+/* Shared-expert gate g[t] = 1 / (1 + exp(-sum_h x[t][h] * w_sg[h])), the
+ * sigmoid of one more router-like row (reading of the shared-expert gate
+ * variant: the pages run the shared expert on every token and name no gate;
+ * this is its gated form). */
+void orc_shared_gate(const uint16_t* x_bf16, const float* w_sg, int32_t T,
+                     int32_t H, double* gate) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    double z = 0.0;
+    for (int h = 0; h < H; ++h)
+      z += orc_bf16_to_f64(x_bf16[(size_t)t * H + h]) * (double)w_sg[h];
+    gate[t] = 1.0 / (1.0 + exp(-z));
   }
 }
 
@@ -256,16 +294,17 @@ void orc_expert_ffn(const orc_qmat* gate_up, const orc_qmat* down, int e,
 }
 
 /* The layer output for the tokens listed in `tokens` (n_tok of them):
- *   y[t] = sum_{j<k} w[t][j] * o_{idx[t][j]}(x_t) + o_shared(x_t)
- * with the routing (idx, w) given.  y is [n_tok, H], in the order of
+ *   y[t] = sum_{j<k} w[t][j] * o_{idx[t][j]}(x_t) + g[t] * o_shared(x_t)
+ * with the routing (idx, w) given and g = shared_w (indexed by token), or
+ * g = 1 when shared_w is NULL.  y is [n_tok, H], in the order of
  * `tokens`.  The k+1 expert outputs of a token are independent and are
  * computed in parallel; the sum is then taken in the order j = 0..k-1,
  * shared last. */
-void orc_moe_layer(const uint16_t* x_bf16, int32_t H, const int32_t* topk_idx,
-                   const double* topk_w, int32_t k, const orc_qmat* gate_up,
-                   const orc_qmat* down, const orc_qmat* shared_gate_up,
-                   const orc_qmat* shared_down, const int32_t* tokens,
-                   int32_t n_tok, double* y) {
+void orc_moe_layer_ex(const uint16_t* x_bf16, int32_t H, const int32_t* topk_idx,
+                      const double* topk_w, int32_t k, const orc_qmat* gate_up,
+                      const orc_qmat* down, const orc_qmat* shared_gate_up,
+                      const orc_qmat* shared_down, const double* shared_w,
+                      const int32_t* tokens, int32_t n_tok, double* y) {
   int64_t n_items = (int64_t)n_tok * (k + 1);
   double* o = (double*)malloc(sizeof(double) * (size_t)n_items * H);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -290,11 +329,21 @@ void orc_moe_layer(const uint16_t* x_bf16, int32_t H, const int32_t* topk_idx,
       double acc = 0.0;
       for (int j = 0; j < k; ++j)
         acc += topk_w[(size_t)t * k + j] * o[(i * (k + 1) + j) * H + n];
-      acc += o[(i * (k + 1) + k) * H + n];
+      acc += (shared_w ? shared_w[t] : 1.0) * o[(i * (k + 1) + k) * H + n];
       y[i * H + n] = acc;
     }
   }
   free(o);
+}
+
+/* The layer with the shared expert at weight 1. */
+void orc_moe_layer(const uint16_t* x_bf16, int32_t H, const int32_t* topk_idx,
+                   const double* topk_w, int32_t k, const orc_qmat* gate_up,
+                   const orc_qmat* down, const orc_qmat* shared_gate_up,
+                   const orc_qmat* shared_down, const int32_t* tokens,
+                   int32_t n_tok, double* y) {
+  orc_moe_layer_ex(x_bf16, H, topk_idx, topk_w, k, gate_up, down, shared_gate_up,
+                   shared_down, NULL, tokens, n_tok, y);
 }
 
 /* ------------------------------------------------------------ dense GEMV */

@@ -28,10 +28,18 @@ MUTANTS = {
     "router bias dropped": ("if (bias) acc += (double)bias[e];", "(void)bias;"),
     "tie break": ("return (a->e < b->e) ? -1 : (a->e > b->e);",
                   "return (a->e > b->e) ? -1 : (a->e < b->e);"),
-    "softmax denominator": ("int nd = renormalize ? k : E;",
-                            "int nd = renormalize ? E : k;"),
-    "softmax sign": ("topk_w[(size_t)t * k + j] = exp(s[j].v - top) / denom;",
-                     "topk_w[(size_t)t * k + j] = exp(top - s[j].v) / denom;"),
+    "softmax denominator": ("for (int j = 0; j < k; ++j) denom += exp(w[s[j].e] - top);",
+                            "for (int j = 0; j < k && j < 1; ++j) denom += exp(w[s[j].e] - top);"),
+    "full softmax over the selection": ("for (int e = 0; e < E; ++e) denom += exp(w[e] - top);",
+                                        "for (int e = 0; e < k; ++e) denom += exp(w[e] - top);"),
+    "softmax sign": ("topk_w[(size_t)t * k + j] = exp(w[s[j].e] - top) / denom;",
+                     "topk_w[(size_t)t * k + j] = exp(top - w[s[j].e]) / denom;"),
+    "weights from the selection logits": ("const double* w = wl + (size_t)t * E;",
+                                          "const double* w = sel + (size_t)t * E;"),
+    "shared gate sign": ("gate[t] = 1.0 / (1.0 + exp(-z));",
+                         "gate[t] = 1.0 / (1.0 + exp(z));"),
+    "shared gate index": ("(double)w_sg[h]", "(double)w_sg[H - 1 - h]"),
+    "shared gate ignored": ("(shared_w ? shared_w[t] : 1.0)", "1.0"),
     "unstable scatter": ("for (int64_t a = 0; a < A; ++a)\n      if (topk_idx[a] == e) perm[pos++] = (int32_t)a;",
                          "for (int64_t a = A - 1; a >= 0; --a)\n      if (topk_idx[a] == e) perm[pos++] = (int32_t)a;"),
     "tile row step": ("tile_map[2 * nt + 1] = offsets[e] + m * BM;",
@@ -39,7 +47,8 @@ MUTANTS = {
     "silu sign": ("return g / (1.0 + exp(-g));", "return g / (1.0 + exp(g));"),
     "gate/up swapped": ("h[i] = orc_silu(gu[i]) * gu[I + i];",
                         "h[i] = orc_silu(gu[I + i]) * gu[i];"),
-    "shared expert dropped": ("acc += o[(i * (k + 1) + k) * H + n];", "(void)0;"),
+    "shared expert dropped": ("acc += (shared_w ? shared_w[t] : 1.0) * o[(i * (k + 1) + k) * H + n];",
+                              "(void)shared_w;"),
     "routing weight pairing": ("acc += topk_w[(size_t)t * k + j] * o[(i * (k + 1) + j) * H + n];",
                                "acc += topk_w[(size_t)t * k + (k - 1 - j)] * o[(i * (k + 1) + j) * H + n];"),
     "gemv block index": ("orc_f16_to_f64(d[(size_t)n * (K / 32) + c / 32])",

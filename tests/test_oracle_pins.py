@@ -366,6 +366,93 @@ def test_layer_token_subset_and_order():
     assert np.array_equal(sub[0], full[3]) and np.array_equal(sub[1], full[1])
 
 
+# ------------------------------------------- router / shared-expert variants
+
+def test_topk_selection_only_bias_hand_example():
+    # E = 4, k = 2, logits l and a bias that moves experts 0 and 2 to the top:
+    # selection by l + b = [4, 2, 3, 1.5] -> experts (0, 2); the weights use
+    # the unbiased logits (1.0, 0.5): w0 = 1 / (1 + e^-0.5); the plain router
+    # weights the biased logits (4, 3) instead: w0 = 1 / (1 + e^-1).
+    l = np.array([[1.0, 2.0, 0.5, 1.5]])
+    b = np.array([3.0, 0.0, 2.5, 0.0])
+    idx, w = oracle.topk_sel(l + b, l, 2, True)
+    assert idx.tolist() == [[0, 2]]
+    np.testing.assert_allclose(w[0], [1 / (1 + math.exp(-0.5)), 1 / (1 + math.exp(0.5))],
+                               rtol=1e-15)
+    idx2, w2 = oracle.topk(l + b, 2, True)
+    assert idx2.tolist() == [[0, 2]]
+    np.testing.assert_allclose(w2[0], [1 / (1 + math.exp(-1.0)), 1 / (1 + math.exp(1.0))],
+                               rtol=1e-15)
+    # full softmax at the selected experts: e^l_j / sum_e e^l_e (unbiased)
+    _, w3 = oracle.topk_sel(l + b, l, 2, False)
+    den = sum(math.exp(v) for v in l[0])
+    np.testing.assert_allclose(w3[0], [math.exp(1.0) / den, math.exp(0.5) / den], rtol=1e-15)
+
+
+def test_route_selection_only_bias_reduces_to_plain():
+    # a zero bias, or one equal for every expert, selects and weights exactly
+    # like the plain router; a real bias changes the selection only through
+    # l + b and leaves the weights those of the unbiased logits
+    L = synth.draw_layer(synth.TINY, "cpu", seed=30, zipf="noise")
+    x = tie_free_x(L, 6, seed=30)
+    xb, wr = bits16(x), L.w_router.numpy()
+    i0, w0 = oracle.route(xb, wr, 2)
+    i1, w1 = oracle.route(xb, wr, 2, np.zeros(16, np.float32), True, True)
+    assert np.array_equal(i0, i1) and np.array_equal(w0, w1)
+    bias = L.logit_bias.numpy()
+    i2, w2 = oracle.route(xb, wr, 2, bias, True, True)
+    lb = oracle.router_logits(xb, wr, bias)
+    lu = oracle.router_logits(xb, wr, None)
+    ref_i = np.argsort(-lb, axis=1, kind="stable")[:, :2]
+    assert np.array_equal(i2, ref_i)
+    sel = np.take_along_axis(lu, ref_i, axis=1)
+    ref_w = np.exp(sel - sel.max(1, keepdims=True))
+    ref_w /= ref_w.sum(1, keepdims=True)
+    np.testing.assert_allclose(w2, ref_w, rtol=1e-13)
+
+
+def test_shared_gate_closed_forms():
+    H = 64
+    x = torch.zeros((3, H))
+    x[0, 5] = 1.0          # one-hot: z = w_sg[5]
+    x[1, :] = 0.5          # constant: z = 0.5 * sum(w_sg)
+    xb = bits16(x.to(torch.bfloat16))
+    w = np.zeros(H, np.float32)
+    g0 = oracle.shared_gate(xb, w)
+    assert np.array_equal(g0, [0.5, 0.5, 0.5])   # sigmoid(0) exactly
+    w[5] = math.log(3.0)
+    g = oracle.shared_gate(xb, w)
+    # sigmoid(ln 3) = 1 / (1 + 1/3) = 3/4; w_sg[5] is ln 3 rounded to fp32,
+    # which moves the gate by less than 1e-8
+    assert abs(g[0] - 0.75) < 1e-8
+    # constant row: z = 0.5 * w_sg[5]
+    z = 0.5 * float(np.float32(math.log(3.0)))
+    np.testing.assert_allclose(g[1], 1 / (1 + math.exp(-z)), rtol=1e-14)
+    assert g[2] == 0.5
+
+
+def test_layer_gated_shared_expert_is_linear_in_the_gate():
+    # y(g) = y(0) + g * o_shared: with g = 1 the gated layer equals the plain
+    # layer bit for bit, and any g interpolates linearly
+    L = synth.draw_layer(synth.TINY, "cpu", seed=31)
+    x = tie_free_x(L, 3, seed=31)
+    xb = bits16(x)
+    idx, w = oracle.route(xb, L.w_router.numpy(), 2)
+    q = oracle_layer(L)
+    plain = oracle.moe_layer(xb, idx, w, *q)
+    y1 = oracle.moe_layer(xb, idx, w, *q, shared_w=np.ones(3))
+    assert np.array_equal(plain, y1)
+    y0 = oracle.moe_layer(xb, idx, w, *q, shared_w=np.zeros(3))
+    g = np.array([0.25, 0.5, 0.9])
+    yg = oracle.moe_layer(xb, idx, w, *q, shared_w=g)
+    np.testing.assert_allclose(yg, y0 + g[:, None] * (y1 - y0), rtol=1e-12, atol=1e-12)
+    # y(1) - y(0) is the shared expert's own output (one-expert FFN)
+    X = x.to(torch.float64).numpy()
+    for t in range(3):
+        o_sh, _, _ = oracle.expert_ffn(q[2], q[3], 0, X[t])
+        np.testing.assert_allclose(y1[t] - y0[t], o_sh, rtol=1e-9, atol=1e-9)
+
+
 # ------------------------------------------------------------------ GEMV
 
 def test_q8_gemv_one_hot_and_library():
