@@ -146,16 +146,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------- ours
 
-def build_layers(qsm, wl, device, seed, fuse=True):
+def build_layers(qsm, wl, device, seed, fuse=True, gated=False, sel_only=False):
     shape = wl["shape"]
     layers, xs, fwds, syn = [], [], [], []
     for l in range(wl["layers"]):
         Lg = synth.draw_layer(shape, device, seed=seed, layer=l, zipf=wl["zipf"])
         syn.append(Lg)
-        L = qsm.Layer.from_synth(Lg)
+        sg = synth.draw_shared_gate(shape.H, device, seed, l) if gated else None
+        L = qsm.Layer.from_synth(Lg, sg)
         layers.append(L)
         xs.append(synth.draw_x(wl["T"], shape.H, device, seed, l))
-        fwds.append(qsm.MoEForward(L, wl["T"], device, fuse_route_group=fuse))
+        fwds.append(qsm.MoEForward(L, wl["T"], device, fuse_route_group=fuse,
+                                   bias_select_only=sel_only))
     return layers, xs, fwds, syn
 
 
@@ -163,8 +165,8 @@ class ChunkedLayer:
     """One layer through moe_layer_forward in chunks, outputs and workspace
     allocated once."""
 
-    def __init__(self, qsm, L, T, chunk, device):
-        self.qsm, self.L, self.chunk = qsm, L, chunk
+    def __init__(self, qsm, L, T, chunk, device, sel_only=False):
+        self.qsm, self.L, self.chunk, self.sel_only = qsm, L, chunk, sel_only
         self.y = torch.empty((T, L.H), dtype=torch.bfloat16, device=device)
         self.idx = torch.empty((T, L.k), dtype=torch.int32, device=device)
         self.w = torch.empty((T, L.k), dtype=torch.float32, device=device)
@@ -173,7 +175,8 @@ class ChunkedLayer:
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def __call__(self, x, stream=None):
-        self.qsm.moe_layer_forward(self.L, x, self.chunk, y=self.y, topk_idx=self.idx,
+        self.qsm.moe_layer_forward(self.L, x, self.chunk, True, self.sel_only, y=self.y,
+                                   topk_idx=self.idx,
                                    topk_w=self.w, workspace=self.ws,
                                    dev_status=self.dev_status, stream=stream)
         return self.y
@@ -198,13 +201,16 @@ def run_ours(args, wl, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     layers, xs, fwds, syn = build_layers(qsm, wl, dev, seed=0,
-                                         fuse=args.route_group == "fused")
+                                         fuse=args.route_group == "fused",
+                                         gated=args.gated_shared,
+                                         sel_only=args.bias_select_only)
     T, nL = wl["T"], wl["layers"]
     stream = torch.cuda.Stream(device=dev)
 
     calls = fwds
     if args.chunk:  # the whole layer per call, in chunks of args.chunk tokens
-        calls = [ChunkedLayer(qsm, L, T, args.chunk, dev) for L in layers]
+        calls = [ChunkedLayer(qsm, L, T, args.chunk, dev, args.bias_select_only)
+                 for L in layers]
 
     def step(s):
         for f, x in zip(calls, xs):
@@ -262,7 +268,7 @@ def run_ours(args, wl, rank, world):
     with torch.cuda.graph(g2, stream=stream):
         s2 = torch.cuda.current_stream()
         for (a, b), f, x, L in zip(evs, fwds, xs, layers):
-            qsm.moe_route(x, L.w_router, L.k, L.logit_bias, True, f.topk_idx,
+            qsm.moe_route(x, L.w_router, L.k, L.logit_bias, f.renormalize, f.topk_idx,
                           f.topk_w, f.route_ws, f.dev_status, s2)
             qsm.moe_group_tokens(f.topk_idx, L.E, f.grouping.tile_rows,
                                  f.grouping, f.dev_status, s2)
@@ -472,6 +478,10 @@ def main():
     ap.add_argument("--route-group", default="fused", choices=["fused", "separate"],
                     help="for T <= 8: one fused route+group launch, or the two "
                          "separate launches")
+    ap.add_argument("--gated-shared", action="store_true",
+                    help="sigmoid-gated shared expert (a random gate vector per layer)")
+    ap.add_argument("--bias-select-only", action="store_true",
+                    help="the logit bias selects experts but leaves the weights")
     ap.add_argument("--chunk", type=int, default=0,
                     help="run each layer through moe_layer_forward in chunks of "
                          "this many tokens (chunked prefill)")
@@ -489,6 +499,10 @@ def main():
         wl["desc"] += f" (layer count overridden: {args.layers})"
     if args.chunk:
         wl["desc"] += f", chunks of {args.chunk} tokens"
+    if args.gated_shared:
+        wl["desc"] += ", gated shared expert"
+    if args.bias_select_only:
+        wl["desc"] += ", selection-only logit bias"
     if args.impl == "reference":
         res = run_reference(args, wl, rank, world)
     else:

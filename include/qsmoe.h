@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define QSM_ABI_VERSION 1
+#define QSM_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define QSM_API __attribute__((visibility("default")))
@@ -101,11 +101,15 @@ typedef struct {
  *   gate_up        [E, 2I, H]  rows 0..I-1 gate, rows I..2I-1 up
  *   down           [E, H, I]
  *   shared_gate_up [1, 2I, H], shared_down [1, H, I]
+ *   shared_gate    [H] fp32, or NULL: the shared expert's output of token t
+ *                  is scaled by sigmoid(x[t] . shared_gate) (a gated shared
+ *                  expert); NULL keeps weight 1 (the pages' shared expert).
  * All four tensors must share one qtype.  Requires H % 64 == 0,
- * I % 64 == 0, 1 <= k <= E <= 1024. */
+ * I % 64 == 0, 1 <= k <= E <= 1024, shared_gate 16-byte aligned. */
 typedef struct {
   int32_t H, I, E, k;
   qsm_qweights gate_up, down, shared_gate_up, shared_down;
+  const float* shared_gate;
 } qsm_moe_layer;
 
 /* The token grouping produced by moe_group_tokens (all device arrays).
@@ -141,11 +145,17 @@ typedef struct {
  * experts. */
 QSM_API size_t moe_route_workspace_bytes(int32_t T, int32_t H, int32_t E);
 
-/* Router: logits l[t,e] = sum_h x[t,h] * w_router[e,h] + logit_bias[e]
- * (fp32 accumulation), then per token the k largest logits (ties to the
- * lower expert index) in descending order, and their weights
- *   renormalize != 0: softmax over the k selected logits;
- *   renormalize == 0: full softmax over all E logits, taken at the selected.
+/* Route flags (the `renormalize` argument of the routing calls). */
+#define QSM_ROUTE_RENORMALIZE 1      /* weights: softmax over the selection */
+#define QSM_ROUTE_BIAS_SELECT_ONLY 2 /* logit_bias picks experts, not weights */
+
+/* Router: logits l[t,e] = sum_h x[t,h] * w_router[e,h] (fp32 accumulation)
+ * and selection logits s[t,e] = l[t,e] + logit_bias[e]; per token the k
+ * largest s (ties to the lower expert index) in descending order, and their
+ * weights from w = s, or w = l with QSM_ROUTE_BIAS_SELECT_ONLY:
+ *   QSM_ROUTE_RENORMALIZE set:   softmax of w over the k selected experts;
+ *   QSM_ROUTE_RENORMALIZE clear: softmax of w over all E, at the selected.
+ * (`renormalize` is these flags; 0 and 1 keep their old meaning.)
  * [Perplexity page, "Qwen creates three distinct workload shapes".]
  *   x          [T, H] bf16
  *   w_router   [E, H] fp32
@@ -157,8 +167,8 @@ QSM_API size_t moe_route_workspace_bytes(int32_t T, int32_t H, int32_t E);
  * Few tokens run on CUDA cores (fp32 FMA); many tokens (T > 64, E a multiple
  * of 16 up to 256, k <= 8) run one tcgen05 GEMM over an exact three-way
  * bf16 split of w_router, which keeps fp32-accurate logits.
- * Requires H % 64 == 0, 1 <= k <= min(E, 32), E <= 1024, T >= 0.
- * A non-finite logit sets QSM_DEV_NONFINITE. */
+ * Requires H % 64 == 0, 1 <= k <= min(E, 32), E <= 1024, T >= 0, no flag
+ * bits beyond the two above.  A non-finite logit sets QSM_DEV_NONFINITE. */
 QSM_API qsm_status moe_route(const uint16_t* x, const float* w_router,
                      const float* logit_bias, int32_t T, int32_t H, int32_t E,
                      int32_t k, int32_t renormalize, int32_t* topk_idx,
@@ -276,7 +286,8 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
  *   Arguments and results are those of moe_ffn_forward.  The scratch comes
  *   from an array inside the library (1 MiB per device, held by every GPU
  *   that loads the library until the process exits), so T must be <= 64 and
- *   the layer's decode scratch ((T*k + T) * I * 2 bytes) must fit in 1 MiB;
+ *   the layer's decode scratch (moe_ffn_workspace_bytes(L, T): h, (T*k + T)
+ *   * I * 2 bytes, and T fp32 shared-expert gates) must fit in 1 MiB;
  *   otherwise QSM_ERR_UNSUPPORTED is returned and nothing is enqueued.
  *   The call allocates nothing.  The first call on each device looks up that
  *   device's copy of the array (make the stream's device current); make that

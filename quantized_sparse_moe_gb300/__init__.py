@@ -49,7 +49,8 @@ class MoELayerC(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("gate_up", QWeightsC), ("down", QWeightsC),
-                ("shared_gate_up", QWeightsC), ("shared_down", QWeightsC)]
+                ("shared_gate_up", QWeightsC), ("shared_down", QWeightsC),
+                ("shared_gate", ctypes.c_void_p)]
 
 
 class GroupingC(ctypes.Structure):
@@ -151,20 +152,32 @@ class Layer:
     """C view of one MoE layer; keeps the torch tensors alive."""
 
     def __init__(self, H, I, E, k, gate_up, down, shared_gate_up,
-                 shared_down, w_router, logit_bias=None):
+                 shared_down, w_router, logit_bias=None, shared_gate=None):
         self.H, self.I, self.E, self.k = H, I, E, k
         self.w_router = w_router
         self.logit_bias = logit_bias
-        self._keep = (gate_up, down, shared_gate_up, shared_down)
+        self.shared_gate = shared_gate  # [H] fp32 or None (ungated)
+        self._keep = (gate_up, down, shared_gate_up, shared_down, shared_gate)
         self.qtype = int(gate_up.qtype)
         self.c = MoELayerC(H, I, E, k, qweights_c(gate_up), qweights_c(down),
-                           qweights_c(shared_gate_up), qweights_c(shared_down))
+                           qweights_c(shared_gate_up), qweights_c(shared_down),
+                           _p(shared_gate))
 
     @classmethod
-    def from_synth(cls, L) -> "Layer":
+    def from_synth(cls, L, shared_gate=None) -> "Layer":
         s = L.shape
         return cls(s.H, s.I, s.E, s.k, L.gate_up, L.down, L.shared_gate_up,
-                   L.shared_down, L.w_router, L.logit_bias)
+                   L.shared_down, L.w_router, L.logit_bias, shared_gate)
+
+
+ROUTE_RENORMALIZE = 1        # weights: softmax over the selected experts
+ROUTE_BIAS_SELECT_ONLY = 2   # the logit bias selects, the weights ignore it
+
+
+def route_flags(renormalize=True, bias_select_only=False) -> int:
+    """The routing calls' flags word: renormalize is a bool, or already a
+    flags word (the library rejects unknown bits)."""
+    return int(renormalize) | (ROUTE_BIAS_SELECT_ONLY if bias_select_only else 0)
 
 
 # ------------------------------------------------------------------ router
@@ -176,7 +189,7 @@ def route_workspace_bytes(T: int, H: int, E: int) -> int:
 def moe_route(x: torch.Tensor, w_router: torch.Tensor, k: int,
               logit_bias: torch.Tensor | None = None, renormalize=True,
               topk_idx=None, topk_w=None, workspace=None, dev_status=None,
-              stream=None):
+              stream=None, *, bias_select_only=False):
     """Router logits, top-k and routing weights -> (topk_idx, topk_w)."""
     T, H = x.shape
     E = w_router.shape[0]
@@ -190,7 +203,8 @@ def moe_route(x: torch.Tensor, w_router: torch.Tensor, k: int,
                                 dtype=torch.uint8, device=dev)
     dev_status = _status(dev_status, dev)
     _check(lib().moe_route(_p(_u16(x)), _p(w_router), _p(logit_bias), T, H, E,
-                           k, int(bool(renormalize)), _p(topk_idx), _p(topk_w),
+                           k, route_flags(renormalize, bias_select_only), _p(topk_idx),
+                           _p(topk_w),
                            _p(workspace), workspace.numel(), _p(dev_status),
                            _stream(stream)), "moe_route")
     return topk_idx, topk_w
@@ -248,7 +262,8 @@ def moe_group_tokens(topk_idx: torch.Tensor, E: int, tile_rows: int,
 def moe_route_group(x: torch.Tensor, w_router: torch.Tensor, k: int,
                     grouping: Grouping, logit_bias=None, renormalize=True,
                     topk_idx=None, topk_w=None, workspace=None, dev_status=None,
-                    stream=None, raise_unsupported=True):
+                    stream=None, raise_unsupported=True, *,
+                    bias_select_only=False):
     """Router + grouping in one launch (T <= 8).  Returns (topk_idx, topk_w),
     or None when the shape is not supported and raise_unsupported is False.
     The workspace is the router's (route_workspace_bytes, zero-initialised
@@ -266,7 +281,8 @@ def moe_route_group(x: torch.Tensor, w_router: torch.Tensor, k: int,
     dev_status = _status(dev_status, dev)
     gc = grouping.c
     st = lib().moe_route_group(_p(_u16(x)), _p(w_router), _p(logit_bias), T, H, E,
-                               k, int(bool(renormalize)), _p(topk_idx),
+                               k, route_flags(renormalize, bias_select_only),
+                               _p(topk_idx),
                                _p(topk_w), ctypes.byref(gc), _p(workspace),
                                workspace.numel(), _p(dev_status), _stream(stream))
     if st == 2 and not raise_unsupported:
@@ -336,6 +352,7 @@ def layer_workspace_bytes(layer: Layer, T: int, chunk: int) -> int:
 
 
 def moe_layer_forward(layer: Layer, x: torch.Tensor, chunk: int, renormalize=True,
+                      bias_select_only=False, *,
                       y=None, y_f32=None, topk_idx=None, topk_w=None,
                       workspace=None, dev_status=None, stream=None):
     """The whole layer (route -> group -> FFN) in chunks of at most `chunk`
@@ -358,7 +375,8 @@ def moe_layer_forward(layer: Layer, x: torch.Tensor, chunk: int, renormalize=Tru
     dev_status = _status(dev_status, dev)
     _check(lib().moe_layer_forward(
         ctypes.byref(layer.c), _p(_u16(x)), T, chunk, _p(layer.w_router),
-        _p(layer.logit_bias), int(bool(renormalize)), _p(topk_idx), _p(topk_w),
+        _p(layer.logit_bias), route_flags(renormalize, bias_select_only), _p(topk_idx),
+        _p(topk_w),
         _p(y), _p(y_f32 if y_f32 is not False else None), _p(workspace),
         workspace.numel(), _p(dev_status), _stream(stream)), "moe_layer_forward")
     return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None), topk_idx, topk_w
@@ -396,8 +414,9 @@ class MoEForward:
     the route and group steps use the fused moe_route_group launch."""
 
     def __init__(self, layer: Layer, T: int, device="cuda", renormalize=True,
-                 want_f32=False, fuse_route_group=True):
-        self.layer, self.T, self.renormalize = layer, T, renormalize
+                 want_f32=False, fuse_route_group=True, *, bias_select_only=False):
+        self.layer, self.T = layer, T
+        self.renormalize = route_flags(renormalize, bias_select_only)
         self.fuse_route_group = fuse_route_group
         k, E, H = layer.k, layer.E, layer.H
         i32 = dict(dtype=torch.int32, device=device)

@@ -63,6 +63,7 @@ qsm_status check_layer(const qsm_moe_layer* L) {
       !check_q(L->shared_gate_up, qt, 1, 2 * L->I, L->H) ||
       !check_q(L->shared_down, qt, 1, L->H, L->I))
     return QSM_ERR_INVALID_ARGUMENT;
+  if (L->shared_gate && !aligned16(L->shared_gate)) return QSM_ERR_INVALID_ARGUMENT;
   return QSM_OK;
 }
 

@@ -131,7 +131,9 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
                   int H, int I, int k, const int32_t* __restrict__ perm,
                   const int32_t* __restrict__ offsets,
                   const int32_t* __restrict__ tile_map, int shared_slots,
-                  int xrows, __half* __restrict__ hbuf, int32_t* dev_status) {
+                  int xrows, __half* __restrict__ hbuf,
+                  const float* __restrict__ sgate, float* __restrict__ gbuf,
+                  int32_t* dev_status) {
   extern __shared__ __align__(128) unsigned char d1_smem[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ float red[kD1Split][32][4];
@@ -234,6 +236,32 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
     *reinterpret_cast<uint4*>(xs + c * xpitch + 8 * j) = bf16x8_to_f16x8(v);
   }
   __syncthreads();
+  // gated shared expert: sigmoid(x . shared_gate) of this slot's tokens,
+  // computed by the slot's first CTA while its weight copies land
+  if (sgate != nullptr && shared_slot && blockIdx.x == 0) {
+    for (int c = kw; c < cnt; c += kD1Split) {
+      const __half* xr = xs + c * xpitch;
+      float z = 0.f;
+      for (int h8 = lane; h8 < H / 8; h8 += 32) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xr + 8 * h8);
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(sgate) + 2 * h8);
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(sgate) + 2 * h8 + 1);
+        const __half2* x2 = reinterpret_cast<const __half2*>(&xv);
+        const float2 a = __half22float2(x2[0]), b = __half22float2(x2[1]);
+        const float2 cc = __half22float2(x2[2]), d = __half22float2(x2[3]);
+        z = fmaf(a.x, w0.x, z);
+        z = fmaf(a.y, w0.y, z);
+        z = fmaf(b.x, w0.z, z);
+        z = fmaf(b.y, w0.w, z);
+        z = fmaf(cc.x, w1.x, z);
+        z = fmaf(cc.y, w1.y, z);
+        z = fmaf(d.x, w1.z, z);
+        z = fmaf(d.y, w1.w, z);
+      }
+      z = warp_sum(z);
+      if (lane == 0) gbuf[row0 + c] = 1.0f / (1.0f + __expf(-z));
+    }
+  }
   // bounded wait for the weight rows; the CTA agrees on the outcome
   if (!__syncthreads_and(mbar_wait_bounded(&bar, 0, kWaitIters))) {
     if (threadIdx.x == 0) set_status(dev_status, QSM_DEV_TIMEOUT);
@@ -320,8 +348,8 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
                 const int32_t* __restrict__ tile_map,
                 const int32_t* __restrict__ n_tiles_p,
                 const float* __restrict__ topk_w, int shared_slots, int hrows,
-                uint16_t* __restrict__ y, float* __restrict__ y32,
-                int32_t* dev_status) {
+                const float* __restrict__ gbuf, uint16_t* __restrict__ y,
+                float* __restrict__ y32, int32_t* dev_status) {
   extern __shared__ __align__(128) unsigned char d2_smem[];
   __shared__ __align__(8) uint64_t bars[kD2Warps];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -406,9 +434,9 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
       tok[cc] = -1;
       wt[cc] = 0.f;
       if (c < cur.cnt) {
-        if (cur.e < 0) {
+        if (cur.e < 0) {  // shared expert: weight 1, or its gate
           tok[cc] = cur.row0 + c;
-          wt[cc] = 1.f;
+          wt[cc] = gbuf ? __ldcg(gbuf + tok[cc]) : 1.f;
         } else {
           const int a = __ldcg(perm + cur.row0 + c);
           tok[cc] = a / k;
@@ -481,7 +509,7 @@ template <int QT>
 static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
                                    int T, const float* topk_w,
                                    const qsm_grouping* g, uint16_t* y,
-                                   float* y32, __half* hbuf,
+                                   float* y32, __half* hbuf, float* gbuf,
                                    int32_t* dev_status, cudaStream_t stream) {
   using namespace decode;
   const int H = L->H, I = L->I, k = L->k;
@@ -505,7 +533,7 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
                           stream, L->gate_up, L->shared_gate_up, L->down,
                           L->shared_down, x, T, H, I, k, (const int32_t*)g->perm,
                           (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
-                          shared_slots, xrows, hbuf, dev_status));
+                          shared_slots, xrows, hbuf, L->shared_gate, gbuf, dev_status));
   QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem2));
@@ -514,7 +542,8 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
                           H, I, k, (const int32_t*)g->perm,
                           (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
                           (const int32_t*)g->n_tiles, topk_w, shared_slots, xrows,
-                          y, y32, dev_status));
+                          L->shared_gate ? (const float*)gbuf : nullptr, y, y32,
+                          dev_status));
   return QSM_OK;
 }
 
@@ -522,17 +551,21 @@ qsm_status decode_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
                              const float* topk_w, const qsm_grouping* g,
                              uint16_t* y, float* y32, void* ws,
                              int32_t* dev_status, cudaStream_t stream) {
+  // [h (T*k + T) x I fp16][shared-expert gates T fp32]
   __half* hbuf = static_cast<__half*>(ws);
+  const size_t hbytes = (((size_t)T * L->k + T) * L->I * sizeof(__half) + 255) & ~size_t(255);
+  float* gbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + hbytes);
   if (L->gate_up.qtype == QSM_Q8_0)
-    return decode_launch_qt<QSM_Q8_0>(L, x, T, topk_w, g, y, y32, hbuf,
+    return decode_launch_qt<QSM_Q8_0>(L, x, T, topk_w, g, y, y32, hbuf, gbuf,
                                       dev_status, stream);
-  return decode_launch_qt<QSM_AFFINE4_G64>(L, x, T, topk_w, g, y, y32, hbuf,
+  return decode_launch_qt<QSM_AFFINE4_G64>(L, x, T, topk_w, g, y, y32, hbuf, gbuf,
                                            dev_status, stream);
 }
 
 size_t decode_ffn_workspace_bytes(const qsm_moe_layer* L, int T) {
   const size_t rows = (size_t)T * L->k + T;
-  return ((rows * L->I * sizeof(__half)) + 255) & ~size_t(255);
+  return (((rows * L->I * sizeof(__half)) + 255) & ~size_t(255)) +
+         (((size_t)T * sizeof(float) + 255) & ~size_t(255));
 }
 
 }  // namespace qsm

@@ -89,6 +89,7 @@ struct Params {
   int nsub;               // weight blocks (two 128-row tiles each) per tile
   __half* hbuf;           // [T*k + T, I]
   float* yacc;            // [T, H]
+  const float* gate;      // [T] shared-expert gates, or NULL (weight 1)
   int32_t* status;
 };
 
@@ -448,9 +449,9 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       int tok = 0;
       float wt = 0.f;
       if (MODE == kDown && live) {
-        if (ti.e < 0) {
+        if (ti.e < 0) {  // shared expert: weight 1, or its gate
           tok = ti.row0 + et;
-          wt = kHScaleInv;
+          wt = (p.gate ? __ldcg(p.gate + tok) : 1.f) * kHScaleInv;
         } else {
           const int asg = __ldcg(p.perm + ti.row0 + et);
           tok = asg / p.k;
@@ -511,11 +512,13 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 // The token operand of gate_up, fp16 [A + T, H] with A = T*k: row r < A
 // holds the token of assignment perm[r] (zero if that assignment has no
 // valid expert), row A + t holds token t.  One warp per row, its 16-byte
-// chunks loaded four at a time before they are converted and stored.  Also
-// zeroes the fp32 output accumulator.
+// chunks loaded four at a time before they are converted and stored.  With
+// a shared-expert gate, the warp of row A + t also forms sigmoid(x[t] .
+// shared_gate) in fp32.  Also zeroes the fp32 output accumulator.
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int T,
             int k, int H, __half* __restrict__ xall, float* __restrict__ yacc,
+            const float* __restrict__ sgate, float* __restrict__ gbuf,
             int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
@@ -532,6 +535,8 @@ prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, in
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t < 0 ? 0 : t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xall + (size_t)r * H);
+    const bool gate_row = sgate != nullptr && r >= A;
+    float z = 0.f;
     for (int c0 = lane; c0 < cpr; c0 += 4 * 32) {
       uint4 v[4];
 #pragma unroll
@@ -545,6 +550,18 @@ prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, in
         if (c >= cpr) break;
         const uint4 h = make_uint4(bf16x2_to_f16x2(v[u].x), bf16x2_to_f16x2(v[u].y),
                                    bf16x2_to_f16x2(v[u].z), bf16x2_to_f16x2(v[u].w));
+        if (gate_row) {
+          const float4 w0 = __ldg(reinterpret_cast<const float4*>(sgate) + 2 * c);
+          const float4 w1 = __ldg(reinterpret_cast<const float4*>(sgate) + 2 * c + 1);
+          z = fmaf(bf16_lo(v[u].x), w0.x, z);
+          z = fmaf(bf16_hi(v[u].x), w0.y, z);
+          z = fmaf(bf16_lo(v[u].y), w0.z, z);
+          z = fmaf(bf16_hi(v[u].y), w0.w, z);
+          z = fmaf(bf16_lo(v[u].z), w1.x, z);
+          z = fmaf(bf16_hi(v[u].z), w1.y, z);
+          z = fmaf(bf16_lo(v[u].w), w1.z, z);
+          z = fmaf(bf16_hi(v[u].w), w1.w, z);
+        }
         const uint32_t* hw = reinterpret_cast<const uint32_t*>(&h);
 #pragma unroll
         for (int q = 0; q < 4; ++q)  // an all-ones exponent: out of fp16 range
@@ -552,6 +569,10 @@ prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, in
             bad = true;
         dst[c] = h;
       }
+    }
+    if (gate_row) {
+      z = warp_sum(z);
+      if (lane == 0) gbuf[t] = 1.0f / (1.0f + __expf(-z));
     }
   }
   const size_t ny = (size_t)T * H / 4;
@@ -624,7 +645,7 @@ qsm_status launch_gemms(const Params& p1, const Params& p2, cudaStream_t stream)
 }
 
 struct WsLayout {
-  size_t xall, hbuf, yacc, total;
+  size_t xall, hbuf, yacc, gate, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -635,7 +656,8 @@ WsLayout ws_layout(const qsm_moe_layer* L, int T) {
   w.xall = 0;
   w.hbuf = up256(rows * L->H * 2);
   w.yacc = w.hbuf + up256(rows * L->I * 2);
-  w.total = w.yacc + up256((size_t)T * L->H * 4);
+  w.gate = w.yacc + up256((size_t)T * L->H * 4);
+  w.total = w.gate + up256((size_t)T * 4);
   return w;
 }
 
@@ -661,11 +683,13 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   __half* xall = reinterpret_cast<__half*>(wsb + wl.xall);
   __half* hbuf = reinterpret_cast<__half*>(wsb + wl.hbuf);
   float* yacc = reinterpret_cast<float*>(wsb + wl.yacc);
+  float* gbuf = reinterpret_cast<float*>(wsb + wl.gate);
   const int nsm = sm_count();
   const size_t rows_h = (size_t)T * k + T;
 
   QSM_CUDA_TRY(launch_pdl(prep_kernel, dim3(4 * nsm), dim3(256), 0, stream, x,
-                          (const int32_t*)g->perm, T, k, H, xall, yacc, dev_status));
+                          (const int32_t*)g->perm, T, k, H, xall, yacc, L->shared_gate,
+                          gbuf, dev_status));
 
   // code tiles: 64 K per step = 64 bytes (Q8_0) or 32 bytes (affine-4) a row
   const bool a4 = L->gate_up.qtype == QSM_AFFINE4_G64;
@@ -701,6 +725,7 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   p1.nsub = I / BM;
   p1.hbuf = hbuf;
   p1.yacc = yacc;
+  p1.gate = L->shared_gate ? gbuf : nullptr;
   p1.status = dev_status;
 
   Params p2 = p1;

@@ -91,6 +91,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // Top k of the values a warp holds, v[i] at index lane + 32 i (i < KPER,
 // indices >= E ignored), in descending order with ties to the lower index.
 // Lane j < k receives the j-th value and its index.  Each round takes every

@@ -4,7 +4,10 @@
 // three distinct workload shapes": the router scores every expert for each
 // token and keeps the best eight.  Readings: ties go to the lower expert
 // index; the weights are the softmax over the selected logits
-// (renormalize != 0) or the full softmax taken at the selected ones.
+// (QSM_ROUTE_RENORMALIZE) or the full softmax taken at the selected ones;
+// with QSM_ROUTE_BIAS_SELECT_ONLY the logit bias decides the selection but
+// the weights use the logits without it.  The workspace holds the logits
+// without the bias; the selecting CTA adds it.
 //
 // Layout of the work: blockIdx.x owns kExpertsPerCta experts, blockIdx.y a
 // block of kTokPerCta tokens.  Each expert's dot products are split over
@@ -28,6 +31,7 @@ constexpr int kThreadsPerExpert = kThreads / kExpertsPerCta;  // 128
 constexpr int kTokPerCta = 8;
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
+constexpr int kRouteFlags = QSM_ROUTE_RENORMALIZE | QSM_ROUTE_BIAS_SELECT_ONLY;
 
 // CUDA-core path workspace: [arrival counters][logits T x E fp32]
 size_t counters_bytes(int T) {
@@ -196,7 +200,6 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
       float v = 0.f;
 #pragma unroll
       for (int wq = 0; wq < kThreadsPerExpert / 32; ++wq) v += red[s2][wq][i];
-      if (bias) v += bias[e2];
       logits[(size_t)(t0 + i) * E + e2] = v;
     }
   }
@@ -215,47 +218,67 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
   if (!is_last) return;
 
   const int warp = tid / 32;
+  const bool renorm = (renormalize & QSM_ROUTE_RENORMALIZE) != 0;
+  const bool sel_only = (renormalize & QSM_ROUTE_BIAS_SELECT_ONLY) != 0 && bias;
   if (warp < nt) {
     const int t = t0 + warp;
-    float v[kPer];
+    const float* lt = logits + (size_t)t * E;
+    float v[kPer], u[kPer];  // selection logits (with the bias), weight logits
+    // all loads first (logits, then the bias), so they are in flight together
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      u[i] = lane + 32 * i < E ? __ldcg(lt + lane + 32 * i) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      v[i] = (bias && lane + 32 * i < E) ? __ldg(bias + lane + 32 * i) : 0.f;
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int ee = lane + 32 * i;
-      float l = -INFINITY;
-      if (ee < E) {
-        l = __ldcg(logits + (size_t)t * E + ee);
-        if (!isfinite(l)) {
-          bad = true;
-          l = -INFINITY;
-        }
+      float l = u[i], sl = bias ? l + v[i] : l;
+      if (lane + 32 * i < E && (!isfinite(sl) || !isfinite(l))) {
+        bad = true;
+        l = sl = -INFINITY;
       }
-      v[i] = l;
+      v[i] = sl;
+      u[i] = sel_only ? l : sl;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0)
       set_status(dev_status, QSM_DEV_NONFINITE);
     float my_l;
     int my_e;
     warp_topk<kPer>(v, E, k, my_l, my_e);
-    if (lane < k) {
-      sel_l[warp][lane] = my_l;
-      sel_e[warp][lane] = my_e;
+    // this lane's selection's weight logit, and the largest one the softmax
+    // runs over (the selection, or all E)
+    float my_w = my_l;
+    if (sel_only && lane < k) {
+      my_w = __ldcg(lt + my_e);
+      if (!isfinite(my_w)) my_w = -INFINITY;
     }
-    __syncwarp();
-    const float top = sel_l[warp][0];
-    float part = 0.f;
-    if (renormalize) {
-      if (lane < k) part = __expf(sel_l[warp][lane] - top);
+    float top = -INFINITY;
+    if (renorm) {
+      top = warp_max(lane < k ? my_w : -INFINITY);
     } else {
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
-        if (lane + 32 * i < E) part += __expf(v[i] - top);
+        if (lane + 32 * i < E) top = fmaxf(top, u[i]);
+      top = warp_max(top);
+    }
+    float part = 0.f;
+    if (renorm) {
+      if (lane < k) part = __expf(my_w - top);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (lane + 32 * i < E) part += __expf(u[i] - top);
     }
     const float inv = 1.0f / warp_sum(part);
     if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = sel_e[warp][lane];
-      topk_w[(size_t)t * k + lane] = __expf(sel_l[warp][lane] - top) * inv;
+      sel_l[warp][lane] = my_l;
+      sel_e[warp][lane] = my_e;
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = __expf(my_w - top) * inv;
     }
+    __syncwarp();
   }
   if (tid == 0) counters[blockIdx.y] = 0u;  // re-arm for the next call
   if constexpr (kGroup) {
@@ -291,7 +314,7 @@ extern "C" qsm_status moe_route(const uint16_t* x, const float* w_router,
                                 int32_t* dev_status, cudaStream_t stream) {
   using namespace qsm;
   if (T < 0 || H <= 0 || H % 64 || E < 1 || E > kMaxE || k < 1 || k > E ||
-      k > kMaxK)
+      k > kMaxK || (renormalize & ~kRouteFlags))
     return QSM_ERR_INVALID_ARGUMENT;
   if (T == 0) return QSM_OK;
   if (!x || !w_router || !topk_idx || !topk_w || !workspace || !dev_status)
@@ -331,6 +354,7 @@ extern "C" qsm_status moe_route_group(const uint16_t* x, const float* w_router,
                                       void* workspace, size_t workspace_bytes,
                                       int32_t* dev_status, cudaStream_t stream) {
   using namespace qsm;
+  if (renormalize & ~kRouteFlags) return QSM_ERR_INVALID_ARGUMENT;
   if (T < 1 || T > kTokPerCta || H <= 0 || H % 64 || E < 1 || E > kThreads ||
       k < 1 || k > E || k > kMaxK)
     return QSM_ERR_UNSUPPORTED;

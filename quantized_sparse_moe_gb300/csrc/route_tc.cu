@@ -208,7 +208,8 @@ route_tc_kernel(const __grid_constant__ Params p) {
     const size_t pstride = (size_t)p.T * p.E;
     const int e4 = p.E / 4;  // float4 columns
     const int n4 = rows * e4;
-    // the slices in order, then the bias; 8 positions per thread in flight
+    // the slices in order (the bias is added at selection); 8 positions
+    // per thread in flight
     for (int b0 = threadIdx.x; b0 < n4; b0 += kThreads * 8) {
       float4 sl[8][KS];
 #pragma unroll
@@ -236,21 +237,20 @@ route_tc_kernel(const __grid_constant__ Params p) {
             a.z += sl[u][s2].z;
             a.w += sl[u][s2].w;
           }
-          if (p.bias) {
-            const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias) + c);
-            a.x += bb.x;
-            a.y += bb.y;
-            a.z += bb.z;
-            a.w += bb.w;
-          }
           *reinterpret_cast<float4*>(lg + r * ld + 4 * c) = a;
         }
       }
     }
+    // the bias, after the tile (both fit in the free stage memory)
+    float* bsm = lg + BM * ld;
+    for (int c = threadIdx.x; c < p.E; c += kThreads) bsm[c] = p.bias ? __ldg(p.bias + c) : 0.f;
     __syncthreads();
-    // one thread per token: the best kMaxTopK in registers (value desc,
-    // index asc; indices arrive in ascending order, so an equal value never
-    // displaces)
+    // one thread per token: the best kMaxTopK selection logits (logit +
+    // bias) in registers (value desc, index asc; indices arrive in
+    // ascending order, so an equal value never displaces); the weights use
+    // the same logits, or the ones without the bias (selection-only bias)
+    const bool renorm = (p.renorm & QSM_ROUTE_RENORMALIZE) != 0;
+    const bool sel_only = (p.renorm & QSM_ROUTE_BIAS_SELECT_ONLY) != 0 && p.bias;
     const int r = threadIdx.x;
     if (r < rows) {
       const float* row = lg + r * ld;
@@ -264,7 +264,14 @@ route_tc_kernel(const __grid_constant__ Params p) {
       bool bad = false;
       for (int c0 = 0; c0 < p.E; c0 += 4) {
         const float4 a = *reinterpret_cast<const float4*>(row + c0);
-        const float l4[4] = {a.x, a.y, a.z, a.w};
+        float l4[4] = {a.x, a.y, a.z, a.w};
+        if (p.bias) {
+          const float4 bb = *reinterpret_cast<const float4*>(bsm + c0);
+          l4[0] = a.x + bb.x;
+          l4[1] = a.y + bb.y;
+          l4[2] = a.z + bb.z;
+          l4[3] = a.w + bb.w;
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float l = l4[c];
@@ -288,19 +295,44 @@ route_tc_kernel(const __grid_constant__ Params p) {
           }
         }
       }
-      const float top = val[0];
+      // weight logits of the selection, and the softmax's largest logit
+      float wl[kMaxTopK];
+#pragma unroll
+      for (int i = 0; i < kMaxTopK; ++i) {
+        wl[i] = val[i];
+        if (sel_only && i < p.k) {
+          wl[i] = row[idx[i]];
+          if (!isfinite(wl[i])) wl[i] = -INFINITY;
+        }
+      }
+      float top = -INFINITY;
       float denom = 0.f;
-      if (p.renorm) {
+      if (renorm) {
 #pragma unroll
         for (int i = 0; i < kMaxTopK; ++i)
-          if (i < p.k) denom += __expf(val[i] - top);
+          if (i < p.k) top = fmaxf(top, wl[i]);
+#pragma unroll
+        for (int i = 0; i < kMaxTopK; ++i)
+          if (i < p.k) denom += __expf(wl[i] - top);
       } else {
-        for (int c0 = 0; c0 < p.E; c0 += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(row + c0);
-          if (isfinite(a.x)) denom += __expf(a.x - top);
-          if (isfinite(a.y)) denom += __expf(a.y - top);
-          if (isfinite(a.z)) denom += __expf(a.z - top);
-          if (isfinite(a.w)) denom += __expf(a.w - top);
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int c0 = 0; c0 < p.E; c0 += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(row + c0);
+            float l4[4] = {a.x, a.y, a.z, a.w};
+            if (p.bias && !sel_only) {
+              const float4 bb = *reinterpret_cast<const float4*>(bsm + c0);
+              l4[0] = a.x + bb.x;
+              l4[1] = a.y + bb.y;
+              l4[2] = a.z + bb.z;
+              l4[3] = a.w + bb.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (!isfinite(l4[c])) continue;
+              if (pass == 0) top = fmaxf(top, l4[c]);
+              else denom += __expf(l4[c] - top);
+            }
+          }
         }
       }
       const float inv = 1.0f / denom;
@@ -309,7 +341,7 @@ route_tc_kernel(const __grid_constant__ Params p) {
       for (int i = 0; i < kMaxTopK; ++i) {
         if (i < p.k) {
           p.topk_idx[t * p.k + i] = idx[i];
-          p.topk_w[t * p.k + i] = __expf(val[i] - top) * inv;
+          p.topk_w[t * p.k + i] = __expf(wl[i] - top) * inv;
         }
       }
       if (bad) set_status(p.status, QSM_DEV_NONFINITE);

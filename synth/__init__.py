@@ -104,6 +104,13 @@ def draw_router(E: int, H: int, device="cpu", seed: int = 0,
                        dtype=torch.float32) * 0.05
 
 
+def draw_shared_gate(H: int, device="cpu", seed: int = 0, layer: int = 0) -> torch.Tensor:
+    """Shared-expert gate vector [H] fp32 ~ N(0, 0.05), like a router row
+    (the gate sigmoid(x . w) then spreads over (0, 1) for x ~ N(0, 1))."""
+    g = _gen(device, seed, layer, "shared_gate")
+    return torch.randn((H,), generator=g, device=device, dtype=torch.float32) * 0.05
+
+
 def zipf_logit_bias(E: int, H: int, seed: int = 0, layer: int = 0,
                     s: float = 1.0, in_noise_units: bool = True,
                     device="cpu") -> torch.Tensor:

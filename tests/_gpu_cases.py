@@ -34,14 +34,18 @@ def x_for(shape, T, seed, Lg, wr, bias, layer_id=0):
     return tie_free_x(cpu_view(Lg, wr, bias), T, seed=seed, layer=layer_id)
 
 
-def oracle_route(x, wr, bias, k, renormalize=True):
+def oracle_route(x, wr, bias, k, renormalize=True, bias_select_only=False):
     return oracle.route(bits16(x), wr.numpy(),
-                        k, None if bias is None else bias.numpy(), renormalize)
+                        k, None if bias is None else bias.numpy(), renormalize,
+                        bias_select_only)
 
 
-def check_layer_output(y, y32, x, idx_o, w_o, q, tokens=None):
-    """fp32 output within TOL of the oracle, bf16 output = RNE(fp32)."""
-    ref = oracle.moe_layer(bits16(x), idx_o, w_o, *q, tokens=tokens)
+def check_layer_output(y, y32, x, idx_o, w_o, q, tokens=None, shared_gate=None):
+    """fp32 output within TOL of the oracle, bf16 output = RNE(fp32).
+    shared_gate: the gate vector [H] of a gated shared expert, or None."""
+    sw = None if shared_gate is None else \
+        oracle.shared_gate(bits16(x), shared_gate.cpu().numpy())
+    ref = oracle.moe_layer(bits16(x), idx_o, w_o, *q, tokens=tokens, shared_w=sw)
     y32n = y32.cpu().numpy().astype(np.float64)
     yb = y.cpu()
     if tokens is not None:
