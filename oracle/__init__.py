@@ -90,6 +90,8 @@ def _load():
                                              ctypes.POINTER(_QMat),
                                              ctypes.POINTER(_QMat), P, P, i32, P]
             lib.orc_q8_gemv.argtypes = [P, P, P, i32, i32, P]
+            lib.orc_q8_quantize_x.argtypes = [P, i32, P, P]
+            lib.orc_q8_gemv_i8.argtypes = [P, P, P, P, i32, i32, P]
             lib.orc_max_threads.restype = ctypes.c_int
             lib.orc_set_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -304,6 +306,28 @@ def q8_gemv(x_bf16, q, d) -> np.ndarray:
     N, K = q.shape
     y = np.empty(N, np.float64)
     _load().orc_q8_gemv(_ptr(x), _ptr(q), _ptr(d), N, K, _ptr(y))
+    return y
+
+
+def q8_quantize_x(x_bf16):
+    """Activation x [K] -> (int8 codes [K], fp32 block scales [K/32])."""
+    x = _u16(x_bf16).ravel()
+    K = x.size
+    q = np.empty(K, np.int8)
+    d = np.empty(K // 32, np.float32)
+    _load().orc_q8_quantize_x(_ptr(x), K, _ptr(q), _ptr(d))
+    return q, d
+
+
+def q8_gemv_i8(qx, dx, q, d) -> np.ndarray:
+    """Q8_0 GEMV on a quantized activation (q8_quantize_x), fp64."""
+    qx = np.ascontiguousarray(qx, dtype=np.int8)
+    dx = np.ascontiguousarray(dx, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    d = _u16(d)
+    N, K = q.shape
+    y = np.empty(N, np.float64)
+    _load().orc_q8_gemv_i8(_ptr(qx), _ptr(dx), _ptr(q), _ptr(d), N, K, _ptr(y))
     return y
 
 

@@ -367,6 +367,55 @@ void orc_q8_gemv(const uint16_t* x_bf16, const int8_t* q, const uint16_t* d,
 
 /* ----------------------------------------------------------------- misc */
 
+/* ---------------------------------------- int8-activation Q8_0 GEMV mode */
+
+/* Quantize the activation once into Q8_0-style blocks of 32 ("Ember: packed
+ * Q8 decode": the Q/K/V and gate/up projections share one activation
+ * quantization, and the dot products then run on 8-bit groups).  Reading
+ * (the page gives no formula): per block b of 32 inputs, in fp32 as the
+ * kernel computes it, d[b] = max|x| / 127 and q[i] = round-half-away(x[i] /
+ * d[b]), clamped to [-127, 127]; an all-zero block has d = 0 and q = 0. */
+void orc_q8_quantize_x(const uint16_t* x_bf16, int32_t K, int8_t* q, float* d) {
+  for (int b = 0; b < K / 32; ++b) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+      const float v = (float)orc_bf16_to_f64(x_bf16[32 * b + i]);
+      const float a = v < 0.0f ? -v : v;
+      if (a > amax) amax = a;
+    }
+    const float db = amax / 127.0f;
+    d[b] = db;
+    for (int i = 0; i < 32; ++i) {
+      float r = 0.0f;
+      if (db != 0.0f) {
+        const float v = (float)orc_bf16_to_f64(x_bf16[32 * b + i]);
+        r = roundf(v / db);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+      }
+      q[32 * b + i] = (int8_t)r;
+    }
+  }
+}
+
+/* y[n] = sum_b dw[n][b] * dx[b] * sum_{i in b} qw[n][i] * qx[i]: the Q8_0
+ * GEMV on the quantized activation, each block's integer dot product exact,
+ * the rest in double. */
+void orc_q8_gemv_i8(const int8_t* qx, const float* dx, const int8_t* q,
+                    const uint16_t* d, int32_t N, int32_t K, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int b = 0; b < K / 32; ++b) {
+      long long isum = 0;
+      for (int i = 0; i < 32; ++i)
+        isum += (long long)q[(size_t)n * K + 32 * b + i] * (long long)qx[32 * b + i];
+      acc += orc_f16_to_f64(d[(size_t)n * (K / 32) + b]) * (double)dx[b] * (double)isum;
+    }
+    y[n] = acc;
+  }
+}
+
 int orc_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -53,6 +53,10 @@ MUTANTS = {
                                "acc += topk_w[(size_t)t * k + (k - 1 - j)] * o[(i * (k + 1) + j) * H + n];"),
     "gemv block index": ("orc_f16_to_f64(d[(size_t)n * (K / 32) + c / 32])",
                          "orc_f16_to_f64(d[(size_t)n * (K / 32)])"),
+    "activation scale 128": ("const float db = amax / 127.0f;", "const float db = amax / 128.0f;"),
+    "truncating activation codes": ("r = roundf(v / db);", "r = truncf(v / db);"),
+    "activation block scale index": ("* (double)dx[b] *", "* (double)dx[0] *"),
+    "int8 dot input index": ("(long long)qx[32 * b + i]", "(long long)qx[i]"),
     "matvec input index": ("acc += orc_weight(m, e, n, c) * x[c];",
                            "acc += orc_weight(m, e, n, c) * x[m->cols - 1 - c];"),
 }

@@ -476,3 +476,62 @@ def test_zipf_offset_leaves_empty_experts():
     E, H = 256, 2048
     b = synth.zipf_logit_bias(E, H, seed=0)
     assert b.max().item() == 0.0 and sorted(b.tolist())[0] < -10
+
+
+# --------------------------------------------- int8-activation GEMV mode
+
+def _exact_blocks(K, seed):
+    """x whose blocks are integers j * 2^-7 with max |j| = 127 per block
+    (then d = 2^-7 exactly and the codes are the integers j), with a
+    different power-of-two scale per block so block indices matter."""
+    rng = np.random.default_rng(seed)
+    j = rng.integers(-127, 128, size=K)
+    j[::32] = 127 * np.where(rng.random(K // 32) < 0.5, 1, -1)
+    scale = 2.0 ** (-7 - (np.arange(K) // 32) % 3)
+    return torch.from_numpy(j * scale).to(torch.bfloat16), j
+
+
+def test_quantize_x_exact_codes_and_special_blocks():
+    x, j = _exact_blocks(256, 40)
+    q, d = oracle.q8_quantize_x(bits16(x))
+    assert np.array_equal(q.astype(np.int64), j)
+    np.testing.assert_array_equal(d, (2.0 ** (-7 - np.arange(8) % 3)).astype(np.float32))
+    z = torch.zeros(64, dtype=torch.bfloat16)
+    z[40] = -3.0
+    qz, dz = oracle.q8_quantize_x(bits16(z))
+    assert dz[0] == 0.0 and not qz[:32].any()          # all-zero block
+    assert qz[40] == -127 and np.count_nonzero(qz[32:]) == 1
+    assert dz[1] == np.float32(3.0) / np.float32(127.0)
+
+
+def test_quantize_x_reconstruction_bound():
+    x = synth.draw_x(1, 4096, "cpu", seed=41).reshape(-1)
+    q, d = oracle.q8_quantize_x(bits16(x))
+    X = x.to(torch.float64).numpy()
+    err = np.abs(X - np.repeat(d.astype(np.float64), 32) * q)
+    # half a step, plus the fp32 rounding of x / d (|x / d| <= 127)
+    assert np.all(err <= np.repeat(d.astype(np.float64), 32) * (0.5 + 127 * 2.0 ** -22))
+    assert np.abs(q).max() == 127
+
+
+def test_gemv_i8_equals_exact_gemv_on_quantizable_x():
+    N, K = 40, 256
+    _, q, d = synth.draw_gemv(N, K, "cpu", seed=42)
+    x, _ = _exact_blocks(K, 43)
+    qx, dx = oracle.q8_quantize_x(bits16(x))
+    y8 = oracle.q8_gemv_i8(qx, dx, q.numpy(), bits16(d))
+    y = oracle.q8_gemv(bits16(x), q.numpy(), bits16(d))
+    np.testing.assert_allclose(y8, y, rtol=1e-12, atol=1e-12)
+
+
+def test_gemv_i8_within_quantization_bound():
+    N, K = 32, 512
+    x, q, d = synth.draw_gemv(N, K, "cpu", seed=44)
+    qx, dx = oracle.q8_quantize_x(bits16(x))
+    y8 = oracle.q8_gemv_i8(qx, dx, q.numpy(), bits16(d))
+    y = oracle.q8_gemv(bits16(x), q.numpy(), bits16(d))
+    dw = d.to(torch.float64).numpy().reshape(N, K // 32)
+    qa = np.abs(q.numpy().astype(np.float64)).reshape(N, K // 32, 32).sum(2)
+    bound = (np.abs(dw) * qa * dx.astype(np.float64)[None, :] / 2).sum(1)
+    assert np.all(np.abs(y8 - y) <= bound * (1 + 1e-6) + 1e-12)
+    assert np.abs(y8 - y).max() > 0   # it is an approximation
