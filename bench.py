@@ -57,6 +57,10 @@ WORKLOADS = {
                     desc="prefill T=4096, 1 layer, Zipf-offset routing, Q8_0"),
     "prefill_a4": dict(shape=synth.QWEN_A4, T=4096, layers=1, zipf="noise",
                        desc="prefill T=4096, 1 layer, Zipf-offset routing, affine-4 g64"),
+    "gemv": dict(gemv="f16", desc="Q8_0 GEMV batch 1, Llama-3.2-1B projection shapes "
+                                  "(2048x2048, 512x2048, 8192x2048, 2048x8192, 128256x2048)"),
+    "gemv_i8": dict(gemv="i8", desc="Q8_0 GEMV batch 1 on the int8-quantized activation, "
+                                    "Llama-3.2-1B projection shapes"),
 }
 
 
@@ -467,6 +471,172 @@ def run_reference(args, wl, rank, world):
     }
 
 
+
+# --------------------------------------------------------------- GEMV sweep
+
+def run_gemv(args, wl, rank, world):
+    """One step = one batch-1 GEMV per Llama-3.2-1B projection shape.  The
+    matrices that fit in L2 rotate over copies so a step's weights exceed
+    four times the L2 (129 MB); the LM head alone is larger than L2."""
+    import quantized_sparse_moe_gb300 as qsm
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    i8 = wl["gemv"] == "i8"
+    shapes = list(synth.GEMV_SHAPES.items())
+    small = sum(n * k for name, (n, k) in shapes if name != "lm_head") * 34 // 32
+    R = max(1, -(-4 * 129_000_000 // small))  # copies of the L2-sized matrices
+    mats = {}
+    for name, (n, k) in shapes:
+        copies = 1 if name == "lm_head" else R
+        mats[name] = [synth.draw_gemv(n, k, dev, seed=c, name=name) for c in range(copies)]
+    step_bytes = sum(n * k * 34 // 32 + 2 * (n + k) for name, (n, k) in shapes)
+    ys = {name: torch.empty(n, dtype=torch.bfloat16, device=dev) for name, (n, _) in shapes}
+    qbuf = {k: (torch.empty(k, dtype=torch.int8, device=dev),
+                torch.empty(k // 32, dtype=torch.float32, device=dev))
+            for k in {k for _, (_, k) in shapes}}
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(name, c, s):
+        x, q, d = mats[name][c % len(mats[name])]
+        if i8:
+            qx, dx = qbuf[q.shape[1]]
+            qsm.q8_quantize_x(x, qx, dx, stream=s)
+            qsm.q8_gemv_i8(qx, dx, q, d, ys[name], stream=s)
+        else:
+            qsm.q8_gemv(x, q, d, ys[name], stream=s)
+
+    def step(c, s):
+        for name, _ in shapes:
+            one(name, c, s)
+
+    with torch.cuda.stream(stream):
+        for c in range(R):
+            step(c, stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    n0 = qsm.launch_count()
+    with torch.cuda.graph(graph, stream=stream):
+        for c in range(R):
+            step(c, torch.cuda.current_stream())
+    launches_per_replay = qsm.launch_count() - n0
+    replays = max(1, -(-args.steps // R))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(dev.index) as clocks, torch.cuda.stream(stream):
+        time.sleep(0.25)
+        ev0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / (replays * R)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+    # per shape: a graph of its R rotations, timed alone
+    per_shape = {}
+    for name, (n, k) in shapes:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in range(R):
+                one(name, c, torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(20):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (20 * R)
+        by = n * k * 34 // 32
+        per_shape[name] = {"N": n, "K": k, "us": us, "GB/s": by / (us * 1e-6) / 1e9}
+    hbm, _, peak_kind = peaks()
+    top = max(per_shape, key=lambda k: per_shape[k]["us"])
+    # end to end: pinned host x in, host y out, each step
+    xh = {name: mats[name][0][0].cpu().pin_memory() for name, _ in shapes}
+    yh = {name: torch.empty_like(ys[name], device="cpu").pin_memory() for name, _ in shapes}
+    xd = {name: torch.empty_like(mats[name][0][0]) for name, _ in shapes}
+    e_ms = []
+    for r in range(args.warmup + min(args.steps, 200)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for name, _ in shapes:
+                xd[name].copy_(xh[name], non_blocking=True)
+                _, q, d = mats[name][r % len(mats[name])]
+                x = xd[name]
+                if i8:
+                    qx, dx = qbuf[q.shape[1]]
+                    qsm.q8_quantize_x(x, qx, dx, stream=stream)
+                    qsm.q8_gemv_i8(qx, dx, q, d, ys[name], stream=stream)
+                else:
+                    qsm.q8_gemv(x, q, d, ys[name], stream=stream)
+                yh[name].copy_(ys[name], non_blocking=True)
+        stream.synchronize()
+        if r >= args.warmup:
+            e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_ms = statistics.median(e_ms)
+    result = {
+        "metric": "Q8_0 GEMV weight GB/s (one GEMV per projection shape per step)",
+        "value": world * step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("int8 activation codes x int8 weight codes, s32 block sums, f32 scales"
+                  if i8 else "q8_0 weights, f16 MMA inputs, f32 accumulate"),
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl["desc"], "rotating_copies": R,
+                   "l2": f"weights per step {step_bytes / 1e6:.0f} MB, L2-sized matrices "
+                         f"rotate over {R} copies"},
+        "per_shape": per_shape,
+        "roofline": {"kernel": f"{'q8_gemv_i8' if i8 else 'q8_gemv'} {top} "
+                               f"({per_shape[top]['N']}x{per_shape[top]['K']})",
+                     "bound": "hbm", "achieved": per_shape[top]["GB/s"], "peak": hbm,
+                     "unit": "GB/s", "frac": per_shape[top]["GB/s"] / hbm, "traffic": None,
+                     "bytes_per_launch": per_shape[top]["N"] * per_shape[top]["K"] * 34 // 32,
+                     "launch_ms": per_shape[top]["us"] / 1e3, "peak_kind": peak_kind},
+        "step_roofline": {"bytes_per_step": step_bytes, "frac": step_bytes / (ms * 1e-3) / 1e9 / hbm},
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": sum(2 * k for _, (_, k) in shapes),
+                "d2h_bytes_per_step": sum(2 * n for _, (n, _) in shapes), "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_replay * replays,
+        "clocks": clocks.summary(),
+    }
+    return result, mats
+
+
+def gemv_cpu_baseline(wl, mats, budget_s=12.0):
+    """The fp64 oracle GEMV over the same shapes (copy 0), cycling until the
+    budget; GB/s of weights."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _helpers import bits16
+    host = {name: (bits16(m[0][0].cpu()), m[0][1].cpu().numpy(), bits16(m[0][2].cpu()))
+            for name, m in mats.items()}
+    t_used, by, calls = 0.0, 0, 0
+    i8 = wl["gemv"] == "i8"
+    while t_used < budget_s:
+        for name, (x, q, d) in host.items():
+            t0 = time.perf_counter()
+            if i8:
+                qx, dx = oracle.q8_quantize_x(x)
+                oracle.q8_gemv_i8(qx, dx, q, d)
+            else:
+                oracle.q8_gemv(x, q, d)
+            t_used += time.perf_counter() - t0
+            by += q.size * 34 // 32
+            calls += 1
+    return {"value": by / t_used / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "sample": f"{calls} GEMVs over the five shapes, "
+                                         f"{t_used:.1f} s of fp64 oracle"}
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,7 +673,29 @@ def main():
         wl["desc"] += ", gated shared expert"
     if args.bias_select_only:
         wl["desc"] += ", selection-only logit bias"
-    if args.impl == "reference":
+    if "gemv" in wl:
+        if args.impl == "reference":
+            res = None
+            if rank == 0:
+                import quantized_sparse_moe_gb300  # noqa: F401 (device init only)
+                dev = torch.device("cuda", 0)
+                mats = {name: [synth.draw_gemv(n, k, dev, seed=0, name=name)]
+                        for name, (n, k) in synth.GEMV_SHAPES.items()}
+                cb = gemv_cpu_baseline(wl, mats, budget_s=min(60.0, max(
+                    5.0, 90.0 * args.steps / (args.steps + args.warmup))))
+                res = {"impl": "reference", "metric": "Q8_0 GEMV weight GB/s (one GEMV per "
+                       "projection shape per step)", "value": cb["value"], "unit": "GB/s",
+                       "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                       "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                       "dtype": "f64", "data": "synthetic", "config": {"workload": wl["desc"]},
+                       "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "GB/s",
+                                                   "h2d_bytes_per_step": 0,
+                                                   "d2h_bytes_per_step": 0}}
+        else:
+            res, mats = run_gemv(args, wl, rank, world)
+            if rank == 0 and not args.no_cpu_baseline:
+                res["cpu_baseline"] = gemv_cpu_baseline(wl, mats)
+    elif args.impl == "reference":
         res = run_reference(args, wl, rank, world)
     else:
         res, (syn, fwds, xs) = run_ours(args, wl, rank, world)

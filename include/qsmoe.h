@@ -315,6 +315,26 @@ QSM_API qsm_status q8_gemv(const uint16_t* x, const int8_t* q, const uint16_t* d
                    int32_t N, int32_t K, uint16_t* y, int32_t* dev_status,
                    cudaStream_t stream);
 
+/* Int8-activation mode of the Q8_0 GEMV ["Ember: packed Q8 decode": the
+ * projections that read one activation share its quantization, and the dot
+ * products run on 8-bit groups].  Reading: blocks of 32 inputs, per block
+ * an fp32 scale dx = max|x| / 127 and codes qx = round-half-away(x / dx)
+ * clamped to [-127, 127] (fp32 arithmetic; an all-zero block has dx = 0).
+ *   q8_quantize_x:  x [K] bf16 -> qx [K] int8 (out), dx [K/32] fp32 (out);
+ *                   K % 32 == 0.
+ *   q8_gemv_i8:     y[n] = sum_b d[n,b] * dx[b] * sum_{c in b} q[n,c] * qx[c]
+ *                   (each block's integer dot product exact, the rest fp32),
+ *                   y [N] bf16 (out); N >= 1, K % 64 == 0, K <= 16384, qx,
+ *                   q, d, y 16-byte aligned.  A row's result does not depend
+ *                   on N.
+ * This changes the numerics against q8_gemv by the activation's rounding
+ * (at most half a step dx/2 per input). */
+QSM_API qsm_status q8_quantize_x(const uint16_t* x, int32_t K, int8_t* qx, float* dx,
+                                 int32_t* dev_status, cudaStream_t stream);
+QSM_API qsm_status q8_gemv_i8(const int8_t* qx, const float* dx, const int8_t* q,
+                              const uint16_t* d, int32_t N, int32_t K, uint16_t* y,
+                              int32_t* dev_status, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ misc */
 
 /* Static description of a status code. */

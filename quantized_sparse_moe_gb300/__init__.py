@@ -96,6 +96,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_forward_noalloc.restype = st
             L.q8_gemv.argtypes = [P, P, P, i32, i32, P, P, P]
             L.q8_gemv.restype = st
+            L.q8_quantize_x.argtypes = [P, i32, P, P, P, P]
+            L.q8_quantize_x.restype = st
+            L.q8_gemv_i8.argtypes = [P, P, P, P, i32, i32, P, P, P]
+            L.q8_gemv_i8.restype = st
             L.qsm_status_str.argtypes = [st]
             L.qsm_status_str.restype = ctypes.c_char_p
             L.qsm_abi_version.restype = i32
@@ -451,3 +455,29 @@ class MoEForward:
                         self.y, self.y_f32 if self.y_f32 is not None else False,
                         self.ffn_ws, self.dev_status, stream)
         return self.y
+
+
+def q8_quantize_x(x: torch.Tensor, qx=None, dx=None, dev_status=None, stream=None):
+    """x [K] bf16 -> (qx [K] int8, dx [K/32] fp32): the activation quantized
+    once for the int8-activation GEMV."""
+    K = x.numel()
+    dev = x.device
+    if qx is None:
+        qx = torch.empty(K, dtype=torch.int8, device=dev)
+    if dx is None:
+        dx = torch.empty(K // 32, dtype=torch.float32, device=dev)
+    dev_status = _status(dev_status, dev)
+    _check(lib().q8_quantize_x(_p(_u16(x)), K, _p(qx), _p(dx), _p(dev_status),
+                               _stream(stream)), "q8_quantize_x")
+    return qx, dx
+
+
+def q8_gemv_i8(qx: torch.Tensor, dx: torch.Tensor, q: torch.Tensor, d: torch.Tensor,
+               y=None, dev_status=None, stream=None) -> torch.Tensor:
+    N, K = q.shape
+    if y is None:
+        y = torch.empty(N, dtype=torch.bfloat16, device=q.device)
+    dev_status = _status(dev_status, q.device)
+    _check(lib().q8_gemv_i8(_p(qx), _p(dx), _p(q), _p(_u16(d)), N, K, _p(y),
+                            _p(dev_status), _stream(stream)), "q8_gemv_i8")
+    return y

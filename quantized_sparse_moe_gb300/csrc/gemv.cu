@@ -85,6 +85,132 @@ cudaError_t launch_ks(const uint16_t* x, const int8_t* q, const uint16_t* d,
                     reinterpret_cast<const __half*>(d), N, K, y);
 }
 
+// ------------------------------------------ int8-activation mode (i8 x i8)
+//
+// "Ember: packed Q8 decode": the projections that read the same activation
+// share one quantization of it, and the dot products run on 8-bit groups.
+// q8_quantize_x turns x into blocks of 32 int8 codes with an fp32 scale
+// max|x| / 127 (codes round half away from zero); q8_gemv_i8 then takes
+// each 32-wide block's dot product exactly as an int8 tensor-core MMA
+// (m16n8k32, one block per MMA, the activation in column 0) and scales it
+// by weight scale * activation scale in fp32.  Same tiling and K-segment
+// order as the f16 GEMV, so results do not depend on N.
+
+__global__ void __launch_bounds__(256)
+q8_quantize_x_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ qx,
+                     float* __restrict__ dx) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // block of 32
+  if (b >= K / 32) return;
+  const float v = __uint_as_float((uint32_t)x[32 * b + lane] << 16);
+  const float amax = warp_max(fabsf(v));
+  const float db = amax / 127.0f;
+  float r = 0.f;
+  if (db != 0.f) r = fminf(fmaxf(roundf(v / db), -127.f), 127.f);
+  qx[32 * b + lane] = (int8_t)r;
+  if (lane == 0) dx[b] = db;
+}
+
+// D(16x8, s32) = A(16x32, s8, row) * B(32x8, s8, col).
+__device__ __forceinline__ void mma_16832_s8(int (&d)[4], const uint32_t (&a)[4],
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
+template <int KS>
+__global__ void __launch_bounds__((KS > 8 ? KS : 8) * 32)
+q8_gemv_i8_kernel(const int8_t* __restrict__ qx, const float* __restrict__ dx,
+                  const int8_t* __restrict__ q8, const __half* __restrict__ d, int N,
+                  int K, uint16_t* __restrict__ y) {
+  constexpr int W = KS > 8 ? KS : 8;  // warps per CTA
+  constexpr int TPC = W / KS;         // 16-row tiles per CTA
+  extern __shared__ float red[];      // [segments][TPC][16]
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int kw = warp % KS, tl = warp / KS;
+  const int n0 = (blockIdx.x * TPC + tl) * 16;
+  QW w;
+  w.codes = reinterpret_cast<const uint8_t*>(q8);
+  w.scales = d;
+  w.biases = nullptr;
+  w.cols = K;
+  const int rg = min(n0 + g, N - 1), rh = min(n0 + g + 8, N - 1);
+  const int nseg = (K + kSeg - 1) / kSeg;
+  for (int seg = kw; seg < nseg; seg += KS) {
+    float ag = 0.f, ah = 0.f;  // rows g and g + 8 (lanes with q == 0)
+    const int kend = min(K, (seg + 1) * kSeg);
+#pragma unroll 4
+    for (int k0 = seg * kSeg; k0 < kend; k0 += 64) {
+      RawA r;
+      load_a<QSM_Q8_0>(r, w, rg, rh, k0, q);
+      // lane (g, q) holds codes k0 + 8q .. + 7 of its rows; the MMA's k
+      // groups 4q.. and 16 + 4q.. take the low and high halves, and the
+      // activation codes (column 0, lanes g == 0) follow the same mapping
+      uint2 x0 = make_uint2(0u, 0u), x1 = x0;
+      if (g == 0) {
+        x0 = __ldg(reinterpret_cast<const uint2*>(qx + k0 + 8 * q));
+        x1 = __ldg(reinterpret_cast<const uint2*>(qx + k0 + 32 + 8 * q));
+      }
+      int s0[4], s1[4];
+      const uint32_t a0[4] = {r.g0.x, r.h0.x, r.g0.y, r.h0.y};
+      const uint32_t a1[4] = {r.g1.x, r.h1.x, r.g1.y, r.h1.y};
+      mma_16832_s8(s0, a0, x0.x, x0.y);
+      mma_16832_s8(s1, a1, x1.x, x1.y);
+      if (q == 0) {
+        const float d0 = __ldg(dx + k0 / 32), d1 = __ldg(dx + k0 / 32 + 1);
+        const float sg0 = __half2float(__ushort_as_half((unsigned short)(r.sg & 0xffffu)));
+        const float sg1 = __half2float(__ushort_as_half((unsigned short)(r.sg >> 16)));
+        const float sh0 = __half2float(__ushort_as_half((unsigned short)(r.sh & 0xffffu)));
+        const float sh1 = __half2float(__ushort_as_half((unsigned short)(r.sh >> 16)));
+        ag = fmaf((float)s0[0], sg0 * d0, ag);
+        ag = fmaf((float)s1[0], sg1 * d1, ag);
+        ah = fmaf((float)s0[2], sh0 * d0, ah);
+        ah = fmaf((float)s1[2], sh1 * d1, ah);
+      }
+    }
+    if (q == 0) {
+      red[(seg * TPC + tl) * 16 + g] = ag;
+      red[(seg * TPC + tl) * 16 + g + 8] = ah;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < TPC * 16) {
+    const int t2 = threadIdx.x / 16, r = threadIdx.x % 16;
+    float s = 0.f;
+    for (int seg = 0; seg < nseg; ++seg) s += red[(seg * TPC + t2) * 16 + r];
+    const int n = (blockIdx.x * TPC + t2) * 16 + r;
+    if (n < N) y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  }
+}
+
+template <int KS>
+cudaError_t launch_i8_ks(const int8_t* qx, const float* dx, const int8_t* q,
+                         const uint16_t* d, int N, int K, uint16_t* y, cudaStream_t s) {
+  constexpr int W = KS > 8 ? KS : 8;
+  constexpr int TPC = W / KS;
+  const int tiles = (N + 15) / 16;
+  const int grid = (tiles + TPC - 1) / TPC;
+  const size_t smem = (size_t)((K + kSeg - 1) / kSeg) * TPC * 16 * sizeof(float);
+  return launch_pdl(q8_gemv_i8_kernel<KS>, dim3(grid), dim3(W * 32), smem, s, qx, dx, q,
+                    reinterpret_cast<const __half*>(d), N, K, y);
+}
+
+int gemv_split(int N, int K) {  // K segments per tile: about 24 warps per SM
+  const long tiles = (N + 15) / 16;
+  int ks = 1;
+  const int nseg = (K + kSeg - 1) / kSeg;
+  while (ks < 32 && ks < nseg && tiles * ks < 152L * 24) ks *= 2;
+  return ks;
+}
+
 }  // namespace
 }  // namespace qsm
 
@@ -100,18 +226,47 @@ extern "C" qsm_status q8_gemv(const uint16_t* x, const int8_t* q,
     return QSM_ERR_INVALID_ARGUMENT;
   if ((size_t)N * K >= ((size_t)1 << 40) || K > 16384) return QSM_ERR_UNSUPPORTED;
   // Split K until there are enough warps in flight (about 24 per SM).
-  const long tiles = (N + 15) / 16;
-  int ks = 1;
-  const int nseg = (K + kSeg - 1) / kSeg;
-  while (ks < 32 && ks < nseg && tiles * ks < 152L * 24) ks *= 2;
   cudaError_t err;
-  switch (ks) {
+  switch (gemv_split(N, K)) {
     case 1: err = launch_ks<1>(x, q, d, N, K, y, stream); break;
     case 2: err = launch_ks<2>(x, q, d, N, K, y, stream); break;
     case 4: err = launch_ks<4>(x, q, d, N, K, y, stream); break;
     case 8: err = launch_ks<8>(x, q, d, N, K, y, stream); break;
     case 16: err = launch_ks<16>(x, q, d, N, K, y, stream); break;
     default: err = launch_ks<32>(x, q, d, N, K, y, stream); break;
+  }
+  return err == cudaSuccess ? QSM_OK : QSM_ERR_CUDA;
+}
+
+extern "C" qsm_status q8_quantize_x(const uint16_t* x, int32_t K, int8_t* qx, float* dx,
+                                    int32_t* dev_status, cudaStream_t stream) {
+  using namespace qsm;
+  (void)dev_status;
+  if (K < 32 || K % 32 || !x || !qx || !dx) return QSM_ERR_INVALID_ARGUMENT;
+  const int blocks = K / 32;
+  QSM_CUDA_TRY(launch_pdl(q8_quantize_x_kernel, dim3((blocks + 7) / 8), dim3(256), 0,
+                          stream, x, (int)K, qx, dx));
+  return QSM_OK;
+}
+
+extern "C" qsm_status q8_gemv_i8(const int8_t* qx, const float* dx, const int8_t* q,
+                                 const uint16_t* d, int32_t N, int32_t K, uint16_t* y,
+                                 int32_t* dev_status, cudaStream_t stream) {
+  using namespace qsm;
+  (void)dev_status;
+  if (N < 1 || K < 64 || K % 64 || !qx || !dx || !q || !d || !y)
+    return QSM_ERR_INVALID_ARGUMENT;
+  if (!aligned16(qx) || !aligned4(dx) || !aligned16(q) || !aligned16(d) || !aligned16(y))
+    return QSM_ERR_INVALID_ARGUMENT;
+  if ((size_t)N * K >= ((size_t)1 << 40) || K > 16384) return QSM_ERR_UNSUPPORTED;
+  cudaError_t err;
+  switch (gemv_split(N, K)) {
+    case 1: err = launch_i8_ks<1>(qx, dx, q, d, N, K, y, stream); break;
+    case 2: err = launch_i8_ks<2>(qx, dx, q, d, N, K, y, stream); break;
+    case 4: err = launch_i8_ks<4>(qx, dx, q, d, N, K, y, stream); break;
+    case 8: err = launch_i8_ks<8>(qx, dx, q, d, N, K, y, stream); break;
+    case 16: err = launch_i8_ks<16>(qx, dx, q, d, N, K, y, stream); break;
+    default: err = launch_i8_ks<32>(qx, dx, q, d, N, K, y, stream); break;
   }
   return err == cudaSuccess ? QSM_OK : QSM_ERR_CUDA;
 }

@@ -68,3 +68,66 @@ def test_gemv_ragged_rows(qsm):
         y = qsm.q8_gemv(x, q, d)
         ref = oracle.q8_gemv(bits16(x), q.cpu().numpy(), bits16(d))
         assert_faithful_bf16(y.float().cpu().numpy(), ref)
+
+
+# ------------------------------------------------ int8-activation mode
+
+@pytest.mark.parametrize("K", [64, 2048, 8192])
+def test_quantize_x_bit_exact(qsm, K):
+    """The activation codes and block scales equal the oracle's bit for bit
+    (both decide in fp32), including an all-zero block and exact halves."""
+    x = synth.draw_x(1, K, "cuda", seed=50 + K)[0]
+    x[32:64] = 0.0
+    qx, dx = qsm.q8_quantize_x(x)
+    torch.cuda.synchronize()
+    q_o, d_o = oracle.q8_quantize_x(bits16(x))
+    assert np.array_equal(qx.cpu().numpy(), q_o)
+    assert np.array_equal(dx.cpu().numpy().view(np.uint32), d_o.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", sorted(synth.GEMV_SHAPES))
+def test_gemv_i8_shapes(qsm, name):
+    """On the Llama-3.2-1B shapes the int8-activation GEMV is within one
+    bf16 ulp of its fp64 oracle (exact block dot products, the same codes)."""
+    N, K = synth.GEMV_SHAPES[name]
+    x, q, d = synth.draw_gemv(N, K, "cuda", seed=7, name=name)
+    qx, dx = qsm.q8_quantize_x(x)
+    y = qsm.q8_gemv_i8(qx, dx, q, d)
+    torch.cuda.synchronize()
+    rows = np.arange(N) if N <= 8192 else np.random.default_rng(1).choice(N, 4096, replace=False)
+    q_o, d_o = oracle.q8_quantize_x(bits16(x))
+    ref = oracle.q8_gemv_i8(q_o, d_o, q[rows].cpu().numpy(), bits16(d[rows]))
+    assert_faithful_bf16(y.float().cpu().numpy()[rows], ref)
+
+
+def test_gemv_i8_ragged_and_fused_rows(qsm):
+    """Ragged N, and rows of a [gate; up] concatenation bit-identical to the
+    separate projections (the summation order depends on K only)."""
+    N, K = 1000, 2048
+    x, gq, gd = synth.draw_gemv(N, K, "cuda", seed=8, name="gate")
+    _, uq, ud = synth.draw_gemv(N, K, "cuda", seed=9, name="up")
+    qx, dx = qsm.q8_quantize_x(x)
+    fused = qsm.q8_gemv_i8(qx, dx, torch.cat([gq, uq]), torch.cat([gd, ud]))
+    g = qsm.q8_gemv_i8(qx, dx, gq, gd)
+    u = qsm.q8_gemv_i8(qx, dx, uq, ud)
+    torch.cuda.synchronize()
+    assert torch.equal(fused[:N].view(torch.int16), g.view(torch.int16))
+    assert torch.equal(fused[N:].view(torch.int16), u.view(torch.int16))
+    q_o, d_o = oracle.q8_quantize_x(bits16(x))
+    assert_faithful_bf16(g.float().cpu().numpy(),
+                         oracle.q8_gemv_i8(q_o, d_o, gq.cpu().numpy(), bits16(gd)))
+
+
+def test_gemv_i8_close_to_exact_gemv(qsm):
+    """The activation's rounding moves the result by at most the analytic
+    bound sum_b |d| * sum|q| * dx / 2 from the exact Q8_0 GEMV."""
+    N, K = 512, 2048
+    x, q, d = synth.draw_gemv(N, K, "cuda", seed=10)
+    qx, dx = qsm.q8_quantize_x(x)
+    y8 = qsm.q8_gemv_i8(qx, dx, q, d).float().cpu().numpy()
+    y = oracle.q8_gemv(bits16(x), q.cpu().numpy(), bits16(d))
+    dw = d.cpu().to(torch.float64).numpy().reshape(N, K // 32)
+    qa = np.abs(q.cpu().numpy().astype(np.float64)).reshape(N, K // 32, 32).sum(2)
+    bound = (dw * qa * dx.cpu().numpy().astype(np.float64)[None, :] / 2).sum(1)
+    ulp = np.abs(y) * 2.0 ** -8  # the bf16 output rounding
+    assert np.all(np.abs(y8 - y) <= bound + ulp + 1e-6)
