@@ -310,7 +310,12 @@ QSM_API qsm_status moe_ffn_forward_noalloc(const qsm_moe_layer* L,
  * [Perplexity page, "Optimizing the single-row weight path"; Ember page,
  * Q8_0 rows].
  *   x [K] bf16;  q [N, K] int8;  d [N, K/32] fp16;  y [N] bf16 (out).
- * Requires K % 64 == 0, 64 <= K <= 16384, N >= 1. */
+ * Requires K % 64 == 0, 64 <= K <= 16384, N >= 1; x, q, d, y 16-byte
+ * aligned.  With K % 256 == 0 the weight tiles arrive by TMA copies whose
+ * waits are bounded: a copy that never completes sets QSM_DEV_TIMEOUT in
+ * *dev_status (which may be NULL: nothing is reported then).  A row's
+ * result does not depend on N (K is summed in fixed 512-wide segments, in
+ * segment order). */
 QSM_API qsm_status q8_gemv(const uint16_t* x, const int8_t* q, const uint16_t* d,
                    int32_t N, int32_t K, uint16_t* y, int32_t* dev_status,
                    cudaStream_t stream);

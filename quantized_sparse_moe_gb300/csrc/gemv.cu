@@ -15,6 +15,7 @@
 // concatenation come out bit-identical to those of the separate matrices
 // (the property the oMLX gate/up fusion relies on).
 #include "gemv_core.cuh"
+#include "tc_common.cuh"
 
 namespace qsm {
 namespace {
@@ -203,6 +204,181 @@ cudaError_t launch_i8_ks(const int8_t* qx, const float* dx, const int8_t* q,
                     reinterpret_cast<const __half*>(d), N, K, y);
 }
 
+// ------------------------------------------ TMA-fed tiles (K % 256 == 0)
+//
+// One CTA = one 16-row tile x `spc` consecutive 512-wide segments, one warp
+// per segment.  A segment's codes (16 rows x 512 bytes) arrive by a single
+// TMA copy of the 3D row view (128-byte swizzle, so the fragment reads of the
+// 8 rows g land in 8 different 16-byte units and are free of bank
+// conflicts), its block scales by a second copy, both issued before the
+// programmatic-launch wait since the weights are static.  When one CTA does
+// not take all of K, the CTAs of a tile form a cluster along x and store
+// their segment partials into the rank-0 CTA's shared memory, which adds
+// them in segment order: the order of the register-fed kernels above, so
+// every row comes out bit-identical to theirs and independent of N.  Rows
+// past N and chunks past K arrive as zeros (TMA fill) and are never stored.
+
+constexpr int kTmaSegBytes = 16 * kSeg;              // codes of one segment
+constexpr int kTmaScaleBytes = 16 * (kSeg / 32) * 2;  // its 16 x 16 fp16 scales
+constexpr int kTmaMaxSpc = 4;
+constexpr int kTmaMaxSeg = 32;                        // K <= 16384
+
+// 8 bytes at byte b (a multiple of 8) of 128-byte line `line` of a tile
+// written with the 128-byte swizzle.
+__device__ __forceinline__ uint2 lds_sw128(const unsigned char* tile, int line, int b) {
+  return *reinterpret_cast<const uint2*>(
+      tile + line * 128 + ((((b >> 4) ^ (line & 7)) << 4) | (b & 15)));
+}
+
+template <bool kI8>
+__global__ void __launch_bounds__(kTmaMaxSpc * 32)
+q8_gemv_tma_kernel(const __grid_constant__ CUtensorMap cmap,
+                   const __grid_constant__ CUtensorMap smap,
+                   const uint16_t* __restrict__ x, const int8_t* __restrict__ qx,
+                   const float* __restrict__ dx, int N, int K, int spc, int tiles,
+                   uint16_t* __restrict__ y, int32_t* dev_status) {
+  extern __shared__ unsigned char gemv_dyn[];
+  __shared__ __align__(8) uint64_t bar[kTmaMaxSpc];
+  __shared__ float red[kTmaMaxSeg][16];  // [segment][row], used in rank 0
+  const int tile = blockIdx.y + gridDim.y * blockIdx.z;
+  if (tile >= tiles) return;  // the whole cluster shares the tile
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int n0 = tile * 16;
+  const int nseg = (K + kSeg - 1) / kSeg;
+  const int seg0 = blockIdx.x * spc;
+  const int mine = min(spc, nseg - seg0);
+  const uint32_t pad = (1024u - (smem_u32(gemv_dyn) & 1023u)) & 1023u;
+  unsigned char* codes = gemv_dyn + pad;               // [spc][4][16][128]
+  unsigned char* scl = codes + spc * kTmaSegBytes;     // [spc][16][16] fp16
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < mine; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < mine; ++s) {
+      mbar_arrive_expect_tx(&bar[s], kTmaSegBytes + kTmaScaleBytes);
+      tc::tma_load_3d(codes + s * kTmaSegBytes, &cmap, 0, n0, (seg0 + s) * (kSeg / 128),
+                      &bar[s]);
+      tc::tma_load_2d(scl + s * kTmaScaleBytes, &smap, (seg0 + s) * (kSeg / 32), n0,
+                      &bar[s]);
+    }
+  }
+  pdl_wait();  // x (or its codes) come from the preceding launch
+  pdl_launch_dependents();
+  float pg = 0.f, ph = 0.f;  // rows g and g + 8 (lanes q == 0)
+  if (warp < mine) {
+    if (!mbar_wait_bounded(&bar[warp], 0, kWaitIters)) {
+      if (lane == 0 && dev_status) set_status(dev_status, QSM_DEV_TIMEOUT);
+      mbar_wait_bounded(&bar[warp], 0, kWaitIters);  // let the copy land
+    } else {
+      const unsigned char* cs = codes + warp * kTmaSegBytes;
+      const uint32_t* ss = reinterpret_cast<const uint32_t*>(scl + warp * kTmaScaleBytes);
+      const int kb = (seg0 + warp) * kSeg;
+      const int nch = min(kSeg, K - kb) / 64;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int ch = 0; ch < nch; ++ch) {
+        RawA r;
+        const int lg = (ch >> 1) * 16 + g;  // line of row g in 128-byte chunk ch / 2
+        const int b = (ch & 1) * 64 + 8 * q;
+        r.g0 = lds_sw128(cs, lg, b);
+        r.g1 = lds_sw128(cs, lg, b + 32);
+        r.h0 = lds_sw128(cs, lg + 8, b);
+        r.h1 = lds_sw128(cs, lg + 8, b + 32);
+        r.sg = ss[g * 8 + ch];
+        r.sh = ss[(g + 8) * 8 + ch];
+        const int k0 = kb + 64 * ch;
+        if constexpr (!kI8) {
+          uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
+          if (g == 0) {
+            X0 = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(x + k0 + 8 * q)));
+            X1 = bf16x8_to_f16x8(
+                __ldg(reinterpret_cast<const uint4*>(x + k0 + 32 + 8 * q)));
+          }
+          chunk_mma<QSM_Q8_0>(acc, r, X0, X1);
+        } else {
+          uint2 x0 = make_uint2(0u, 0u), x1 = x0;
+          if (g == 0) {
+            x0 = __ldg(reinterpret_cast<const uint2*>(qx + k0 + 8 * q));
+            x1 = __ldg(reinterpret_cast<const uint2*>(qx + k0 + 32 + 8 * q));
+          }
+          int s0[4], s1[4];
+          const uint32_t a0[4] = {r.g0.x, r.h0.x, r.g0.y, r.h0.y};
+          const uint32_t a1[4] = {r.g1.x, r.h1.x, r.g1.y, r.h1.y};
+          mma_16832_s8(s0, a0, x0.x, x0.y);
+          mma_16832_s8(s1, a1, x1.x, x1.y);
+          if (q == 0) {
+            const float d0 = __ldg(dx + k0 / 32), d1 = __ldg(dx + k0 / 32 + 1);
+            const float sg0 = __half2float(__ushort_as_half((unsigned short)(r.sg & 0xffffu)));
+            const float sg1 = __half2float(__ushort_as_half((unsigned short)(r.sg >> 16)));
+            const float sh0 = __half2float(__ushort_as_half((unsigned short)(r.sh & 0xffffu)));
+            const float sh1 = __half2float(__ushort_as_half((unsigned short)(r.sh >> 16)));
+            acc[0] = fmaf((float)s0[0], sg0 * d0, acc[0]);
+            acc[0] = fmaf((float)s1[0], sg1 * d1, acc[0]);
+            acc[2] = fmaf((float)s0[2], sh0 * d0, acc[2]);
+            acc[2] = fmaf((float)s1[2], sh1 * d1, acc[2]);
+          }
+        }
+      }
+      pg = acc[0];
+      ph = acc[2];
+    }
+  }
+  if (warp < mine && q == 0) {
+    const int seg = seg0 + warp;
+    if (gridDim.x == 1) {
+      red[seg][g] = pg;
+      red[seg][g + 8] = ph;
+    } else {
+      dsmem_st_f32(dsmem_addr(&red[seg][g], 0), pg);
+      dsmem_st_f32(dsmem_addr(&red[seg][g + 8], 0), ph);
+    }
+  }
+  if (gridDim.x > 1) cluster_sync_all();
+  else __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x < 16) {
+    float s = 0.f;
+    for (int seg = 0; seg < nseg; ++seg) s += red[seg][threadIdx.x];
+    const int n = n0 + threadIdx.x;
+    if (n < N) y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  }
+}
+
+// Segments per CTA: as many as possible (at most 4) while the grid keeps at
+// least ~1024 CTAs, and few enough that a tile's CTAs fit one cluster of 8.
+int gemv_tma_spc(long tiles, int nseg) {
+  const int lo = (nseg + 7) / 8;
+  int spc = nseg < kTmaMaxSpc ? nseg : kTmaMaxSpc;
+  while (spc / 2 >= lo && tiles * ((nseg + spc - 1) / spc) < 1024) spc /= 2;
+  return spc;
+}
+
+// Launches the TMA-fed kernel; false when the shape or the tensor maps do
+// not allow it (the caller then uses the register-fed kernels).
+template <bool kI8>
+bool launch_tma(const uint16_t* x, const int8_t* qx, const float* dx, const int8_t* q,
+                const uint16_t* d, int N, int K, uint16_t* y, int32_t* status,
+                cudaStream_t s, cudaError_t* err) {
+  if (K % 256) return false;
+  CUtensorMap cmap, smap;
+  if (!tc::make_map_rows3d(&cmap, q, (uint64_t)N, (uint64_t)K, 16, kSeg / 128)) return false;
+  if (!tc::make_map_2d(&smap, d, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)N,
+                       (uint64_t)K / 32, kSeg / 32, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return false;
+  const long tiles = (N + 15) / 16;
+  const int nseg = (K + kSeg - 1) / kSeg;
+  const int spc = gemv_tma_spc(tiles, nseg);
+  const int slices = (nseg + spc - 1) / spc;
+  const long gy = tiles < 65535 ? tiles : 65535;
+  const dim3 grid(slices, (unsigned)gy, (unsigned)((tiles + gy - 1) / gy));
+  const size_t smem = 1024 + (size_t)spc * (kTmaSegBytes + kTmaScaleBytes);
+  *err = launch_pdl_cluster(q8_gemv_tma_kernel<kI8>, grid, dim3(spc * 32), slices, smem, s,
+                            cmap, smap, x, qx, dx, N, K, spc, (int)tiles, y, status);
+  return true;
+}
+
 int gemv_split(int N, int K) {  // K segments per tile: about 24 warps per SM
   const long tiles = (N + 15) / 16;
   int ks = 1;
@@ -219,14 +395,15 @@ extern "C" qsm_status q8_gemv(const uint16_t* x, const int8_t* q,
                               uint16_t* y, int32_t* dev_status,
                               cudaStream_t stream) {
   using namespace qsm;
-  (void)dev_status;  // nothing device-side to report for a dense GEMV
   if (N < 1 || K < 64 || K % 64 || !x || !q || !d || !y)
     return QSM_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(q) || !aligned16(d) || !aligned16(y))
     return QSM_ERR_INVALID_ARGUMENT;
   if ((size_t)N * K >= ((size_t)1 << 40) || K > 16384) return QSM_ERR_UNSUPPORTED;
-  // Split K until there are enough warps in flight (about 24 per SM).
   cudaError_t err;
+  if (launch_tma<false>(x, nullptr, nullptr, q, d, N, K, y, dev_status, stream, &err))
+    return err == cudaSuccess ? QSM_OK : QSM_ERR_CUDA;
+  // Split K until there are enough warps in flight (about 24 per SM).
   switch (gemv_split(N, K)) {
     case 1: err = launch_ks<1>(x, q, d, N, K, y, stream); break;
     case 2: err = launch_ks<2>(x, q, d, N, K, y, stream); break;
@@ -253,13 +430,14 @@ extern "C" qsm_status q8_gemv_i8(const int8_t* qx, const float* dx, const int8_t
                                  const uint16_t* d, int32_t N, int32_t K, uint16_t* y,
                                  int32_t* dev_status, cudaStream_t stream) {
   using namespace qsm;
-  (void)dev_status;
   if (N < 1 || K < 64 || K % 64 || !qx || !dx || !q || !d || !y)
     return QSM_ERR_INVALID_ARGUMENT;
   if (!aligned16(qx) || !aligned4(dx) || !aligned16(q) || !aligned16(d) || !aligned16(y))
     return QSM_ERR_INVALID_ARGUMENT;
   if ((size_t)N * K >= ((size_t)1 << 40) || K > 16384) return QSM_ERR_UNSUPPORTED;
   cudaError_t err;
+  if (launch_tma<true>(nullptr, qx, dx, q, d, N, K, y, dev_status, stream, &err))
+    return err == cudaSuccess ? QSM_OK : QSM_ERR_CUDA;
   switch (gemv_split(N, K)) {
     case 1: err = launch_i8_ks<1>(qx, dx, q, d, N, K, y, stream); break;
     case 2: err = launch_i8_ks<2>(qx, dx, q, d, N, K, y, stream); break;

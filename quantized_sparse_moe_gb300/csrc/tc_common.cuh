@@ -53,7 +53,38 @@ inline bool make_map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row tiles of a row-major byte matrix [rows, cols] (cols a multiple of 128)
+// seen as the 3D tensor {128 bytes, rows, cols / 128}: one box of
+// {128, box_rows, box_chunks} brings box_rows full rows of box_chunks * 128
+// bytes in a single copy, laid out [chunk][row][128 bytes] with the 128-byte
+// swizzle (16-byte unit u of line L stored at unit u ^ (L & 7)).  The
+// chunk dimension's stride (128) is smaller than the row stride: the view
+// overlaps nothing, it only reorders the box.
+inline bool make_map_rows3d(CUtensorMap* m, const void* base, uint64_t rows,
+                            uint64_t cols, uint32_t box_rows, uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || cols % 128) return false;
+  const cuuint64_t dims[3] = {128, rows, cols / 128};
+  const cuuint64_t strides[2] = {cols, 128};
+  const cuuint32_t box[3] = {128, box_rows, box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // -------------------------------------------------------------- device
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map,
+                                            int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(smem_u32(bar))
+      : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
                                             int c0, int c1, uint64_t* bar) {

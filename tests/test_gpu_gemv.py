@@ -70,6 +70,39 @@ def test_gemv_ragged_rows(qsm):
         assert_faithful_bf16(y.float().cpu().numpy(), ref)
 
 
+# K % 256 == 0 takes the TMA-fed tiles (one cluster per tile when the
+# segments are split over CTAs: K = 768 with a partial last segment, K =
+# 16384 with 8 CTAs per tile); the other K take the register-fed kernels.
+GEMV_EDGE = [(33, 768), (7, 16384), (100, 832), (64, 64), (3000, 2304), (129, 256)]
+
+
+@pytest.mark.parametrize("N,K", GEMV_EDGE)
+def test_gemv_edge_shapes(qsm, N, K):
+    x, q, d = synth.draw_gemv(N, K, "cuda", seed=N + K)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = qsm.q8_gemv(x, q, d, dev_status=st)
+    qx, dx = qsm.q8_quantize_x(x)
+    y8 = qsm.q8_gemv_i8(qx, dx, q, d, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_faithful_bf16(y.float().cpu().numpy(),
+                         oracle.q8_gemv(bits16(x), q.cpu().numpy(), bits16(d)))
+    q_o, d_o = oracle.q8_quantize_x(bits16(x))
+    assert_faithful_bf16(y8.float().cpu().numpy(),
+                         oracle.q8_gemv_i8(q_o, d_o, q.cpu().numpy(), bits16(d)))
+
+
+def test_gemv_rows_independent_of_n(qsm):
+    """A row's bits do not depend on how many rows the call has (the split
+    of K over CTAs changes with N; the summation order does not)."""
+    K = 8192
+    x, q, d = synth.draw_gemv(4096, K, "cuda", seed=12)
+    full = qsm.q8_gemv(x, q, d)
+    part = qsm.q8_gemv(x, q[:48].contiguous(), d[:48].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(full[:48].view(torch.int16), part.view(torch.int16))
+
+
 # ------------------------------------------------ int8-activation mode
 
 @pytest.mark.parametrize("K", [64, 2048, 8192])
