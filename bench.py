@@ -65,14 +65,14 @@ WORKLOADS = {
 
 
 def measured_traffic(workload):
-    """DRAM bytes per expert-FFN call from the committed ncu capture, or None
-    when the kernel sources changed since it was taken."""
+    """DRAM bytes per launch of the workload's dominant kernel (group) from the
+    committed ncu capture, or None when its sources changed since."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ffn_dram_traffic.json")
     if not os.path.exists(p):
         return None
-    ent = json.load(open(p)).get("prefill" if workload == "prefill" else "decode")
-    if not ent or workload not in ("decode", "prefill"):
+    ent = json.load(open(p)).get(workload)
+    if not ent:
         return None
     m = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_sparse_moe_gb300", "csrc")
@@ -193,7 +193,7 @@ def touched_bytes(layers, fwds, qtype):
     total = 0
     n_exp = 0
     for L, f in zip(layers, fwds):
-        ne = int((f.grouping.counts > 0).sum().item())
+        ne = int(torch.unique(f.topk_idx).numel())
         n_exp += ne
         T = f.T
         total += (ne + 1) * (gu + dn) + ROUTER_BYTES + 2 * T * L.H * 2
@@ -267,11 +267,17 @@ def run_ours(args, wl, rank, world):
         # an event-record node inside the captured graph (timing enabled)
         return torch.cuda.Event(enable_timing=True, external=True)
 
+    one_launch = fwds[0].decode_ws is not None and not args.chunk
     evs = [(graph_event(), graph_event()) for _ in range(nL)]
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
         s2 = torch.cuda.current_stream()
         for (a, b), f, x, L in zip(evs, fwds, xs, layers):
+            if one_launch:  # the whole layer is the one launch
+                a.record(s2)
+                f(x, stream=s2)
+                b.record(s2)
+                continue
             qsm.moe_route(x, L.w_router, L.k, L.logit_bias, f.renormalize, f.topk_idx,
                           f.topk_w, f.route_ws, f.dev_status, s2)
             qsm.moe_group_tokens(f.topk_idx, L.E, f.grouping.tile_rows,
@@ -291,8 +297,11 @@ def run_ours(args, wl, rank, world):
     step_bytes, n_exp = touched_bytes(layers, fwds, qtype)
     gu, dn = Q8_EXPERT_BYTES[qtype]
     ffn_bytes_per_layer = (n_exp / nL + 1) * (gu + dn) + 2 * T * 2048 * 2
+    if one_launch:
+        ffn_bytes_per_layer += ROUTER_BYTES
     hbm, _, peak_kind = peaks()
-    traffic = measured_traffic(args.workload)  # DRAM bytes per FFN call (ncu)
+    # DRAM bytes per FFN call (ncu), or per layer launch for the one-launch path
+    traffic = measured_traffic(args.workload + ("_one_launch" if one_launch else ""))
     if args.chunk:
         # the dominant launch group is the whole chunked layer call
         ffn_ms = ms / nL
@@ -348,10 +357,12 @@ def run_ours(args, wl, rank, world):
         "data": "synthetic (seeded; random-init weights of the layer shapes)",
         "config": {"workload": wl["desc"], "tokens_per_layer": T,
                    "layers": nL, "parallelism": f"replicas x{world}",
-                   "route_group": args.route_group if T <= 8 else "separate",
+                   "route_group": ("one launch per layer" if one_launch else
+                                   args.route_group if T <= 8 else "separate"),
                    "chunk_tokens": args.chunk or None,
                    "workspace_bytes_per_layer": int(
                        calls[0].ws.numel() if args.chunk else
+                       fwds[0].decode_ws.numel() if one_launch else
                        fwds[0].route_ws.numel() + fwds[0].ffn_ws.numel()),
                    "l2": "inputs larger than L2 (touched weights per step "
                          f"{step_bytes / 1e9:.2f} GB)"},
@@ -363,7 +374,9 @@ def run_ours(args, wl, rank, world):
             "frac": max(t_hbm, t_tc) / (ms / 1e3),
             "peak_gbs": hbm, "peak_tflops": tc_peak, "peak_kind": peak_kind},
         "roofline": ({
-            "kernel": "moe_ffn_forward (d1 gate_up+SwiGLU, d2 down+combine)",
+            "kernel": ("moe_decode_layer (router, selection, gate_up+SwiGLU, "
+                       "down+combine in one launch)" if one_launch else
+                       "moe_ffn_forward (d1 gate_up+SwiGLU, d2 down+combine)"),
             "bound": "hbm", "achieved": achieved, "peak": hbm,
             "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
             "bytes_per_launch": ffn_bytes_per_layer,

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define QSM_ABI_VERSION 2
+#define QSM_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define QSM_API __attribute__((visibility("default")))
@@ -276,6 +276,35 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
                                      uint16_t* y, float* y_f32, void* workspace,
                                      size_t workspace_bytes, int32_t* dev_status,
                                      cudaStream_t stream);
+
+/* The whole layer for a few tokens (1 <= T <= 8) in one launch: router,
+ * selection, gate_up + SwiGLU, down + combine, separated by two grid-wide
+ * barriers instead of three dependent launches [Perplexity page, "Keeping
+ * expert routing on the GPU", "Reducing intermediate and state traffic",
+ * "Overlapping independent GPU work"].  Results: topk_idx and topk_w
+ * bit-identical to moe_route's; y the layer output as moe_ffn_forward
+ * computes it (same arithmetic per product; the combine's fp32 additions in
+ * another order).
+ *   Arguments as for moe_layer_forward, without a chunk size.
+ *   Supported: Q8_0 or affine-4 (all four weight planes alike), H % 256 ==
+ *   0, H / 16 <= the device's SM count (one CTA per 16 output rows, all
+ *   resident for the barriers), I % 128 == 0 (Q8_0) or % 256 == 0
+ *   (affine-4), E <= 1024, k <= 32; all pointers 16-byte aligned except
+ *   topk_idx, topk_w, y, y_f32 and logit_bias (4 bytes).  Otherwise
+ *   QSM_ERR_UNSUPPORTED (moe_layer_forward serves every shape).
+ *   workspace  >= moe_decode_layer_workspace_bytes(L, T) bytes, zeros before
+ *              its first use.  Its first 8 bytes count barrier arrivals
+ *              across calls: the calls that share a workspace must have the
+ *              same H, and after a QSM_DEV_TIMEOUT it must be zeroed again.
+ * Every wait in the kernel is bounded: a barrier or copy that does not
+ * complete sets QSM_DEV_TIMEOUT and the call's results are invalid. */
+QSM_API size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T);
+QSM_API qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x, int32_t T,
+                                    const float* w_router, const float* logit_bias,
+                                    int32_t flags, int32_t* topk_idx, float* topk_w,
+                                    uint16_t* y, float* y_f32, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status,
+                                    cudaStream_t stream);
 
 /* moe_ffn_forward without a workspace argument, for callers that cannot
  * allocate device memory (code running inside another runtime's memory

@@ -110,6 +110,11 @@ def lib() -> ctypes.CDLL:
             L.moe_layer_forward.argtypes = [ctypes.POINTER(MoELayerC), P, i32, i32, P,
                                             P, i32, P, P, P, P, P, sz, P, P]
             L.moe_layer_forward.restype = st
+            L.moe_decode_layer_workspace_bytes.argtypes = [ctypes.POINTER(MoELayerC), i32]
+            L.moe_decode_layer_workspace_bytes.restype = sz
+            L.moe_decode_layer.argtypes = [ctypes.POINTER(MoELayerC), P, i32, P, P, i32,
+                                           P, P, P, P, P, sz, P, P]
+            L.moe_decode_layer.restype = st
             L.qsm_launch_count.argtypes = []
             L.qsm_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -386,6 +391,46 @@ def moe_layer_forward(layer: Layer, x: torch.Tensor, chunk: int, renormalize=Tru
     return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None), topk_idx, topk_w
 
 
+def decode_layer_workspace_bytes(layer: Layer, T: int) -> int:
+    """0 when the one-launch decode layer does not support the layer or T."""
+    return int(lib().moe_decode_layer_workspace_bytes(ctypes.byref(layer.c), T))
+
+
+def moe_decode_layer(layer: Layer, x: torch.Tensor, renormalize=True,
+                     bias_select_only=False, *, y=None, y_f32=None, topk_idx=None,
+                     topk_w=None, workspace=None, dev_status=None, stream=None,
+                     raise_unsupported=True):
+    """The layer for T <= 8 tokens in one launch (router, selection, gate_up,
+    down, combine).  The workspace must start zeroed and serve layers of one
+    hidden size.  Returns (y, y_f32 or None, topk_idx, topk_w), or None when
+    unsupported and raise_unsupported is False."""
+    T, H = x.shape
+    dev = x.device
+    k = layer.k
+    need = decode_layer_workspace_bytes(layer, T)
+    if need == 0:
+        if raise_unsupported:
+            raise QSMError("moe_decode_layer: unsupported layer or token count")
+        return None
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if y_f32 is True:
+        y_f32 = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if topk_idx is None:
+        topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    dev_status = _status(dev_status, dev)
+    _check(lib().moe_decode_layer(
+        ctypes.byref(layer.c), _p(_u16(x)), T, _p(layer.w_router), _p(layer.logit_bias),
+        route_flags(renormalize, bias_select_only), _p(topk_idx), _p(topk_w), _p(y),
+        _p(y_f32 if y_f32 is not False else None), _p(workspace), workspace.numel(),
+        _p(dev_status), _stream(stream)), "moe_decode_layer")
+    return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None), topk_idx, topk_w
+
+
 def force_path(mode: str | int) -> None:
     """Test hook: "auto", "decode" or "prefill"."""
     m = {"auto": 0, "decode": 1, "prefill": 2}.get(mode, mode)
@@ -413,15 +458,20 @@ def q8_gemv(x: torch.Tensor, q: torch.Tensor, d: torch.Tensor, y=None,
 # ---------------------------------------------------------- whole layer
 
 class MoEForward:
-    """Buffers of one MoE layer call for T tokens, and the call sequence
-    route -> group -> FFN on one stream (nothing is read back).  For T <= 8
-    the route and group steps use the fused moe_route_group launch."""
+    """Buffers of one MoE layer call for T tokens, and the call sequence on
+    one stream (nothing is read back).  When moe_decode_layer supports the
+    layer and T (T <= 8), one launch (one_launch=True); otherwise route ->
+    group -> FFN, with the fused moe_route_group launch for T <= 8."""
 
     def __init__(self, layer: Layer, T: int, device="cuda", renormalize=True,
-                 want_f32=False, fuse_route_group=True, *, bias_select_only=False):
+                 want_f32=False, fuse_route_group=True, *, bias_select_only=False,
+                 one_launch=True):
         self.layer, self.T = layer, T
         self.renormalize = route_flags(renormalize, bias_select_only)
         self.fuse_route_group = fuse_route_group
+        dl = decode_layer_workspace_bytes(layer, T) if one_launch else 0
+        self.decode_ws = (torch.zeros(dl, dtype=torch.uint8, device=device)
+                          if dl else None)
         k, E, H = layer.k, layer.E, layer.H
         i32 = dict(dtype=torch.int32, device=device)
         self.topk_idx = torch.empty((T, k), **i32)
@@ -438,6 +488,13 @@ class MoEForward:
 
     def __call__(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         L = self.layer
+        if self.decode_ws is not None:
+            _check(lib().moe_decode_layer(
+                ctypes.byref(L.c), _p(_u16(x)), self.T, _p(L.w_router),
+                _p(L.logit_bias), self.renormalize, _p(self.topk_idx), _p(self.topk_w),
+                _p(self.y), _p(self.y_f32), _p(self.decode_ws), self.decode_ws.numel(),
+                _p(self.dev_status), _stream(stream)), "moe_decode_layer")
+            return self.y
         fused = None
         if self.fuse_route_group and self.T <= 8:
             fused = moe_route_group(x, L.w_router, L.k, self.grouping,

@@ -1,0 +1,850 @@
+// The MoE layer for a few tokens (T <= 8) in one launch: router, expert
+// selection, gate_up + SwiGLU, down + routing weights + shared expert.
+//
+// "Optimizing on-device inference for Apple Silicon": section "Keeping
+// expert routing on the GPU" (the routing never leaves the device), section
+// "Reducing intermediate and state traffic" (the input projections with
+// their gated activation, then the output projection with its routing score
+// and the shared expert's result, summed per token) and section
+// "Overlapping independent GPU work"; the fused [gate; up] rows of "oMLX MoE
+// gate/up 融合优化", section "融合原理".  The dependent launches of the
+// decode path (router + grouping, gate_up, down) become three phases of one
+// launch, separated by two grid-wide barriers.  No grouping is needed: every
+// CTA derives its work from the selection itself.
+//
+//   A  CTA c computes the logits of its experts for the T tokens, with the
+//      arithmetic of moe_route (router rows fetched before the
+//      programmatic-launch wait), into the workspace.          grid barrier
+//   B  Every CTA selects each token's experts from the logits with the code
+//      of moe_route (ids and weights bit-identical to it), forms the sorted
+//      set U of selected experts and computes gate_up + SwiGLU for its
+//      tiles.  Tile tau = (slot, 8 intermediates): slot 0 is the shared
+//      expert, slot s >= 1 the s-th expert of U; a tile covers all T tokens
+//      (pairs that are not routed are computed and never read).  h goes to
+//      the workspace.                                           grid barrier
+//   C  CTA c computes rows 16c..16c+15 of y: for every slot, the down rows
+//      times the slot's h, times the token's weight for the slot's expert
+//      (the shared expert's gate, or 1; pairs with weight 0 are skipped),
+//      summed over the slots in a fixed order.
+//
+// Weights stream through a two-slot shared-memory ring filled by TMA from
+// one producer thread: B tiles (gate and up halves of 8 rows, each one copy
+// of the 3D row view with the 128-byte swizzle) and then C items (the down
+// tiles of up to m slots, 16 rows each).  As soon as the selection is known
+// the producer requests into L2 every weight byte its CTA will read, so HBM
+// streams the whole layer at once and the ring mostly reads L2.  The shared
+// expert's first tile and its down rows are requested before the wait.
+//
+// The grid barriers need all G = H / 16 CTAs resident at once: G is at most
+// the SM count and a launch's CTAs are all running once the launch lets its
+// dependents start (every CTA triggers).  Every wait is bounded; when one
+// runs out the kernel sets QSM_DEV_TIMEOUT, keeps its control flow (later
+// waits are short), lets its own copies land and returns.  The barrier
+// counter is a 64-bit ticket in the workspace: calls that share a workspace
+// must use the same H, and a workspace is zeroed again after a timeout.
+#include "gemv_core.cuh"
+#include "route_select.cuh"
+#include "tc_common.cuh"
+
+namespace qsm {
+namespace dlayer {
+
+using namespace gemv;
+
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;  // + the producer warp
+constexpr int kMaxS = 5;                  // ring slots (at most)
+constexpr int kMaxT = 8;
+constexpr int kMaxE = 1024;
+constexpr int kTPE = 128;                 // router threads per expert
+constexpr int kWPer = 4;                  // float4 of a router row per thread and batch
+constexpr float kHScale = 1.0f / 16.0f;
+constexpr float kHScaleInv = 16.0f;
+constexpr int kBarCons = 1;               // named barrier of the consumer warps
+constexpr uint32_t kShortWait = 1u << 10; // waits after a timeout
+
+struct Params {
+  CUtensorMap gu, gu_sh;  // gate_up codes, 3D row views, box {128, 8, hb/128}
+  CUtensorMap dn, dn_sh;  // down codes, box {128, 16, ib/128}
+  const uint8_t* gu_c;
+  const uint8_t* gush_c;
+  const uint8_t* dn_c;
+  const uint8_t* dnsh_c;
+  const __half* gu_s;     // scales (and affine-4 biases) per row
+  const __half* gu_b;
+  const __half* gush_s;
+  const __half* gush_b;
+  const __half* dn_s;
+  const __half* dn_b;
+  const __half* dnsh_s;
+  const __half* dnsh_b;
+  const uint16_t* x;      // [T, H] bf16
+  const float* wr;        // [E, H]
+  const float* bias;      // [E] or null
+  const float* sgate;     // [H] or null
+  int T, H, I, E, k, flags, G, epc;
+  int hb, hsb, ib, isb;   // code / scale bytes per gate_up row and per down row
+  int m;                  // down tiles per C item
+  int ns;                 // ring slots
+  int hall;               // all of h fits one shared-memory copy
+  int slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off, wm_off;
+  unsigned long long* gbar;
+  float* logits;          // [T, E]
+  __half* hbuf;           // [slots, T, I], h / 16
+  int32_t* topk_idx;
+  float* topk_w;
+  uint16_t* y;
+  float* y32;
+  int32_t* status;
+};
+
+// Barrier over n threads (a multiple of 32) of the CTA; the non-aligned form,
+// so lanes of one warp may reach it apart.
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One thread per CTA: count this CTA's arrival (release: the CTA's earlier
+// writes, ordered before by a CTA barrier, become visible first) and wait
+// until the counter reaches `target`.  False when the wait ran out.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* ctr,
+                                             unsigned long long target, uint32_t iters) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+  for (uint32_t i = 0; i < iters; ++i) {
+    if ((long long)(ld_acquire_u64(ctr) - target) >= 0) return true;
+    if (i > 64) __nanosleep(32);
+  }
+  return false;
+}
+
+// 8 bytes at byte b (a multiple of 8) of 128-byte line `line`, 128-byte swizzle.
+__device__ __forceinline__ uint2 lds_sw(const unsigned char* t, int line, int b) {
+  return *reinterpret_cast<const uint2*>(
+      t + line * 128 + ((((b >> 4) ^ (line & 7)) << 4) | (b & 15)));
+}
+
+// Ask L2 for `bytes` from `base`, one 128-byte line per thread and step.
+__device__ __forceinline__ void prefetch_lines(const void* base, uint32_t bytes, int t,
+                                               int nt) {
+  const char* b = static_cast<const char*>(base);
+  for (uint32_t off = (uint32_t)t * 128u; off < bytes; off += (uint32_t)nt * 128u)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(b + off));
+}
+
+// Raw A fragment of the 64-chunk ch of a tile whose rows g / g + 8 are lines
+// lg / lh (+ 128-byte chunk index x rows per chunk) of `codes`, with scales
+// (and biases) as fp16 rows of `spitch` bytes.
+template <int QT>
+__device__ __forceinline__ void load_tile_a(RawA& r, const unsigned char* codes_g,
+                                            const unsigned char* codes_h, int rows_per_chunk,
+                                            int g, int gh, const unsigned char* sc_g,
+                                            const unsigned char* sc_h, const unsigned char* bi_g,
+                                            const unsigned char* bi_h, int ch, int q) {
+  if (QT == QSM_Q8_0) {
+    const int c = ch >> 1, b = (ch & 1) * 64 + 8 * q;
+    const int lg = c * rows_per_chunk + g, lh = c * rows_per_chunk + gh;
+    r.g0 = lds_sw(codes_g, lg, b);
+    r.g1 = lds_sw(codes_g, lg, b + 32);
+    r.h0 = lds_sw(codes_h, lh, b);
+    r.h1 = lds_sw(codes_h, lh, b + 32);
+    r.sg = reinterpret_cast<const uint32_t*>(sc_g)[ch];
+    r.sh = reinterpret_cast<const uint32_t*>(sc_h)[ch];
+  } else {
+    const int c = ch >> 2, b = (ch & 3) * 32 + 8 * q;
+    r.g0 = lds_sw(codes_g, c * rows_per_chunk + g, b);
+    r.h0 = lds_sw(codes_h, c * rows_per_chunk + gh, b);
+    const uint16_t* sg = reinterpret_cast<const uint16_t*>(sc_g);
+    const uint16_t* sh = reinterpret_cast<const uint16_t*>(sc_h);
+    const uint16_t* bg = reinterpret_cast<const uint16_t*>(bi_g);
+    const uint16_t* bh = reinterpret_cast<const uint16_t*>(bi_h);
+    r.sg = (uint32_t)sg[ch] | ((uint32_t)bg[ch] << 16);
+    r.sh = (uint32_t)sh[ch] | ((uint32_t)bh[ch] << 16);
+  }
+}
+
+template <int QT, int kPer>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_layer_kernel(const __grid_constant__ Params p) {
+  extern __shared__ unsigned char dl_dyn[];
+  __shared__ __align__(8) uint64_t full[kMaxS], empty[kMaxS], hfull[2], hempty[2];
+  __shared__ __align__(8) uint64_t xbar, rdy, b2;
+  __shared__ float red[2][kCW][32][4];
+  __shared__ float rsum[2][kTPE / 32][kMaxT];
+  __shared__ int sel_e[kMaxT][32];
+  __shared__ float sel_w[kMaxT][32];
+  __shared__ unsigned bm[kMaxE / 32];
+  __shared__ float sgv[kMaxT];
+  __shared__ int s_nu;
+  __shared__ volatile int s_bad;  // a wait ran out: later waits are short
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int c = blockIdx.x;
+  const int n0 = 16 * c;
+  const int T = p.T, H = p.H, I = p.I, E = p.E, k = p.k, G = p.G;
+  const int tps = I / 8;  // B tiles per slot
+  const int ns = p.ns;
+  const uint32_t pad = (1024u - (smem_u32(dl_dyn) & 1023u)) & 1023u;
+  unsigned char* ring = dl_dyn + pad;
+  const uint16_t* xs = reinterpret_cast<const uint16_t*>(ring + p.xs_off);  // bf16 [T][H]
+  const float* sgs = reinterpret_cast<const float*>(ring + p.sg_off);       // [H]
+  const float* wrs = reinterpret_cast<const float*>(ring + p.wr_off);       // [epc][H]
+  unsigned char* hs = ring + p.hs_off;
+  int* ulist = reinterpret_cast<int*>(ring + p.ul_off);
+  float* wmat = reinterpret_cast<float*>(ring + p.wm_off);  // [(slots)][T]
+  constexpr int kBi = QT == QSM_Q8_0 ? 1 : 2;  // scale planes (scales, biases)
+
+  if (tid == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCW);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&hfull[b], 1);
+      mbar_init(&hempty[b], kCW);
+    }
+    mbar_init(&xbar, 1);
+    mbar_init(&rdy, 1);
+    mbar_init(&b2, 1);
+    s_bad = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < kMaxE / 32; i += kThreads) bm[i] = 0u;
+  __syncthreads();
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (mbar_wait_bounded(bar, parity, s_bad ? kShortWait : kWaitIters)) return;
+    s_bad = 1;
+    set_status(p.status, QSM_DEV_TIMEOUT);
+  };
+
+  // ================================================================ producer
+  if (warp == kCW) {
+    if (lane != 0) return;
+    int nu = 0, nB = 0, items = 0;
+    auto expert_of_slot = [&](int s) { return s == 0 ? 0 : ulist[s - 1]; };
+    // B tile tau -> ring buffer sb, barrier bar
+    auto issue_b = [&](int tau, unsigned char* sb, uint64_t* bar) {
+      const int s = tau / tps, i0 = 8 * (tau % tps);
+      const int e = expert_of_slot(s);
+      const int rg = (s == 0 ? 0 : e * 2 * I) + i0, ru = rg + I;
+      const CUtensorMap* map = s == 0 ? &p.gu_sh : &p.gu;
+      const __half* sc = s == 0 ? p.gush_s : p.gu_s;
+      const __half* bi = s == 0 ? p.gush_b : p.gu_b;
+      mbar_arrive_expect_tx(bar, 16u * p.hb + 16u * p.hsb * kBi);
+      tc::tma_load_3d(sb, map, 0, rg, 0, bar);
+      tc::tma_load_3d(sb + 8 * p.hb, map, 0, ru, 0, bar);
+      unsigned char* ss = sb + 16 * p.hb;
+      bulk_g2s(ss, sc + (size_t)rg * (p.hsb / 2), 8 * p.hsb, bar);
+      bulk_g2s(ss + 8 * p.hsb, sc + (size_t)ru * (p.hsb / 2), 8 * p.hsb, bar);
+      if (QT != QSM_Q8_0) {
+        bulk_g2s(ss + 16 * p.hsb, bi + (size_t)rg * (p.hsb / 2), 8 * p.hsb, bar);
+        bulk_g2s(ss + 24 * p.hsb, bi + (size_t)ru * (p.hsb / 2), 8 * p.hsb, bar);
+      }
+    };
+    auto down_row = [&](int s) { return (s == 0 ? 0 : expert_of_slot(s) * H) + n0; };
+    auto issue_c = [&](int it, unsigned char* sb, uint64_t* bar) {
+      const int cnt = min(p.m, nu + 1 - p.m * it);
+      mbar_arrive_expect_tx(bar, (uint32_t)cnt * (16u * p.ib + 16u * p.isb * kBi));
+      for (int j = 0; j < cnt; ++j) {
+        const int s = p.m * it + j, r = down_row(s);
+        tc::tma_load_3d(sb + j * 16 * p.ib, s == 0 ? &p.dn_sh : &p.dn, 0, r, 0, bar);
+        unsigned char* ss = sb + p.m * 16 * p.ib + j * 16 * p.isb;
+        bulk_g2s(ss, (s == 0 ? p.dnsh_s : p.dn_s) + (size_t)r * (p.isb / 2), 16 * p.isb, bar);
+        if (QT != QSM_Q8_0)
+          bulk_g2s(ss + p.m * 16 * p.isb, (s == 0 ? p.dnsh_b : p.dn_b) + (size_t)r * (p.isb / 2),
+                   16 * p.isb, bar);
+      }
+    };
+    auto issue_pos = [&](int pos) {
+      unsigned char* sb = ring + (pos % ns) * p.slot_bytes;
+      if (pos < nB) issue_b(c + pos * G, sb, &full[pos % ns]);
+      else issue_c(pos - nB, sb, &full[pos % ns]);
+    };
+    bool b2_seen = false;
+    // h of C item `it` (or, with hall, of every slot at once)
+    auto issue_h = [&](int it) {
+      if (!b2_seen) {
+        wait(&b2, 0);
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        b2_seen = true;
+      }
+      if (p.hall) {
+        const uint32_t bytes = (uint32_t)(nu + 1) * T * I * 2;
+        mbar_arrive_expect_tx(&hfull[0], bytes);
+        bulk_g2s(hs, p.hbuf, bytes, &hfull[0]);
+        return items;
+      }
+      if (it >= 2) wait(&hempty[it & 1], ((it >> 1) - 1) & 1);
+      const int cnt = min(p.m, nu + 1 - p.m * it);
+      const uint32_t bytes = (uint32_t)cnt * T * I * 2;
+      mbar_arrive_expect_tx(&hfull[it & 1], bytes);
+      bulk_g2s(hs + (it & 1) * p.hs_bytes, p.hbuf + (size_t)p.m * it * T * I, bytes,
+               &hfull[it & 1]);
+      return it + 1;
+    };
+
+    // before the wait: static weights only (the shared expert's tiles at the
+    // head of this CTA's sequence, its down rows, the shared-expert gate)
+    int pre = 0;
+    while (pre < ns && c + pre * G < tps) {
+      issue_b(c + pre * G, ring + pre * p.slot_bytes, &full[pre]);
+      ++pre;
+    }
+    bulk_prefetch_l2(p.dnsh_c + (size_t)n0 * p.ib, 16 * p.ib);
+    bulk_prefetch_l2(p.dnsh_s + (size_t)n0 * (p.isb / 2), 16 * p.isb);
+    {  // this CTA's router rows; counted in xbar's phase without arriving
+      const int ea = c * p.epc, ne = min(E, ea + p.epc) - ea;
+      if (ne > 0) {
+        mbar_expect_tx(&xbar, (uint32_t)ne * H * 4);
+        bulk_g2s(ring + p.wr_off, p.wr + (size_t)ea * H, ne * H * 4, &xbar);
+      }
+    }
+    if (p.sgate) {  // counted in xbar's phase without arriving
+      mbar_expect_tx(&xbar, (uint32_t)H * 4);
+      bulk_g2s(ring + p.sg_off, p.sgate, H * 4, &xbar);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    mbar_arrive_expect_tx(&xbar, (uint32_t)T * H * 2);
+    bulk_g2s(ring + p.xs_off, p.x, T * H * 2, &xbar);
+
+    wait(&rdy, 0);  // the selection: s_nu, ulist
+    nu = s_nu;
+    const int NT = (nu + 1) * tps;
+    nB = c < NT ? (NT - c + G - 1) / G : 0;
+    items = (nu + 1 + p.m - 1) / p.m;
+    const int total = nB + items;
+    int pos = pre;
+    for (; pos < total && pos < ns; ++pos) issue_pos(pos);
+    // the down tiles past the first fill -> L2 now (needed after barrier 2)
+    for (int it = ns > nB ? ns - nB : 0; it < items; ++it) {
+      const int cnt = min(p.m, nu + 1 - p.m * it);
+      for (int j = 0; j < cnt; ++j) {
+        const int s = p.m * it + j, r = down_row(s);
+        bulk_prefetch_l2((s == 0 ? p.dnsh_c : p.dn_c) + (size_t)r * p.ib, 16 * p.ib);
+        bulk_prefetch_l2((s == 0 ? p.dnsh_s : p.dn_s) + (size_t)r * (p.isb / 2), 16 * p.isb);
+        if (QT != QSM_Q8_0)
+          bulk_prefetch_l2((s == 0 ? p.dnsh_b : p.dn_b) + (size_t)r * (p.isb / 2),
+                           16 * p.isb);
+      }
+    }
+    int hi = 0;  // next C item whose h is copied
+    for (; pos < total; ++pos) {
+      // the slot's previous position must be consumed; if it was a C item,
+      // its h has to be on its way first
+      const int prev = pos - ns;
+      if (prev >= nB)
+        while (hi <= prev - nB) hi = issue_h(hi);
+      wait(&empty[pos % ns], ((pos / ns) - 1) & 1);
+      issue_pos(pos);
+    }
+    while (hi < items) hi = issue_h(hi);
+    // normally every copy has been consumed; after a timeout, let the last
+    // copy of each buffer land before the CTA's shared memory goes away
+    if (s_bad) {
+      for (int s = 0; s < ns && s < total; ++s) {
+        const int last = s + ((total - 1 - s) / ns) * ns;
+        mbar_wait_bounded(&full[s], (last / ns) & 1, kWaitIters);
+      }
+      const int nhb = p.hall ? 1 : 2;
+      for (int b = 0; b < nhb && b < items; ++b) {
+        const int last = p.hall ? 0 : b + ((items - 1 - b) / 2) * 2;
+        mbar_wait_bounded(&hfull[b], (last >> 1) & 1, kWaitIters);
+      }
+    }
+    return;
+  }
+
+  // ================================================================ consumers
+  // ---- A: logits of experts [ea, eb) (pairs of experts, 128 threads each)
+  const int sub = tid / kTPE, st = tid % kTPE;
+  const int ea = c * p.epc, eb = min(E, ea + p.epc);
+  const int H4 = H / 4;
+  pdl_wait();
+  pdl_launch_dependents();
+  // barrier base: every earlier call on this workspace has completed, so the
+  // counter holds a multiple of G plus arrivals of this call
+  unsigned long long gbase = 0;
+  if (tid == 0) {
+    const unsigned long long v = ld_acquire_u64(p.gbar);
+    gbase = v - v % (unsigned long long)G;
+  }
+  wait(&xbar, 0);  // router rows, x (and the shared-expert gate vector)
+  for (int e0 = ea; e0 < eb; e0 += 2) {
+    const int e = e0 + sub;
+    const bool mine = e < eb;
+    const float4* wrow = reinterpret_cast<const float4*>(wrs + (size_t)(mine ? e - ea : 0) * H);
+    float acc[kMaxT];
+#pragma unroll
+    for (int i = 0; i < kMaxT; ++i) acc[i] = 0.f;
+    for (int hb = 0; hb < H4; hb += kWPer * kTPE) {
+      float4 wv[kWPer];
+#pragma unroll
+      for (int i = 0; i < kWPer; ++i) {
+        const int h4 = hb + st + i * kTPE;
+        wv[i] = (mine && h4 < H4) ? wrow[h4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int tt = 0; tt < kMaxT; ++tt) {
+        if (tt < T) {
+          const uint2* xr = reinterpret_cast<const uint2*>(xs + (size_t)tt * H);
+          uint2 xv[kWPer];
+#pragma unroll
+          for (int i = 0; i < kWPer; ++i) {
+            const int h4 = hb + st + i * kTPE;
+            xv[i] = h4 < H4 ? xr[h4] : make_uint2(0u, 0u);
+          }
+          float a = acc[tt];
+#pragma unroll
+          for (int i = 0; i < kWPer; ++i) {
+            a = fmaf(wv[i].x, bf16_lo(xv[i].x), a);
+            a = fmaf(wv[i].y, bf16_hi(xv[i].x), a);
+            a = fmaf(wv[i].z, bf16_lo(xv[i].y), a);
+            a = fmaf(wv[i].w, bf16_hi(xv[i].y), a);
+          }
+          acc[tt] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxT; ++i) {
+      if (i < T) {
+        const float s2 = warp_sum(acc[i]);
+        if (lane == 0) rsum[sub][st / 32][i] = s2;
+      }
+    }
+    named_bar(kBarCons, kCW * 32);
+    if (tid < 2 * kMaxT) {
+      const int s2 = tid / kMaxT, i = tid % kMaxT;
+      const int e2 = e0 + s2;
+      if (e2 < eb && i < T) {
+        float v = 0.f;
+#pragma unroll
+        for (int wq = 0; wq < kTPE / 32; ++wq) v += rsum[s2][wq][i];
+        p.logits[(size_t)i * E + e2] = v;
+      }
+    }
+    named_bar(kBarCons, kCW * 32);
+  }
+  // the shared expert's gate sigmoid(x . shared_gate), one warp per token
+  if (p.sgate) {
+    for (int t = warp; t < T; t += kCW) {
+      const uint16_t* xr = xs + (size_t)t * H;
+      float z = 0.f;
+      for (int h = lane; h < H; h += 32)
+        z = fmaf(__uint_as_float((uint32_t)xr[h] << 16), sgs[h], z);
+      z = warp_sum(z);
+      if (lane == 0) sgv[t] = 1.0f / (1.0f + __expf(-z));
+    }
+  }
+
+  // ---- grid barrier 1: all logits written
+  named_bar(kBarCons, kCW * 32);
+  if (tid == 0 && !grid_barrier(p.gbar, gbase + G, s_bad ? kShortWait : kWaitIters)) {
+    s_bad = 1;
+    set_status(p.status, QSM_DEV_TIMEOUT);
+  }
+  __syncwarp();
+  named_bar(kBarCons, kCW * 32);
+
+  // ---- B: selection (one warp per token), the set U, weights per slot
+  if (warp < T) {
+    int my_e;
+    float my_l, my_w;
+    route_select_warp<kPer>(p.logits + (size_t)warp * E, p.bias, E, k, p.flags, p.status,
+                            my_e, my_l, my_w);
+    if (lane < k) {
+      sel_e[warp][lane] = my_e;
+      sel_w[warp][lane] = my_w;
+      if (c == 0) {
+        p.topk_idx[(size_t)warp * k + lane] = my_e;
+        p.topk_w[(size_t)warp * k + lane] = my_w;
+      }
+    }
+  }
+  named_bar(kBarCons, kCW * 32);
+  if (tid < T * k) {
+    const int e = sel_e[tid / k][tid % k];
+    atomicOr(&bm[e >> 5], 1u << (e & 31));
+  }
+  named_bar(kBarCons, kCW * 32);
+  if (warp == 0) {  // sorted distinct ids: prefix popcounts of the bitmap
+    const unsigned word = lane < (E + 31) / 32 ? bm[lane] : 0u;
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int pos = incl - cnt;
+    for (unsigned w = word; w; w &= w - 1) ulist[pos++] = 32 * lane + (__ffs(w) - 1);
+    if (lane == 31) s_nu = incl;
+  }
+  named_bar(kBarCons, kCW * 32);
+  const int nu = s_nu;
+  for (int i = tid; i < (nu + 1) * T; i += kCW * 32) {
+    const int s = i / T, t = i - s * T;
+    float w = 0.f;
+    if (s == 0) {
+      w = p.sgate ? sgv[t] : 1.f;
+    } else {
+      const int e = ulist[s - 1];
+      for (int j = 0; j < k; ++j)
+        if (sel_e[t][j] == e) w = sel_w[t][j];
+    }
+    wmat[i] = w;
+  }
+  named_bar(kBarCons, kCW * 32);
+  if (tid == 0) tc::mbar_arrive(&rdy);
+
+  const int NT = (nu + 1) * tps;
+  const int nB = c < NT ? (NT - c + G - 1) / G : 0;
+
+  // ---- B: gate_up + SwiGLU tiles
+  const int nch = H / 64;
+  bool range_bad = false;
+  for (int j = 0; j < nB; ++j) {
+    const int sl = j % ns;
+    wait(&full[sl], (j / ns) & 1);
+    const unsigned char* sb = ring + sl * p.slot_bytes;
+    const unsigned char* ss = sb + 16 * p.hb;  // gate scales, up scales (, biases)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ch = warp; ch < nch; ch += kCW) {
+      RawA r;
+      load_tile_a<QT>(r, sb, sb + 8 * p.hb, 8, g, g, ss + g * p.hsb,
+                      ss + 8 * p.hsb + g * p.hsb, ss + 16 * p.hsb + g * p.hsb,
+                      ss + 24 * p.hsb + g * p.hsb, ch, q);
+      uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
+      if (g < T) {
+        const uint16_t* xr = xs + (size_t)g * H + 64 * ch;
+        X0 = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(xr + b_off0<QT>(q)));
+        X1 = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(xr + b_off1<QT>(q)));
+      }
+      chunk_mma<QT>(acc, r, X0, X1);
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[sl]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[j & 1][warp][lane][i] = acc[i];
+    named_bar(kBarCons, kCW * 32);
+    if (warp == 0) {
+      float a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) s += red[j & 1][w][lane][i];
+        a[i] = s;
+      }
+      const int tau = c + j * G, s = tau / tps, i0 = 8 * (tau % tps);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int t = 2 * q + cc;
+        if (t < T) {
+          const float h = silu(a[cc]) * a[2 + cc] * kHScale;
+          if (!(fabsf(h) <= 65504.f)) range_bad = true;
+          p.hbuf[((size_t)s * T + t) * I + i0 + g] = __float2half_rn(h);
+        }
+      }
+    }
+  }
+  if (range_bad) set_status(p.status, QSM_DEV_FP16_RANGE);
+
+  // ---- grid barrier 2: all h written
+  named_bar(kBarCons, kCW * 32);
+  if (tid == 0) {
+    if (!grid_barrier(p.gbar, gbase + 2ull * G, s_bad ? kShortWait : kWaitIters)) {
+      s_bad = 1;
+      set_status(p.status, QSM_DEV_TIMEOUT);
+    }
+    tc::mbar_arrive(&b2);  // the producer may copy h
+  }
+  __syncwarp();  // warp 0 converges before its MMAs
+
+  // ---- C: down rows n0..n0+15 of every slot, weighted per token
+  const int items = (nu + 1 + p.m - 1) / p.m;
+  const int ich = I / 64;
+  float yp[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int it = 0; it < items; ++it) {
+    const int pos = nB + it, sl = pos % ns;
+    wait(&full[sl], (pos / ns) & 1);
+    if (!p.hall) wait(&hfull[it & 1], (it >> 1) & 1);
+    else if (it == 0) wait(&hfull[0], 0);
+    const unsigned char* sb = ring + sl * p.slot_bytes;
+    // h rows of the item's first slot
+    const __half* hb = reinterpret_cast<const __half*>(
+        p.hall ? hs + (size_t)p.m * it * T * I * 2 : hs + (it & 1) * p.hs_bytes);
+    // the item's (slot, chunk) pairs, flattened and cut evenly over the warps
+    const int cnt = min(p.m, nu + 1 - p.m * it);
+    const int tot = cnt * ich, per = (tot + kCW - 1) / kCW;
+    const int lo = min(tot, warp * per), hi = min(tot, lo + per);
+    for (int j = lo / ich; j * ich < hi; ++j) {
+      const int s = p.m * it + j;
+      const int c0 = max(lo, j * ich) - j * ich, c1 = min(hi, (j + 1) * ich) - j * ich;
+      const unsigned char* cd = sb + j * 16 * p.ib;
+      const unsigned char* ss = sb + p.m * 16 * p.ib + j * 16 * p.isb;
+      const unsigned char* bs = ss + p.m * 16 * p.isb;
+      const __half* hr = hb + ((size_t)j * T + min(g, T - 1)) * I;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int ch = c0; ch < c1; ++ch) {
+        RawA r;
+        load_tile_a<QT>(r, cd, cd, 16, g, g + 8, ss + g * p.isb, ss + (g + 8) * p.isb,
+                        bs + g * p.isb, bs + (g + 8) * p.isb, ch, q);
+        uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
+        if (g < T) {
+          X0 = *reinterpret_cast<const uint4*>(hr + 64 * ch + b_off0<QT>(q));
+          X1 = *reinterpret_cast<const uint4*>(hr + 64 * ch + b_off1<QT>(q));
+        }
+        chunk_mma<QT>(acc, r, X0, X1);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int t = 2 * q + cc;
+        const float w = t < T ? wmat[s * T + t] : 0.f;
+        if (w != 0.f) {
+          yp[cc] = fmaf(w * kHScaleInv, acc[cc], yp[cc]);
+          yp[2 + cc] = fmaf(w * kHScaleInv, acc[2 + cc], yp[2 + cc]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      tc::mbar_arrive(&empty[sl]);
+      if (!p.hall) tc::mbar_arrive(&hempty[it & 1]);
+    }
+  }
+  // per-warp partials, summed in warp order
+#pragma unroll
+  for (int i = 0; i < 4; ++i) red[0][warp][lane][i] = yp[i];
+  named_bar(kBarCons, kCW * 32);
+  if (tid < 16 * T) {
+    const int r = tid & 15, t = tid >> 4;
+    const int ln = 4 * (r & 7) + (t >> 1), ii = (r >= 8 ? 2 : 0) + (t & 1);
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) s += red[0][w][ln][ii];
+    const size_t o = (size_t)t * H + n0 + r;
+    p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+    if (p.y32) p.y32[o] = s;
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+inline size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int sm_count_dl() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return n;
+}
+
+// dynamic shared memory per CTA: the per-block maximum minus the static part
+constexpr size_t kSmemBudget = 227 * 1024 - 12 * 1024;
+
+struct Geo {
+  int hb, hsb, ib, isb, m, ns, hall, slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off,
+      wm_off;
+  size_t smem;
+  int numax;
+};
+
+bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
+  const int qt = L->gate_up.qtype;
+  const int H = L->H, I = L->I, E = L->E, k = L->k;
+  if (T < 1 || T > kMaxT || E < 1 || E > kMaxE || k < 1 || k > 32 || k > E) return false;
+  if (qt != QSM_Q8_0 && qt != QSM_AFFINE4_G64) return false;
+  if (L->down.qtype != qt || L->shared_gate_up.qtype != qt || L->shared_down.qtype != qt)
+    return false;
+  if (H % 256 || I % (qt == QSM_Q8_0 ? 128 : 256)) return false;
+  if (H / 16 > sm_count_dl() || H > 16384 || I > 16384) return false;
+  const int bi = qt == QSM_Q8_0 ? 1 : 2;
+  Geo g;
+  g.hb = qt == QSM_Q8_0 ? H : H / 2;
+  g.hsb = (qt == QSM_Q8_0 ? H / 32 : H / 64) * 2;
+  g.ib = qt == QSM_Q8_0 ? I : I / 2;
+  g.isb = (qt == QSM_Q8_0 ? I / 32 : I / 64) * 2;
+  const size_t btile = 16 * (size_t)g.hb + 16 * (size_t)g.hsb * bi;
+  const size_t dtile = 16 * (size_t)g.ib + 16 * (size_t)g.isb * bi;
+  g.slot_bytes = (int)up(btile > dtile ? btile : dtile, 1024);
+  g.numax = T * k < E ? T * k : E;
+  const int G = H / 16, epc = (E + G - 1) / G;
+  // the deepest ring (then the largest C items) that fits
+  const size_t hall_bytes = (size_t)(g.numax + 1) * T * I * 2;
+  const int mmax = (int)(g.slot_bytes / dtile) > 8 ? 8 : (int)(g.slot_bytes / dtile);
+  bool fit = false;
+  for (g.ns = kMaxS; g.ns >= 2 && !fit; --g.ns) {
+    for (g.m = mmax; g.m >= 1; --g.m) {
+      size_t off = (size_t)g.ns * g.slot_bytes;
+      g.xs_off = (int)off;
+      off = up(off + (size_t)T * H * 2, 128);
+      g.sg_off = (int)off;
+      off = up(off + (L->shared_gate ? (size_t)H * 4 : 0), 128);
+      // the router rows (phase A) and the h copies (phase C) share a region
+      g.wr_off = g.hs_off = (int)off;
+      g.hs_bytes = (int)((size_t)g.m * T * I * 2);
+      g.hall = hall_bytes <= 32 * 1024 ? 1 : 0;
+      const size_t wr = (size_t)epc * H * 4, hsz = g.hall ? hall_bytes : 2 * (size_t)g.hs_bytes;
+      off = up(off + (wr > hsz ? wr : hsz), 128);
+      g.ul_off = (int)off;
+      off = up(off + (size_t)g.numax * 4, 16);
+      g.wm_off = (int)off;
+      off = up(off + (size_t)(g.numax + 1) * T * 4, 16);
+      g.smem = 1024 + off;
+      if (g.smem <= kSmemBudget) {
+        fit = true;
+        break;
+      }
+    }
+  }
+  if (!fit) return false;
+  ++g.ns;  // undo the loop's last decrement
+  *o = g;
+  return true;
+}
+
+struct WsLayout {
+  size_t logits, hbuf, total;
+};
+
+WsLayout ws_layout(const qsm_moe_layer* L, int T, const Geo& g) {
+  WsLayout w;
+  w.logits = 256;
+  w.hbuf = w.logits + up((size_t)T * L->E * 4, 256);
+  w.total = w.hbuf + up((size_t)(g.numax + 1) * T * L->I * 2, 256);
+  return w;
+}
+
+template <int QT, int kPer>
+cudaError_t launch(const Params& prm, size_t smem, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<QT, kPer>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(decode_layer_kernel<QT, kPer>, dim3(prm.G), dim3(kThreads), smem, stream,
+                    prm);
+}
+
+}  // namespace dlayer
+}  // namespace qsm
+
+extern "C" size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T) {
+  qsm::dlayer::Geo g;
+  if (!L || !qsm::dlayer::geo_of(L, T, &g)) return 0;
+  return qsm::dlayer::ws_layout(L, T, g).total;
+}
+
+extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x, int32_t T,
+                                       const float* w_router, const float* logit_bias,
+                                       int32_t flags, int32_t* topk_idx, float* topk_w,
+                                       uint16_t* y, float* y_f32, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status,
+                                       cudaStream_t stream) {
+  using namespace qsm;
+  using namespace qsm::dlayer;
+  if (!L || T < 0 || (flags & ~(QSM_ROUTE_RENORMALIZE | QSM_ROUTE_BIAS_SELECT_ONLY)))
+    return QSM_ERR_INVALID_ARGUMENT;
+  if (T == 0) return QSM_OK;
+  if (!x || !w_router || !topk_idx || !topk_w || !y || !workspace || !dev_status)
+    return QSM_ERR_INVALID_ARGUMENT;
+  Geo g;
+  if (!geo_of(L, T, &g)) return QSM_ERR_UNSUPPORTED;
+  const WsLayout wl = ws_layout(L, T, g);
+  if (workspace_bytes < wl.total) return QSM_ERR_WORKSPACE_TOO_SMALL;
+  const qsm_qweights *gu = &L->gate_up, *gs = &L->shared_gate_up, *dn = &L->down,
+                     *ds = &L->shared_down;
+  const bool a4 = gu->qtype == QSM_AFFINE4_G64;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace) || !aligned4(topk_idx) ||
+      !aligned4(topk_w) || !aligned4(y) || (y_f32 && !aligned4(y_f32)) ||
+      (logit_bias && !aligned4(logit_bias)) || (L->shared_gate && !aligned16(L->shared_gate)))
+    return QSM_ERR_INVALID_ARGUMENT;
+  for (const qsm_qweights* w : {gu, gs, dn, ds}) {
+    if (!w->codes || !w->scales || !aligned16(w->codes) || !aligned16(w->scales) ||
+        (a4 && (!w->biases || !aligned16(w->biases))))
+      return QSM_ERR_INVALID_ARGUMENT;
+  }
+  if (gu->experts != L->E || gu->rows != 2 * L->I || gu->cols != L->H || dn->experts != L->E ||
+      dn->rows != L->H || dn->cols != L->I || gs->rows != 2 * L->I || gs->cols != L->H ||
+      ds->rows != L->H || ds->cols != L->I)
+    return QSM_ERR_INVALID_ARGUMENT;
+  Params prm;
+  const int H = L->H, I = L->I, E = L->E;
+  bool ok = tc::make_map_rows3d(&prm.gu, gu->codes, (uint64_t)E * 2 * I, g.hb, 8, g.hb / 128) &&
+            tc::make_map_rows3d(&prm.gu_sh, gs->codes, (uint64_t)2 * I, g.hb, 8, g.hb / 128) &&
+            tc::make_map_rows3d(&prm.dn, dn->codes, (uint64_t)E * H, g.ib, 16, g.ib / 128) &&
+            tc::make_map_rows3d(&prm.dn_sh, ds->codes, (uint64_t)H, g.ib, 16, g.ib / 128);
+  if (!ok) return QSM_ERR_UNSUPPORTED;
+  prm.gu_c = static_cast<const uint8_t*>(gu->codes);
+  prm.gush_c = static_cast<const uint8_t*>(gs->codes);
+  prm.dn_c = static_cast<const uint8_t*>(dn->codes);
+  prm.dnsh_c = static_cast<const uint8_t*>(ds->codes);
+  prm.gu_s = reinterpret_cast<const __half*>(gu->scales);
+  prm.gu_b = reinterpret_cast<const __half*>(gu->biases);
+  prm.gush_s = reinterpret_cast<const __half*>(gs->scales);
+  prm.gush_b = reinterpret_cast<const __half*>(gs->biases);
+  prm.dn_s = reinterpret_cast<const __half*>(dn->scales);
+  prm.dn_b = reinterpret_cast<const __half*>(dn->biases);
+  prm.dnsh_s = reinterpret_cast<const __half*>(ds->scales);
+  prm.dnsh_b = reinterpret_cast<const __half*>(ds->biases);
+  prm.x = x;
+  prm.wr = w_router;
+  prm.bias = logit_bias;
+  prm.sgate = L->shared_gate;
+  prm.T = T;
+  prm.H = H;
+  prm.I = I;
+  prm.E = E;
+  prm.k = L->k;
+  prm.flags = flags;
+  prm.G = H / 16;
+  prm.epc = (E + prm.G - 1) / prm.G;
+  prm.hb = g.hb;
+  prm.hsb = g.hsb;
+  prm.ib = g.ib;
+  prm.isb = g.isb;
+  prm.m = g.m;
+  prm.ns = g.ns;
+  prm.hall = g.hall;
+  prm.slot_bytes = g.slot_bytes;
+  prm.xs_off = g.xs_off;
+  prm.sg_off = g.sg_off;
+  prm.wr_off = g.wr_off;
+  prm.hs_off = g.hs_off;
+  prm.hs_bytes = g.hs_bytes;
+  prm.ul_off = g.ul_off;
+  prm.wm_off = g.wm_off;
+  char* ws = static_cast<char*>(workspace);
+  prm.gbar = reinterpret_cast<unsigned long long*>(ws);
+  prm.logits = reinterpret_cast<float*>(ws + wl.logits);
+  prm.hbuf = reinterpret_cast<__half*>(ws + wl.hbuf);
+  prm.topk_idx = topk_idx;
+  prm.topk_w = topk_w;
+  prm.y = y;
+  prm.y32 = y_f32;
+  prm.status = dev_status;
+  cudaError_t err;
+  if (E <= 256)
+    err = a4 ? launch<QSM_AFFINE4_G64, 8>(prm, g.smem, stream)
+             : launch<QSM_Q8_0, 8>(prm, g.smem, stream);
+  else
+    err = a4 ? launch<QSM_AFFINE4_G64, 32>(prm, g.smem, stream)
+             : launch<QSM_Q8_0, 32>(prm, g.smem, stream);
+  return err == cudaSuccess ? QSM_OK : QSM_ERR_CUDA;
+}

@@ -117,7 +117,7 @@ q8_quantize_x_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
 // D(16x8, s32) = A(16x32, s8, row) * B(32x8, s8, col).
 __device__ __forceinline__ void mma_16832_s8(int (&d)[4], const uint32_t (&a)[4],
                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
       : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])

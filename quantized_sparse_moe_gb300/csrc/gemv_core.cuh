@@ -112,26 +112,31 @@ template <int QT>
 __device__ __forceinline__ void chunk_mma(float (&acc)[4], const RawA& r,
                                           const uint4& X0, const uint4& X1) {
   if (QT == QSM_Q8_0) {
+    // one fp32 partial per 32-block (its two MMAs accumulate in order); the
+    // two blocks' MMA chains are interleaved so their latencies overlap
+    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint2 wg = blk ? r.g1 : r.g0, wh = blk ? r.h1 : r.h0;
+    for (int jj = 0; jj < 2; ++jj) {
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
+      for (int blk = 0; blk < 2; ++blk) {
+        const uint2 wg = blk ? r.g1 : r.g0, wh = blk ? r.h1 : r.h0;
         uint32_t a[4], b0, b1;
         s8x4_to_f16x2x2(jj ? wg.y : wg.x, a[0], a[2]);
         s8x4_to_f16x2x2(jj ? wh.y : wh.x, a[1], a[3]);
         b_frag<QT>(X0, X1, 2 * blk + jj, b0, b1);
-        mma_16816(d, a, b0, b1);
+        mma_16816(d[blk], a, b0, b1);
       }
+    }
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
       const float sg = __half2float(__ushort_as_half(
           (unsigned short)(blk ? (r.sg >> 16) : (r.sg & 0xffff))));
       const float sh = __half2float(__ushort_as_half(
           (unsigned short)(blk ? (r.sh >> 16) : (r.sh & 0xffff))));
-      acc[0] = fmaf(sg, d[0], acc[0]);
-      acc[1] = fmaf(sg, d[1], acc[1]);
-      acc[2] = fmaf(sh, d[2], acc[2]);
-      acc[3] = fmaf(sh, d[3], acc[3]);
+      acc[0] = fmaf(sg, d[blk][0], acc[0]);
+      acc[1] = fmaf(sg, d[blk][1], acc[1]);
+      acc[2] = fmaf(sh, d[blk][2], acc[2]);
+      acc[3] = fmaf(sh, d[blk][3], acc[3]);
     }
   } else {
 #pragma unroll

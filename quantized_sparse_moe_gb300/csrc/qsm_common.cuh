@@ -124,43 +124,89 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Top k of the values a warp holds, v[i] at index lane + 32 i (i < KPER,
 // indices >= E ignored), in descending order with ties to the lower index.
-// Lane j < k receives the j-th value and its index.  Each round takes every
-// lane's best untaken candidate, packed as (order-preserving key << 32 |
-// ~index), and a butterfly of 64-bit maxima over the warp.  Non-finite
-// values must be mapped to -inf by the caller.
+// Lane j < k receives the j-th value and its index.  Non-finite values must
+// be mapped to -inf by the caller.  Candidates are compared as (order-
+// preserving key, inverted index) pairs, a strict total order.
+//
+// KPER == 8: each lane sorts its 8 candidates once (a 19-exchange network),
+// then every round takes the best head over the warp with two warp
+// reductions (the largest key, then among the lanes holding it the largest
+// inverted index) and the winning lane drops its head.  Other KPER: each
+// round takes every lane's best untaken candidate and a butterfly of 64-bit
+// maxima.  Both give the same selection.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t kv) {
+  return __uint_as_float((kv & 0x80000000u) ? (kv & 0x7fffffffu) : ~kv);
+}
+__device__ __forceinline__ void cas_desc(unsigned long long& a, unsigned long long& b) {
+  const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
 template <int KPER>
 __device__ __forceinline__ void warp_topk(const float (&v)[KPER], int E, int k,
                                           float& out_v, int& out_e) {
   const int lane = threadIdx.x & 31;
-  uint32_t key[KPER];
-#pragma unroll
-  for (int i = 0; i < KPER; ++i) {
-    const uint32_t u = __float_as_uint(v[i]);
-    key[i] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  }
-  uint32_t taken = 0;
   out_v = 0.f;
   out_e = 0;
-  for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
+  if constexpr (KPER == 8) {
+    unsigned long long c[8];  // (key << 32 | ~index), 0 = no candidate
 #pragma unroll
-    for (int i = 0; i < KPER; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      const unsigned long long c =
-          ((unsigned long long)key[i] << 32) | (unsigned long long)(~(uint32_t)e);
-      if (e < E && !((taken >> i) & 1u) && c > best) best = c;
+      c[i] = e < E ? ((unsigned long long)order_key(v[i]) << 32) | (uint32_t)~e : 0ull;
     }
+    // Batcher's odd-even merge sort of 8, descending
+    cas_desc(c[0], c[1]); cas_desc(c[2], c[3]); cas_desc(c[4], c[5]); cas_desc(c[6], c[7]);
+    cas_desc(c[0], c[2]); cas_desc(c[1], c[3]); cas_desc(c[4], c[6]); cas_desc(c[5], c[7]);
+    cas_desc(c[1], c[2]); cas_desc(c[5], c[6]);
+    cas_desc(c[0], c[4]); cas_desc(c[1], c[5]); cas_desc(c[2], c[6]); cas_desc(c[3], c[7]);
+    cas_desc(c[2], c[4]); cas_desc(c[3], c[5]);
+    cas_desc(c[1], c[2]); cas_desc(c[3], c[4]); cas_desc(c[5], c[6]);
+    for (int j = 0; j < k; ++j) {
+      const uint32_t hk = (uint32_t)(c[0] >> 32), hi = (uint32_t)c[0];
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+      const uint32_t mi = __reduce_max_sync(0xffffffffu, hk == mk ? hi : 0u);
+      if (hk == mk && hi == mi) {  // this lane held the winner: drop it
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
+        for (int i = 0; i < 7; ++i) c[i] = c[i + 1];
+        c[7] = 0ull;
+      }
+      if (lane == j) {
+        out_v = key_value(mk);
+        out_e = (int)~mi;
+      }
     }
-    const uint32_t e = ~(uint32_t)best;
-    const uint32_t kv = (uint32_t)(best >> 32);
-    if ((e & 31u) == (uint32_t)lane) taken |= 1u << (e >> 5);
-    if (lane == j) {
-      out_v = __uint_as_float((kv & 0x80000000u) ? (kv & 0x7fffffffu) : ~kv);
-      out_e = (int)e;
+  } else {
+    uint32_t key[KPER];
+#pragma unroll
+    for (int i = 0; i < KPER; ++i) key[i] = order_key(v[i]);
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int i = 0; i < KPER; ++i) {
+        const int e = lane + 32 * i;
+        const unsigned long long c =
+            ((unsigned long long)key[i] << 32) | (unsigned long long)(~(uint32_t)e);
+        if (e < E && !((taken >> i) & 1u) && c > best) best = c;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      const uint32_t e = ~(uint32_t)best;
+      const uint32_t kv = (uint32_t)(best >> 32);
+      if ((e & 31u) == (uint32_t)lane) taken |= 1u << (e >> 5);
+      if (lane == j) {
+        out_v = key_value(kv);
+        out_e = (int)e;
+      }
     }
   }
 }
@@ -195,10 +241,12 @@ __device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo,
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col).  Not volatile: a
+// pure function of its operands, so the compiler may interleave independent
+// MMAs (their latency is what bounds a warp's tile loop).
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
                                           uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -246,7 +294,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                "r"(count)
                : "memory");
 }
-// Make an initialised mbarrier visible to the async (TMA) proxy.
 // Distributed shared memory: the address of `p` (this CTA's shared memory)
 // in the CTA of cluster rank `rank`, and a 32-bit store there.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
@@ -264,6 +311,7 @@ __device__ __forceinline__ void cluster_sync_all() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Make an initialised mbarrier visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

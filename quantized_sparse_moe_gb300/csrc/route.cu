@@ -20,7 +20,7 @@
 // the T*k assignments ("Keeping expert routing on the GPU": histogram,
 // prefix scan, stable scatter, block map) from the ids it holds in shared
 // memory, so routing plus grouping is one launch for decode batches.
-#include "qsm_common.cuh"
+#include "route_select.cuh"
 
 namespace qsm {
 namespace {
@@ -218,65 +218,17 @@ route_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w,
   if (!is_last) return;
 
   const int warp = tid / 32;
-  const bool renorm = (renormalize & QSM_ROUTE_RENORMALIZE) != 0;
-  const bool sel_only = (renormalize & QSM_ROUTE_BIAS_SELECT_ONLY) != 0 && bias;
   if (warp < nt) {
     const int t = t0 + warp;
-    const float* lt = logits + (size_t)t * E;
-    float v[kPer], u[kPer];  // selection logits (with the bias), weight logits
-    // all loads first (logits, then the bias), so they are in flight together
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      u[i] = lane + 32 * i < E ? __ldcg(lt + lane + 32 * i) : -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      v[i] = (bias && lane + 32 * i < E) ? __ldg(bias + lane + 32 * i) : 0.f;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      float l = u[i], sl = bias ? l + v[i] : l;
-      if (lane + 32 * i < E && (!isfinite(sl) || !isfinite(l))) {
-        bad = true;
-        l = sl = -INFINITY;
-      }
-      v[i] = sl;
-      u[i] = sel_only ? l : sl;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0)
-      set_status(dev_status, QSM_DEV_NONFINITE);
-    float my_l;
     int my_e;
-    warp_topk<kPer>(v, E, k, my_l, my_e);
-    // this lane's selection's weight logit, and the largest one the softmax
-    // runs over (the selection, or all E)
-    float my_w = my_l;
-    if (sel_only && lane < k) {
-      my_w = __ldcg(lt + my_e);
-      if (!isfinite(my_w)) my_w = -INFINITY;
-    }
-    float top = -INFINITY;
-    if (renorm) {
-      top = warp_max(lane < k ? my_w : -INFINITY);
-    } else {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (lane + 32 * i < E) top = fmaxf(top, u[i]);
-      top = warp_max(top);
-    }
-    float part = 0.f;
-    if (renorm) {
-      if (lane < k) part = __expf(my_w - top);
-    } else {
-#pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (lane + 32 * i < E) part += __expf(u[i] - top);
-    }
-    const float inv = 1.0f / warp_sum(part);
+    float my_l, my_w;
+    route_select_warp<kPer>(logits + (size_t)t * E, bias, E, k, renormalize, dev_status,
+                            my_e, my_l, my_w);
     if (lane < k) {
       sel_l[warp][lane] = my_l;
       sel_e[warp][lane] = my_e;
       topk_idx[(size_t)t * k + lane] = my_e;
-      topk_w[(size_t)t * k + lane] = __expf(my_w - top) * inv;
+      topk_w[(size_t)t * k + lane] = my_w;
     }
     __syncwarp();
   }

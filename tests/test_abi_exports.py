@@ -46,7 +46,7 @@ def test_library_builds_loads_and_exports_everything():
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared but not exported"
     lib.qsm_abi_version.restype = ctypes.c_int32
-    assert lib.qsm_abi_version() == 2
+    assert lib.qsm_abi_version() == 3
     lib.qsm_status_str.restype = ctypes.c_char_p
     assert lib.qsm_status_str(0) == b"ok"
     # host-only helpers need no device

@@ -15,18 +15,18 @@ Q8_CASES = [1, 2, 3, 16, 40, 63, 64]
 A4_CASES = [1, 16, 64]
 
 
-def run(qsm, Lg, x, renorm=True):
+def run(qsm, Lg, x, renorm=True, one_launch=True):
     fwd = qsm.MoEForward(qsm.Layer.from_synth(Lg), x.shape[0], renormalize=renorm,
-                         want_f32=True)
+                         want_f32=True, one_launch=one_launch)
     fwd(x.cuda())
     torch.cuda.synchronize()
     return fwd
 
 
-def _check(qsm, shape, T, seed, zipf=None, renorm=True, tokens=None):
+def _check(qsm, shape, T, seed, zipf=None, renorm=True, tokens=None, one_launch=True):
     Lg, q, wr, bias = layer(shape, seed, zipf)
     x = x_for(shape, T, seed + T, Lg, wr, bias)
-    fwd = run(qsm, Lg, x, renorm)
+    fwd = run(qsm, Lg, x, renorm, one_launch)
     assert fwd.dev_status.item() == 0
     idx_o, w_o = oracle_route(x, wr, bias, shape.k, renorm)
     assert np.array_equal(fwd.topk_idx.cpu().numpy(), idx_o)
@@ -36,22 +36,32 @@ def _check(qsm, shape, T, seed, zipf=None, renorm=True, tokens=None):
     return err
 
 
-def test_tiny_layer(qsm):
-    _check(qsm, synth.TINY, 4, seed=0)
+# one_launch: T <= 8 goes through moe_decode_layer (one launch) or through
+# route + group + FFN launches; larger T always takes the launches.
+@pytest.mark.parametrize("one_launch", [True, False])
+def test_tiny_layer(qsm, one_launch):
+    _check(qsm, synth.TINY, 4, seed=0, one_launch=one_launch)
 
 
+@pytest.mark.parametrize("one_launch", [True, False])
 @pytest.mark.parametrize("T", Q8_CASES)
-def test_qwen_q8_decode(qsm, T):
-    _check(qsm, synth.QWEN, T, seed=0)
+def test_qwen_q8_decode(qsm, T, one_launch):
+    if T > 8 and not one_launch:
+        pytest.skip("the launches path is the only path for T > 8")
+    _check(qsm, synth.QWEN, T, seed=0, one_launch=one_launch)
 
 
+@pytest.mark.parametrize("one_launch", [True, False])
 @pytest.mark.parametrize("T", A4_CASES)
-def test_qwen_affine4_decode(qsm, T):
-    _check(qsm, synth.QWEN_A4, T, seed=1)
+def test_qwen_affine4_decode(qsm, T, one_launch):
+    if T > 8 and not one_launch:
+        pytest.skip("the launches path is the only path for T > 8")
+    _check(qsm, synth.QWEN_A4, T, seed=1, one_launch=one_launch)
 
 
-def test_full_softmax_weights(qsm):
-    _check(qsm, synth.QWEN, 5, seed=0, renorm=False)
+@pytest.mark.parametrize("one_launch", [True, False])
+def test_full_softmax_weights(qsm, one_launch):
+    _check(qsm, synth.QWEN, 5, seed=0, renorm=False, one_launch=one_launch)
 
 
 def test_all_tokens_on_same_experts(qsm):
