@@ -370,12 +370,10 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   pdl_wait();
   pdl_launch_dependents();
   // barrier base: every earlier call on this workspace has completed, so the
-  // counter holds a multiple of G plus arrivals of this call
-  unsigned long long gbase = 0;
-  if (tid == 0) {
-    const unsigned long long v = ld_acquire_u64(p.gbar);
-    gbase = v - v % (unsigned long long)G;
-  }
+  // counter holds a multiple of G plus arrivals of this call.  The load is
+  // used only at barrier 1, so its latency hides behind phase A.
+  unsigned long long gread = 0;
+  if (tid == 0) gread = ld_acquire_u64(p.gbar);
   wait(&xbar, 0);  // router rows, x (and the shared-expert gate vector)
   for (int e0 = ea; e0 < eb; e0 += 2) {
     const int e = e0 + sub;
@@ -447,6 +445,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
 
   // ---- grid barrier 1: all logits written
   named_bar(kBarCons, kCW * 32);
+  const unsigned long long gbase = gread - gread % (unsigned long long)G;
   if (tid == 0 && !grid_barrier(p.gbar, gbase + G, s_bad ? kShortWait : kWaitIters)) {
     s_bad = 1;
     set_status(p.status, QSM_DEV_TIMEOUT);

@@ -214,9 +214,10 @@ cudaError_t launch_i8_ks(const int8_t* qx, const float* dx, const int8_t* q,
 // programmatic-launch wait since the weights are static.  When one CTA does
 // not take all of K, the CTAs of a tile form a cluster along x and store
 // their segment partials into the rank-0 CTA's shared memory, which adds
-// them in segment order: the order of the register-fed kernels above, so
-// every row comes out bit-identical to theirs and independent of N.  Rows
-// past N and chunks past K arrive as zeros (TMA fill) and are never stored.
+// them in segment order.  Every TMA-fed kernel sums a row in the same order
+// (fixed by K alone, see segment_partial), so a row's bits do not depend on N
+// or on which of them ran.  Rows past N and chunks past K arrive as zeros
+// (TMA fill) and are never stored.
 
 constexpr int kTmaSegBytes = 16 * kSeg;              // codes of one segment
 constexpr int kTmaScaleBytes = 16 * (kSeg / 32) * 2;  // its 16 x 16 fp16 scales
@@ -228,6 +229,104 @@ constexpr int kTmaMaxSeg = 32;                        // K <= 16384
 __device__ __forceinline__ uint2 lds_sw128(const unsigned char* tile, int line, int b) {
   return *reinterpret_cast<const uint2*>(
       tile + line * 128 + ((((b >> 4) ^ (line & 7)) << 4) | (b & 15)));
+}
+
+// One 64-chunk of a 16-row tile (TMA-written codes, 3D row view with the
+// 128-byte swizzle, and scales in shared memory) into the accumulators of
+// rows g and g + 8: acc[0] / acc[2] (valid in lanes q == 0).  The activation
+// comes from global memory (bf16, kXs false) or from shared memory (fp16,
+// kXs true); in the int8 mode its codes and block scales likewise.
+template <bool kI8, bool kXs>
+__device__ __forceinline__ void tile_chunk(float (&acc)[4], const unsigned char* cs,
+                                           const uint32_t* ss, const void* xa,
+                                           const float* xd, int kb, int ch, int g, int q) {
+  RawA r;
+  const int lg = (ch >> 1) * 16 + g;  // line of row g in 128-byte chunk ch / 2
+  const int b = (ch & 1) * 64 + 8 * q;
+  r.g0 = lds_sw128(cs, lg, b);
+  r.g1 = lds_sw128(cs, lg, b + 32);
+  r.h0 = lds_sw128(cs, lg + 8, b);
+  r.h1 = lds_sw128(cs, lg + 8, b + 32);
+  r.sg = ss[g * 8 + ch];
+  r.sh = ss[(g + 8) * 8 + ch];
+  const int k0 = kb + 64 * ch;
+  if constexpr (!kI8) {
+    uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
+    if (g == 0) {
+      if constexpr (kXs) {
+        const __half* xs = static_cast<const __half*>(xa);
+        X0 = *reinterpret_cast<const uint4*>(xs + k0 + 8 * q);
+        X1 = *reinterpret_cast<const uint4*>(xs + k0 + 32 + 8 * q);
+      } else {
+        const uint16_t* x = static_cast<const uint16_t*>(xa);
+        X0 = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(x + k0 + 8 * q)));
+        X1 = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(x + k0 + 32 + 8 * q)));
+      }
+    }
+    chunk_mma<QSM_Q8_0>(acc, r, X0, X1);
+  } else {
+    const int8_t* qx = static_cast<const int8_t*>(xa);
+    uint2 x0 = make_uint2(0u, 0u), x1 = x0;
+    if (g == 0) {
+      x0 = *reinterpret_cast<const uint2*>(qx + k0 + 8 * q);
+      x1 = *reinterpret_cast<const uint2*>(qx + k0 + 32 + 8 * q);
+    }
+    int s0[4], s1[4];
+    const uint32_t a0[4] = {r.g0.x, r.h0.x, r.g0.y, r.h0.y};
+    const uint32_t a1[4] = {r.g1.x, r.h1.x, r.g1.y, r.h1.y};
+    mma_16832_s8(s0, a0, x0.x, x0.y);
+    mma_16832_s8(s1, a1, x1.x, x1.y);
+    if (q == 0) {
+      const float d0 = xd[k0 / 32], d1 = xd[k0 / 32 + 1];
+      const float sg0 = __half2float(__ushort_as_half((unsigned short)(r.sg & 0xffffu)));
+      const float sg1 = __half2float(__ushort_as_half((unsigned short)(r.sg >> 16)));
+      const float sh0 = __half2float(__ushort_as_half((unsigned short)(r.sh & 0xffffu)));
+      const float sh1 = __half2float(__ushort_as_half((unsigned short)(r.sh >> 16)));
+      acc[0] = fmaf((float)s0[0], sg0 * d0, acc[0]);
+      acc[0] = fmaf((float)s1[0], sg1 * d1, acc[0]);
+      acc[2] = fmaf((float)s0[2], sh0 * d0, acc[2]);
+      acc[2] = fmaf((float)s1[2], sh1 * d1, acc[2]);
+    }
+  }
+}
+
+// The partial of a 512-wide segment is (chain over chunks 0..3) + (chain
+// over chunks 4..7), each chain accumulated from zero in chunk order; the
+// TMA-fed kernels all follow this order, so a row's bits depend on K only.
+constexpr int kChain = 4;  // chunks per chain
+
+// Both chains of the segment at kb in one warp, interleaved (independent
+// accumulators, so the chains' latencies overlap).
+template <bool kI8, bool kXs>
+__device__ __forceinline__ void segment_partial(const unsigned char* cs,
+                                                const unsigned char* scl, const void* xa,
+                                                const float* xd, int kb, int K, int g, int q,
+                                                float& pg, float& ph) {
+  const uint32_t* ss = reinterpret_cast<const uint32_t*>(scl);
+  const int nch = min(kSeg, K - kb) / 64;
+  float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kChain; ++i) {
+    if (i < nch) tile_chunk<kI8, kXs>(a, cs, ss, xa, xd, kb, i, g, q);
+    if (kChain + i < nch) tile_chunk<kI8, kXs>(b, cs, ss, xa, xd, kb, kChain + i, g, q);
+  }
+  pg = a[0] + b[0];
+  ph = a[2] + b[2];
+}
+
+// One chain (half = 0: chunks 0..3, 1: chunks 4..7) of the segment at kb.
+template <bool kI8, bool kXs>
+__device__ __forceinline__ void chain_partial(const unsigned char* cs, const unsigned char* scl,
+                                              const void* xa, const float* xd, int kb, int K,
+                                              int half, int g, int q, float& pg, float& ph) {
+  const uint32_t* ss = reinterpret_cast<const uint32_t*>(scl);
+  const int nch = min(kSeg, K - kb) / 64;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kChain; ++i)
+    if (kChain * half + i < nch) tile_chunk<kI8, kXs>(a, cs, ss, xa, xd, kb, kChain * half + i, g, q);
+  pg = a[0];
+  ph = a[2];
 }
 
 template <bool kI8>
@@ -273,57 +372,12 @@ q8_gemv_tma_kernel(const __grid_constant__ CUtensorMap cmap,
       if (lane == 0 && dev_status) set_status(dev_status, QSM_DEV_TIMEOUT);
       mbar_wait_bounded(&bar[warp], 0, kWaitIters);  // let the copy land
     } else {
-      const unsigned char* cs = codes + warp * kTmaSegBytes;
-      const uint32_t* ss = reinterpret_cast<const uint32_t*>(scl + warp * kTmaScaleBytes);
-      const int kb = (seg0 + warp) * kSeg;
-      const int nch = min(kSeg, K - kb) / 64;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int ch = 0; ch < nch; ++ch) {
-        RawA r;
-        const int lg = (ch >> 1) * 16 + g;  // line of row g in 128-byte chunk ch / 2
-        const int b = (ch & 1) * 64 + 8 * q;
-        r.g0 = lds_sw128(cs, lg, b);
-        r.g1 = lds_sw128(cs, lg, b + 32);
-        r.h0 = lds_sw128(cs, lg + 8, b);
-        r.h1 = lds_sw128(cs, lg + 8, b + 32);
-        r.sg = ss[g * 8 + ch];
-        r.sh = ss[(g + 8) * 8 + ch];
-        const int k0 = kb + 64 * ch;
-        if constexpr (!kI8) {
-          uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
-          if (g == 0) {
-            X0 = bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(x + k0 + 8 * q)));
-            X1 = bf16x8_to_f16x8(
-                __ldg(reinterpret_cast<const uint4*>(x + k0 + 32 + 8 * q)));
-          }
-          chunk_mma<QSM_Q8_0>(acc, r, X0, X1);
-        } else {
-          uint2 x0 = make_uint2(0u, 0u), x1 = x0;
-          if (g == 0) {
-            x0 = __ldg(reinterpret_cast<const uint2*>(qx + k0 + 8 * q));
-            x1 = __ldg(reinterpret_cast<const uint2*>(qx + k0 + 32 + 8 * q));
-          }
-          int s0[4], s1[4];
-          const uint32_t a0[4] = {r.g0.x, r.h0.x, r.g0.y, r.h0.y};
-          const uint32_t a1[4] = {r.g1.x, r.h1.x, r.g1.y, r.h1.y};
-          mma_16832_s8(s0, a0, x0.x, x0.y);
-          mma_16832_s8(s1, a1, x1.x, x1.y);
-          if (q == 0) {
-            const float d0 = __ldg(dx + k0 / 32), d1 = __ldg(dx + k0 / 32 + 1);
-            const float sg0 = __half2float(__ushort_as_half((unsigned short)(r.sg & 0xffffu)));
-            const float sg1 = __half2float(__ushort_as_half((unsigned short)(r.sg >> 16)));
-            const float sh0 = __half2float(__ushort_as_half((unsigned short)(r.sh & 0xffffu)));
-            const float sh1 = __half2float(__ushort_as_half((unsigned short)(r.sh >> 16)));
-            acc[0] = fmaf((float)s0[0], sg0 * d0, acc[0]);
-            acc[0] = fmaf((float)s1[0], sg1 * d1, acc[0]);
-            acc[2] = fmaf((float)s0[2], sh0 * d0, acc[2]);
-            acc[2] = fmaf((float)s1[2], sh1 * d1, acc[2]);
-          }
-        }
-      }
-      pg = acc[0];
-      ph = acc[2];
+      if constexpr (kI8)
+        segment_partial<true, false>(codes + warp * kTmaSegBytes, scl + warp * kTmaScaleBytes,
+                                     qx, dx, (seg0 + warp) * kSeg, K, g, q, pg, ph);
+      else
+        segment_partial<false, false>(codes + warp * kTmaSegBytes, scl + warp * kTmaScaleBytes,
+                                      x, nullptr, (seg0 + warp) * kSeg, K, g, q, pg, ph);
     }
   }
   if (warp < mine && q == 0) {
@@ -343,6 +397,138 @@ q8_gemv_tma_kernel(const __grid_constant__ CUtensorMap cmap,
     for (int seg = 0; seg < nseg; ++seg) s += red[seg][threadIdx.x];
     const int n = n0 + threadIdx.x;
     if (n < N) y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  }
+}
+
+// ------------------------------------------ persistent streaming (large N)
+//
+// With many tiles, one CTA per SM walks tiles t = blockIdx.x, t + gridDim.x,
+// ...; a tile's segments stream through a ring of kStreamS stages (up to 4
+// segments each) filled by one producer thread, so every SM keeps ~170 KB of
+// weights in flight for the whole call instead of relaunching a CTA per tile.
+// The activation is staged once in shared memory (fp16, or the int8 codes
+// and block scales).  Two groups of eight consumer warps take alternate
+// tiles; in a group each warp takes one chain (half a segment) of a stage,
+// and a tile's chains and segments are added in the order above.
+
+constexpr int kStreamS = 5;
+constexpr int kStreamSeg = 4;  // segments per stage
+constexpr int kStageBytes = kStreamSeg * (kTmaSegBytes + kTmaScaleBytes);  // 34 KB
+constexpr int kStreamGW = 2 * kStreamSeg;  // warps of a consumer group: one per chain
+constexpr int kStreamCW = 2 * kStreamGW;   // two groups, alternate tiles
+constexpr int kStreamWarps = kStreamCW + 1;
+
+template <bool kI8>
+__global__ void __launch_bounds__(kStreamWarps * 32, 1)
+q8_gemv_stream_kernel(const __grid_constant__ CUtensorMap cmap,
+                      const __grid_constant__ CUtensorMap smap,
+                      const uint16_t* __restrict__ x, const int8_t* __restrict__ qx,
+                      const float* __restrict__ dx, int N, int K, int tiles,
+                      uint16_t* __restrict__ y, int32_t* dev_status) {
+  extern __shared__ unsigned char gemv_dyn[];
+  __shared__ __align__(8) uint64_t full[kStreamS], empty[kStreamS];
+  __shared__ float red[2][2][kTmaMaxSeg][2][16];  // [group][tile parity][seg][chain][row]
+  __shared__ volatile int s_bad;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int nseg = (K + kSeg - 1) / kSeg;
+  const int nst = (nseg + kStreamSeg - 1) / kStreamSeg;  // stages per tile
+  const int G = gridDim.x;
+  const int ntile = (tiles - (int)blockIdx.x + G - 1) / G;
+  const int total = ntile * nst;
+  const uint32_t pad = (1024u - (smem_u32(gemv_dyn) & 1023u)) & 1023u;
+  unsigned char* ring = gemv_dyn + pad;  // stage: [4][8 KB] codes, then [4][512] scales
+  unsigned char* xsm = ring + kStreamS * kStageBytes;  // fp16 x [K], or int8 codes + scales
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStreamS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStreamGW);  // the stage's consumer group
+    }
+    s_bad = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (mbar_wait_bounded(bar, parity, s_bad ? 1024u : kWaitIters)) return;
+    s_bad = 1;
+    if (dev_status) set_status(dev_status, QSM_DEV_TIMEOUT);
+  };
+
+  if (warp == kStreamCW) {  // producer
+    if (lane != 0) return;
+    auto issue = [&](int p) {
+      const int slot = p % kStreamS;
+      unsigned char* st = ring + slot * kStageBytes;
+      const int tile = (int)blockIdx.x + (p / nst) * G, seg0 = (p % nst) * kStreamSeg;
+      const int cnt = min(kStreamSeg, nseg - seg0);
+      mbar_arrive_expect_tx(&full[slot], (uint32_t)cnt * (kTmaSegBytes + kTmaScaleBytes));
+      for (int j = 0; j < cnt; ++j) {
+        tc::tma_load_3d(st + j * kTmaSegBytes, &cmap, 0, tile * 16, (seg0 + j) * (kSeg / 128),
+                        &full[slot]);
+        tc::tma_load_2d(st + kStreamSeg * kTmaSegBytes + j * kTmaScaleBytes, &smap,
+                        (seg0 + j) * (kSeg / 32), tile * 16, &full[slot]);
+      }
+    };
+    int p = 0;
+    for (; p < total && p < kStreamS; ++p) issue(p);  // static weights: before the wait
+    pdl_wait();
+    pdl_launch_dependents();
+    for (; p < total; ++p) {
+      wait(&empty[p % kStreamS], ((p / kStreamS) - 1) & 1);
+      issue(p);
+    }
+    if (s_bad)  // let the last copy of every stage land
+      for (int s = 0; s < kStreamS && s < total; ++s)
+        mbar_wait_bounded(&full[s], (((s + ((total - 1 - s) / kStreamS) * kStreamS)) /
+                                     kStreamS) & 1, kWaitIters);
+    return;
+  }
+
+  pdl_wait();  // x (or its codes) come from the preceding launch
+  pdl_launch_dependents();
+  constexpr int nct = kStreamCW * 32;
+  if constexpr (!kI8) {  // x -> fp16 in shared memory, once
+    for (int i = threadIdx.x; i < K / 8; i += nct)
+      reinterpret_cast<uint4*>(xsm)[i] =
+          bf16x8_to_f16x8(__ldg(reinterpret_cast<const uint4*>(x) + i));
+  } else {
+    for (int i = threadIdx.x; i < K / 16; i += nct)
+      reinterpret_cast<uint4*>(xsm)[i] = __ldg(reinterpret_cast<const uint4*>(qx) + i);
+    for (int i = threadIdx.x; i < K / 32; i += nct)
+      reinterpret_cast<float*>(xsm + K)[i] = __ldg(dx + i);
+  }
+  asm volatile("barrier.sync 1, %0;" ::"r"(nct) : "memory");
+  const void* xa = xsm;
+  const float* xd = kI8 ? reinterpret_cast<const float*>(xsm + K) : nullptr;
+  const int grp = warp / kStreamGW, gw = warp % kStreamGW;
+  const int sw = gw >> 1, half = gw & 1;  // segment of the stage, chain of the segment
+  for (int p = 0; p < total; ++p) {
+    const int slot = p % kStreamS, i = p / nst, seg = (p % nst) * kStreamSeg + sw;
+    if ((i & 1) != grp) continue;  // the other group's tile
+    wait(&full[slot], (p / kStreamS) & 1);
+    const unsigned char* st = ring + slot * kStageBytes;
+    if (seg < nseg) {
+      float pg, ph;
+      chain_partial<kI8, true>(st + sw * kTmaSegBytes,
+                               st + kStreamSeg * kTmaSegBytes + sw * kTmaScaleBytes, xa, xd,
+                               seg * kSeg, K, half, g, q, pg, ph);
+      if (q == 0) {
+        red[grp][(i >> 1) & 1][seg][half][g] = pg;
+        red[grp][(i >> 1) & 1][seg][half][g + 8] = ph;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[slot]);
+    if (p % nst == nst - 1) {  // the tile's last stage: add its segments
+      asm volatile("barrier.sync %0, %1;" ::"r"(2 + grp), "r"(kStreamGW * 32) : "memory");
+      if (gw == 0 && lane < 16) {
+        const float(*rr)[2][16] = red[grp][(i >> 1) & 1];
+        float sum = 0.f;
+        for (int s2 = 0; s2 < nseg; ++s2) sum += rr[s2][0][lane] + rr[s2][1][lane];
+        const int n = ((int)blockIdx.x + i * G) * 16 + lane;
+        if (n < N) y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+      }
+    }
   }
 }
 
@@ -369,6 +555,22 @@ bool launch_tma(const uint16_t* x, const int8_t* qx, const float* dx, const int8
     return false;
   const long tiles = (N + 15) / 16;
   const int nseg = (K + kSeg - 1) / kSeg;
+  int nsm = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (nsm > 0 && tiles >= 8L * nsm && tiles < (1L << 30)) {  // persistent streaming
+    static bool attr[2] = {false, false};  // sized for K <= 16384
+    const size_t smem = 1024 + (size_t)kStreamS * kStageBytes + (size_t)K * 2;
+    if (!attr[kI8]) {
+      cudaFuncSetAttribute(q8_gemv_stream_kernel<kI8>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(1024 + (size_t)kStreamS * kStageBytes + 16384 * 2));
+      attr[kI8] = true;
+    }
+    *err = launch_pdl(q8_gemv_stream_kernel<kI8>, dim3(nsm), dim3(kStreamWarps * 32), smem,
+                      s, cmap, smap, x, qx, dx, N, K, (int)tiles, y, status);
+    return true;
+  }
   const int spc = gemv_tma_spc(tiles, nseg);
   const int slices = (nseg + spc - 1) / spc;
   const long gy = tiles < 65535 ? tiles : 65535;

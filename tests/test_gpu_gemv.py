@@ -92,15 +92,26 @@ def test_gemv_edge_shapes(qsm, N, K):
                          oracle.q8_gemv_i8(q_o, d_o, q.cpu().numpy(), bits16(d)))
 
 
-def test_gemv_rows_independent_of_n(qsm):
-    """A row's bits do not depend on how many rows the call has (the split
-    of K over CTAs changes with N; the summation order does not)."""
-    K = 8192
-    x, q, d = synth.draw_gemv(4096, K, "cuda", seed=12)
-    full = qsm.q8_gemv(x, q, d)
+@pytest.mark.parametrize("N,K", [(4096, 8192), (20000, 2048), (20000, 8192), (20000, 768)])
+def test_gemv_rows_independent_of_n(qsm, N, K):
+    """A row's bits do not depend on how many rows the call has: the split
+    of K over CTAs changes with N, and 20000 rows (>= 8 tiles per SM) take
+    the persistent streaming kernel, but the summation order is the same."""
+    x, q, d = synth.draw_gemv(N, K, "cuda", seed=12)
+    qx, dx = qsm.q8_quantize_x(x)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    full = qsm.q8_gemv(x, q, d, dev_status=st)
+    full8 = qsm.q8_gemv_i8(qx, dx, q, d, dev_status=st)
     part = qsm.q8_gemv(x, q[:48].contiguous(), d[:48].contiguous())
+    part8 = qsm.q8_gemv_i8(qx, dx, q[:48].contiguous(), d[:48].contiguous())
     torch.cuda.synchronize()
+    assert st.item() == 0
     assert torch.equal(full[:48].view(torch.int16), part.view(torch.int16))
+    assert torch.equal(full8[:48].view(torch.int16), part8.view(torch.int16))
+    rows = np.random.default_rng(N + K).choice(N, 512, replace=False)
+    ref = oracle.q8_gemv(bits16(x), q[rows].cpu().numpy(), bits16(d[rows]))
+    assert_faithful_bf16(full.float().cpu().numpy()[rows], ref)
+    assert int(rows.max()) < N
 
 
 # ------------------------------------------------ int8-activation mode
