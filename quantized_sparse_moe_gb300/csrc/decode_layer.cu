@@ -51,8 +51,10 @@ namespace dlayer {
 
 using namespace gemv;
 
-constexpr int kCW = 8;                    // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;  // + the producer warp
+// consumer warps: 16 when the top-k keeps few candidates per lane (E <= 256;
+// the registers then allow 17 warps), else 8; plus one producer warp
+template <int kPer>
+constexpr int consumer_warps() { return kPer <= 8 ? 16 : 8; }
 constexpr int kMaxS = 5;                  // ring slots (at most)
 constexpr int kMaxT = 8;
 constexpr int kMaxE = 1024;
@@ -168,14 +170,16 @@ __device__ __forceinline__ void load_tile_a(RawA& r, const unsigned char* codes_
   }
 }
 
-template <int QT, int kPer>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int QT, int kPer, int kCW = consumer_warps<kPer>()>
+__global__ void __launch_bounds__((kCW + 1) * 32, 1)
 decode_layer_kernel(const __grid_constant__ Params p) {
+  constexpr int kThreads = (kCW + 1) * 32;
+  constexpr int kSubs = kCW * 32 / kTPE;  // experts per router pass
   extern __shared__ unsigned char dl_dyn[];
   __shared__ __align__(8) uint64_t full[kMaxS], empty[kMaxS], hfull[2], hempty[2];
   __shared__ __align__(8) uint64_t xbar, rdy, b2;
   __shared__ float red[2][kCW][32][4];
-  __shared__ float rsum[2][kTPE / 32][kMaxT];
+  __shared__ float rsum[kSubs][kTPE / 32][kMaxT];
   __shared__ int sel_e[kMaxT][32];
   __shared__ float sel_w[kMaxT][32];
   __shared__ unsigned bm[kMaxE / 32];
@@ -363,7 +367,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   }
 
   // ================================================================ consumers
-  // ---- A: logits of experts [ea, eb) (pairs of experts, 128 threads each)
+  // ---- A: logits of experts [ea, eb), kSubs experts per pass, 128 threads each
   const int sub = tid / kTPE, st = tid % kTPE;
   const int ea = c * p.epc, eb = min(E, ea + p.epc);
   const int H4 = H / 4;
@@ -375,7 +379,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   unsigned long long gread = 0;
   if (tid == 0) gread = ld_acquire_u64(p.gbar);
   wait(&xbar, 0);  // router rows, x (and the shared-expert gate vector)
-  for (int e0 = ea; e0 < eb; e0 += 2) {
+  for (int e0 = ea; e0 < eb; e0 += kSubs) {
     const int e = e0 + sub;
     const bool mine = e < eb;
     const float4* wrow = reinterpret_cast<const float4*>(wrs + (size_t)(mine ? e - ea : 0) * H);
@@ -419,7 +423,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       }
     }
     named_bar(kBarCons, kCW * 32);
-    if (tid < 2 * kMaxT) {
+    if (tid < kSubs * kMaxT) {
       const int s2 = tid / kMaxT, i = tid % kMaxT;
       const int e2 = e0 + s2;
       if (e2 < eb && i < T) {
@@ -652,7 +656,7 @@ int sm_count_dl() {
 }
 
 // dynamic shared memory per CTA: the per-block maximum minus the static part
-constexpr size_t kSmemBudget = 227 * 1024 - 12 * 1024;
+constexpr size_t kSmemBudget = 227 * 1024 - 20 * 1024;
 
 struct Geo {
   int hb, hsb, ib, isb, m, ns, hall, slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off,
@@ -737,7 +741,8 @@ cudaError_t launch(const Params& prm, size_t smem, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(decode_layer_kernel<QT, kPer>, dim3(prm.G), dim3(kThreads), smem, stream,
+  return launch_pdl(decode_layer_kernel<QT, kPer>, dim3(prm.G),
+                    dim3((consumer_warps<kPer>() + 1) * 32), smem, stream,
                     prm);
 }
 
