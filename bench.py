@@ -306,6 +306,10 @@ def run_ours(args, wl, rank, world):
         # the dominant launch group is the whole chunked layer call
         ffn_ms = ms / nL
         traffic = None
+    elif one_launch:
+        # the timed step is nL back-to-back launches of this one kernel (the
+        # event-bracketed replay above breaks their programmatic overlap)
+        ffn_ms = ms / nL
 
     # end to end through the public API: pinned host x in, host y out
     xh = torch.stack(xs).cpu().pin_memory()
@@ -612,7 +616,9 @@ def run_gemv(args, wl, rank, world):
         "roofline": {"kernel": f"{'q8_gemv_i8' if i8 else 'q8_gemv'} {top} "
                                f"({per_shape[top]['N']}x{per_shape[top]['K']})",
                      "bound": "hbm", "achieved": per_shape[top]["GB/s"], "peak": hbm,
-                     "unit": "GB/s", "frac": per_shape[top]["GB/s"] / hbm, "traffic": None,
+                     "unit": "GB/s", "frac": per_shape[top]["GB/s"] / hbm,
+                     # DRAM bytes of one LM-head launch (ncu), int8-activation mode not captured
+                     "traffic": measured_traffic("gemv") if not i8 and top == "lm_head" else None,
                      "bytes_per_launch": per_shape[top]["N"] * per_shape[top]["K"] * 34 // 32,
                      "launch_ms": per_shape[top]["us"] / 1e3, "peak_kind": peak_kind},
         "step_roofline": {"bytes_per_step": step_bytes, "frac": step_bytes / (ms * 1e-3) / 1e9 / hbm},

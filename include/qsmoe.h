@@ -74,8 +74,9 @@ typedef enum {
 #define QSM_DEV_BAD_EXPERT_ID 1 /* topk_idx entry outside [0, E) */
 #define QSM_DEV_NONFINITE 2     /* non-finite router logit */
 #define QSM_DEV_FP16_RANGE 4    /* a value staged in fp16 overflowed */
-#define QSM_DEV_TIMEOUT 8       /* a bounded wait on a copy ran out (the
-                                   kernel skipped its work and returned) */
+#define QSM_DEV_TIMEOUT 8       /* a bounded wait (on a copy, or a grid
+                                   barrier of moe_decode_layer) ran out: the
+                                   kernel returned, its results are invalid */
 
 typedef enum { QSM_Q8_0 = 0, QSM_AFFINE4_G64 = 1 } qsm_qtype;
 
@@ -386,6 +387,14 @@ QSM_API uint64_t qsm_launch_count(void);
 /* Test hook: 0 = choose the FFN path by T (default), 1 = always the decode
  * kernels, 2 = always the prefill kernels (when T allows).  Process-wide. */
 QSM_API qsm_status qsm_debug_force_path(int32_t mode);
+
+/* Test hook for the bounded waits: raise the targets of moe_decode_layer's
+ * grid barriers by `skew` arrivals (0 = off, the default), so that no call
+ * can complete them: every wait runs out, the kernel sets QSM_DEV_TIMEOUT
+ * in *dev_status, finishes with invalid results and returns, and the
+ * context stays usable.  The barrier counter stays consistent (every CTA
+ * still arrives once per barrier).  Process-wide; skew in [0, 1024]. */
+QSM_API qsm_status qsm_debug_barrier_skew(int32_t skew);
 
 #ifdef __cplusplus
 }

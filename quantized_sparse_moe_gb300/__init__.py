@@ -29,6 +29,7 @@ AFFINE4_G64 = 1
 DEV_BAD_EXPERT_ID = 1
 DEV_NONFINITE = 2
 DEV_FP16_RANGE = 4
+DEV_TIMEOUT = 8
 
 _lock = threading.Lock()
 _lib = None
@@ -115,6 +116,8 @@ def lib() -> ctypes.CDLL:
             L.moe_decode_layer.argtypes = [ctypes.POINTER(MoELayerC), P, i32, P, P, i32,
                                            P, P, P, P, P, sz, P, P]
             L.moe_decode_layer.restype = st
+            L.qsm_debug_barrier_skew.argtypes = [i32]
+            L.qsm_debug_barrier_skew.restype = st
             L.qsm_launch_count.argtypes = []
             L.qsm_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -429,6 +432,11 @@ def moe_decode_layer(layer: Layer, x: torch.Tensor, renormalize=True,
         _p(y_f32 if y_f32 is not False else None), _p(workspace), workspace.numel(),
         _p(dev_status), _stream(stream)), "moe_decode_layer")
     return y, (y_f32 if isinstance(y_f32, torch.Tensor) else None), topk_idx, topk_w
+
+
+def debug_barrier_skew(skew: int) -> None:
+    """Test hook: raise the decode layer's grid-barrier targets (0 = off)."""
+    _check(lib().qsm_debug_barrier_skew(int(skew)), "qsm_debug_barrier_skew")
 
 
 def force_path(mode: str | int) -> None:

@@ -98,6 +98,7 @@ struct Params {
   uint16_t* y;
   float* y32;
   int32_t* status;
+  int skew;               // test hook: added to the barrier targets (0)
 };
 
 // Barrier over n threads (a multiple of 32) of the CTA; the non-aligned form,
@@ -450,7 +451,8 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   // ---- grid barrier 1: all logits written
   named_bar(kBarCons, kCW * 32);
   const unsigned long long gbase = gread - gread % (unsigned long long)G;
-  if (tid == 0 && !grid_barrier(p.gbar, gbase + G, s_bad ? kShortWait : kWaitIters)) {
+  if (tid == 0 &&
+      !grid_barrier(p.gbar, gbase + G + p.skew, s_bad ? kShortWait : kWaitIters)) {
     s_bad = 1;
     set_status(p.status, QSM_DEV_TIMEOUT);
   }
@@ -564,7 +566,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   // ---- grid barrier 2: all h written
   named_bar(kBarCons, kCW * 32);
   if (tid == 0) {
-    if (!grid_barrier(p.gbar, gbase + 2ull * G, s_bad ? kShortWait : kWaitIters)) {
+    if (!grid_barrier(p.gbar, gbase + 2ull * G + p.skew, s_bad ? kShortWait : kWaitIters)) {
       s_bad = 1;
       set_status(p.status, QSM_DEV_TIMEOUT);
     }
@@ -719,6 +721,8 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
   return true;
 }
 
+int g_barrier_skew = 0;  // qsm_debug_barrier_skew
+
 struct WsLayout {
   size_t logits, hbuf, total;
 };
@@ -748,6 +752,12 @@ cudaError_t launch(const Params& prm, size_t smem, cudaStream_t stream) {
 
 }  // namespace dlayer
 }  // namespace qsm
+
+extern "C" qsm_status qsm_debug_barrier_skew(int32_t skew) {
+  if (skew < 0 || skew > 1024) return QSM_ERR_INVALID_ARGUMENT;
+  qsm::dlayer::g_barrier_skew = skew;
+  return QSM_OK;
+}
 
 extern "C" size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T) {
   qsm::dlayer::Geo g;
@@ -843,6 +853,7 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.y = y;
   prm.y32 = y_f32;
   prm.status = dev_status;
+  prm.skew = g_barrier_skew;
   cudaError_t err;
   if (E <= 256)
     err = a4 ? launch<QSM_AFFINE4_G64, 8>(prm, g.smem, stream)

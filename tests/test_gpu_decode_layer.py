@@ -107,3 +107,30 @@ def test_decode_layer_unsupported(qsm):
     assert qsm.moe_decode_layer(L, x, raise_unsupported=False) is None
     with pytest.raises(qsm.QSMError):
         qsm.moe_decode_layer(L, x)
+
+
+def test_decode_layer_barrier_timeout_is_reported(qsm):
+    """A grid barrier that cannot complete (test hook: target raised by one)
+    makes every bounded wait run out: the call sets QSM_DEV_TIMEOUT and
+    returns; the context stays usable and the next call is exact."""
+    shape = synth.TINY
+    Lg, q, wr, bias = layer(shape, 7, None)
+    L = qsm.Layer.from_synth(Lg)
+    x = x_for(shape, 1, 57, Lg, wr, bias).cuda()
+    ws = torch.zeros(qsm.decode_layer_workspace_bytes(L, 1), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qsm.debug_barrier_skew(1)
+    try:
+        qsm.moe_decode_layer(L, x, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        qsm.debug_barrier_skew(0)
+    assert st.item() & qsm.DEV_TIMEOUT
+    st.zero_()
+    y, y32, idx, w = qsm.moe_decode_layer(L, x, y_f32=True, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    idx_o, w_o = oracle_route(x.cpu(), wr, bias, shape.k, True)
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    err, _ = check_layer_output(y, y32, x.cpu(), idx_o, w_o, q)
+    assert err <= TOL
