@@ -16,10 +16,11 @@
 
 namespace qsm {
 
-// lt: the token's E logits without the bias (read through L2: another CTA
-// may have written them in this launch).  Lane j < k receives the j-th
+// lt: the token's E logits without the bias, in global memory (read
+// through L2: another CTA may have written them in this launch) or, with
+// kShared, in this CTA's shared memory.  Lane j < k receives the j-th
 // selected expert, its selection logit and its routing weight.
-template <int kPer>
+template <int kPer, bool kShared = false>
 __device__ __forceinline__ void route_select_warp(const float* __restrict__ lt,
                                                   const float* __restrict__ bias, int E,
                                                   int k, int flags, int32_t* dev_status,
@@ -31,7 +32,8 @@ __device__ __forceinline__ void route_select_warp(const float* __restrict__ lt,
   // all loads first (logits, then the bias), so they are in flight together
 #pragma unroll
   for (int i = 0; i < kPer; ++i)
-    u[i] = lane + 32 * i < E ? __ldcg(lt + lane + 32 * i) : -INFINITY;
+    u[i] = lane + 32 * i < E ? (kShared ? lt[lane + 32 * i] : __ldcg(lt + lane + 32 * i))
+                             : -INFINITY;
 #pragma unroll
   for (int i = 0; i < kPer; ++i)
     v[i] = (bias && lane + 32 * i < E) ? __ldg(bias + lane + 32 * i) : 0.f;
@@ -54,7 +56,7 @@ __device__ __forceinline__ void route_select_warp(const float* __restrict__ lt,
   // runs over (the selection, or all E)
   float my_w = my_l;
   if (sel_only && lane < k) {
-    my_w = __ldcg(lt + my_e);
+    my_w = kShared ? lt[my_e] : __ldcg(lt + my_e);
     if (!isfinite(my_w)) my_w = -INFINITY;
   }
   float top = -INFINITY;

@@ -17,12 +17,14 @@
 // error near plain fp32 accumulation, and the KS CTAs of a tile run on KS
 // SMs.  Warp 0 streams x tiles and split-weight tiles by TMA (128-byte
 // swizzle), lane 0 of warp 1 issues the MMAs, and warps 4-7 (one
-// tensor-memory lane = one token each) write the partial logits to the
-// workspace.  The CTA that finishes a tile last (a per-tile arrival counter,
-// no waiting) adds the KS partials of each token in slice order plus the
-// bias into a shared-memory tile (all its threads, coalesced), then one
-// thread per token keeps the top k in registers and writes the routing
-// weights; it re-arms the counter.
+// tensor-memory lane = one token each) write the slice's partial logits
+// into the CTA's own shared memory.  The KS CTAs of a tile form a cluster:
+// after a cluster barrier, CTA q adds, for its 128/KS tokens, the KS slices
+// in slice order, reading the others' shared memory (distributed shared
+// memory), and its eight warps select each token's experts with the
+// router's warp selection (route_select_warp: one warp per token, ties to
+// the lower index, the routing flags' weights).
+#include "route_select.cuh"
 #include "tc_common.cuh"
 
 namespace qsm {
@@ -33,14 +35,13 @@ constexpr int BK = 64;
 constexpr int kStages = 4;
 constexpr int kThreads = 256;
 constexpr int kMaxTopK = 8;
+constexpr int kMaxE = 256;
 
 struct Params {
   CUtensorMap xa;  // x [T, H] bf16, box {64, 128}
   CUtensorMap wb;  // split router weight [3E, H] bf16, box {64, E}
   const float* bias;
   int T, H, E, k, renorm, ntiles, ks;
-  float* part;          // partial logits [ks][T][E] fp32
-  unsigned* counters;   // [ntiles] arrival counters, zero between calls
   int32_t* topk_idx;
   float* topk_w;
   int32_t* status;
@@ -92,7 +93,7 @@ route_tc_kernel(const __grid_constant__ Params p) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag, is_last;
+  __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x / KS, q = blockIdx.x - tile * KS;
   if (threadIdx.x == 0) {
@@ -168,188 +169,72 @@ route_tc_kernel(const __grid_constant__ Params p) {
   } else if (warp >= 4) {
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;  // token row of the tile = TMEM lane
-    const int t = tile * BM + row;
     const bool ok = wait(&accf_bar, 0);
     tc::tc_fence_after();
-    // partial logits of this slice: the token's E values, 64 bytes at a time
+    // this slice's partial logits -> this CTA's shared memory [row][E + 4]
+    // (the pipeline stages are free: every MMA has completed)
     const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16);
-    float* prow = p.part + ((size_t)q * p.T + (t < p.T ? t : 0)) * p.E;
+    float* prow = reinterpret_cast<float*>(smem) + row * (p.E + 4);
     if (ok) {
       for (int c0 = 0; c0 < p.E; c0 += 16) {
         float v[16];
         tc::tmem_ld16(taddr + c0, v);
-        if (t < p.T) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            __stcg(reinterpret_cast<float4*>(prow + c0) + u,
-                   make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
-        }
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<float4*>(prow + c0 + 4 * u) =
+              make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
       }
     }
-    __threadfence();  // this thread's partial logits, before the arrival
   }
+  tc::tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // every slice of the tile is in its CTA's shared memory
 
-  // arrival: the last of the tile's ks CTAs selects the experts, one token
-  // per warp at a time
-  tc::tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(p.counters + tile, 1u);
-    is_last = prev == (unsigned)(KS - 1);
-    if (is_last) __threadfence();
+  // CTA q: tokens [q * rpc, (q + 1) * rpc) of the tile.  Their logits: the
+  // KS slices added in slice order (the bias is added at selection).  All
+  // slices of a position are read before its sum is written.
+  const int ld = p.E + 4;
+  const int rpc = BM / KS, r0 = q * rpc;
+  const int rows = min(BM, p.T - tile * BM);
+  const float* pl = reinterpret_cast<const float*>(smem);  // [BM][ld], every CTA
+  // the sums overwrite this CTA's own rows in place: the other CTAs read only
+  // the rows of their own token ranges from this CTA
+  float* lg = reinterpret_cast<float*>(smem) + r0 * ld;      // [rpc][ld]
+  const int e4 = p.E / 4;
+#pragma unroll 4
+  for (int pos = threadIdx.x; pos < rpc * e4; pos += kThreads) {
+    const int rr = pos / e4, c = pos - rr * e4;
+    const uint32_t off = smem_u32(pl + (r0 + rr) * ld + 4 * c);
+    float4 sl[KS];
+#pragma unroll
+    for (int s2 = 0; s2 < KS; ++s2) sl[s2] = dsmem_ld_f4(dsmem_addr_u32(off, s2));
+    float4 a = sl[0];
+#pragma unroll
+    for (int s2 = 1; s2 < KS; ++s2) {
+      a.x += sl[s2].x;
+      a.y += sl[s2].y;
+      a.z += sl[s2].z;
+      a.w += sl[s2].w;
+    }
+    *reinterpret_cast<float4*>(lg + rr * ld + 4 * c) = a;
   }
   __syncthreads();
-  if (is_last && !*abort_p) {
-    // the pipeline stages are free: the tile's logits go to shared memory,
-    // [row][E + 4] fp32 (the pad spreads a column over the banks)
-    float* lg = reinterpret_cast<float*>(smem);
-    const int ld = p.E + 4;
-    const int rows = min(BM, p.T - tile * BM);
-    const size_t pstride = (size_t)p.T * p.E;
-    const int e4 = p.E / 4;  // float4 columns
-    const int n4 = rows * e4;
-    // the slices in order (the bias is added at selection); 8 positions
-    // per thread in flight
-    for (int b0 = threadIdx.x; b0 < n4; b0 += kThreads * 8) {
-      float4 sl[8][KS];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int pos = b0 + u * kThreads;
-        if (pos < n4) {
-          const int r = pos / e4, c = pos - r * e4;
-          const float4* src = reinterpret_cast<const float4*>(
-                                  p.part + (size_t)(tile * BM + r) * p.E) + c;
-#pragma unroll
-          for (int s2 = 0; s2 < KS; ++s2)
-            sl[u][s2] = __ldcg(src + s2 * (pstride / 4));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int pos = b0 + u * kThreads;
-        if (pos < n4) {
-          const int r = pos / e4, c = pos - r * e4;
-          float4 a = sl[u][0];
-#pragma unroll
-          for (int s2 = 1; s2 < KS; ++s2) {
-            a.x += sl[u][s2].x;
-            a.y += sl[u][s2].y;
-            a.z += sl[u][s2].z;
-            a.w += sl[u][s2].w;
-          }
-          *reinterpret_cast<float4*>(lg + r * ld + 4 * c) = a;
-        }
+  // one warp per token: top k, routing weights
+  if (!*abort_p) {
+    for (int rr = warp; rr < rpc; rr += kThreads / 32) {
+      if (r0 + rr >= rows) break;
+      int my_e;
+      float my_l, my_w;
+      route_select_warp<kMaxE / 32, true>(lg + rr * ld, p.bias, p.E, p.k, p.renorm, p.status,
+                                          my_e, my_l, my_w);
+      const size_t t = (size_t)tile * BM + r0 + rr;
+      if (lane < p.k) {
+        p.topk_idx[t * p.k + lane] = my_e;
+        p.topk_w[t * p.k + lane] = my_w;
       }
     }
-    // the bias, after the tile (both fit in the free stage memory)
-    float* bsm = lg + BM * ld;
-    for (int c = threadIdx.x; c < p.E; c += kThreads) bsm[c] = p.bias ? __ldg(p.bias + c) : 0.f;
-    __syncthreads();
-    // one thread per token: the best kMaxTopK selection logits (logit +
-    // bias) in registers (value desc, index asc; indices arrive in
-    // ascending order, so an equal value never displaces); the weights use
-    // the same logits, or the ones without the bias (selection-only bias)
-    const bool renorm = (p.renorm & QSM_ROUTE_RENORMALIZE) != 0;
-    const bool sel_only = (p.renorm & QSM_ROUTE_BIAS_SELECT_ONLY) != 0 && p.bias;
-    const int r = threadIdx.x;
-    if (r < rows) {
-      const float* row = lg + r * ld;
-      float val[kMaxTopK];
-      int idx[kMaxTopK];
-#pragma unroll
-      for (int i = 0; i < kMaxTopK; ++i) {
-        val[i] = -INFINITY;
-        idx[i] = 0x7fffffff;
-      }
-      bool bad = false;
-      for (int c0 = 0; c0 < p.E; c0 += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(row + c0);
-        float l4[4] = {a.x, a.y, a.z, a.w};
-        if (p.bias) {
-          const float4 bb = *reinterpret_cast<const float4*>(bsm + c0);
-          l4[0] = a.x + bb.x;
-          l4[1] = a.y + bb.y;
-          l4[2] = a.z + bb.z;
-          l4[3] = a.w + bb.w;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float l = l4[c];
-          if (!isfinite(l)) {
-            bad = true;
-            l = -INFINITY;
-          }
-          int ci = c0 + c;
-          if (l > val[kMaxTopK - 1] || (l == val[kMaxTopK - 1] && ci < idx[kMaxTopK - 1])) {
-#pragma unroll
-            for (int i = 0; i < kMaxTopK; ++i) {
-              if (l > val[i] || (l == val[i] && ci < idx[i])) {
-                const float tv = val[i];
-                const int ti = idx[i];
-                val[i] = l;
-                idx[i] = ci;
-                l = tv;
-                ci = ti;
-              }
-            }
-          }
-        }
-      }
-      // weight logits of the selection, and the softmax's largest logit
-      float wl[kMaxTopK];
-#pragma unroll
-      for (int i = 0; i < kMaxTopK; ++i) {
-        wl[i] = val[i];
-        if (sel_only && i < p.k) {
-          wl[i] = row[idx[i]];
-          if (!isfinite(wl[i])) wl[i] = -INFINITY;
-        }
-      }
-      float top = -INFINITY;
-      float denom = 0.f;
-      if (renorm) {
-#pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i)
-          if (i < p.k) top = fmaxf(top, wl[i]);
-#pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i)
-          if (i < p.k) denom += __expf(wl[i] - top);
-      } else {
-        for (int pass = 0; pass < 2; ++pass) {
-          for (int c0 = 0; c0 < p.E; c0 += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(row + c0);
-            float l4[4] = {a.x, a.y, a.z, a.w};
-            if (p.bias && !sel_only) {
-              const float4 bb = *reinterpret_cast<const float4*>(bsm + c0);
-              l4[0] = a.x + bb.x;
-              l4[1] = a.y + bb.y;
-              l4[2] = a.z + bb.z;
-              l4[3] = a.w + bb.w;
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (!isfinite(l4[c])) continue;
-              if (pass == 0) top = fmaxf(top, l4[c]);
-              else denom += __expf(l4[c] - top);
-            }
-          }
-        }
-      }
-      const float inv = 1.0f / denom;
-      const size_t t = (size_t)tile * BM + r;
-#pragma unroll
-      for (int i = 0; i < kMaxTopK; ++i) {
-        if (i < p.k) {
-          p.topk_idx[t * p.k + i] = idx[i];
-          p.topk_w[t * p.k + i] = __expf(wl[i] - top) * inv;
-        }
-      }
-      if (bad) set_status(p.status, QSM_DEV_NONFINITE);
-    }
-    if (threadIdx.x == 0) p.counters[tile] = 0u;  // re-arm for the next call
   }
-  tc::tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while another still reads its slices
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, 256);
 }
@@ -373,12 +258,11 @@ int k_slices(int H) { return H % (4 * BK) == 0 ? 4 : (H % (2 * BK) == 0 ? 2 : 1)
 inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace route_tc
 
-// [arrival counters][split router weight 3*E*H bf16][partials ks*T*E fp32]
+// [256-byte header, zero][split router weight 3*E*H bf16]
 size_t route_tc_workspace_bytes(int T, int H, int E) {
   using namespace route_tc;
-  const size_t ntiles = (size_t)(T + BM - 1) / BM;
-  return up256(ntiles * 4) + up256((size_t)3 * E * H * 2) +
-         (size_t)k_slices(H) * T * E * 4;
+  (void)T;
+  return 256 + up256((size_t)3 * E * H * 2);
 }
 
 qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
@@ -390,9 +274,7 @@ qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
   const size_t n = (size_t)E * H;
   const int ntiles = (T + BM - 1) / BM;
   char* ws = static_cast<char*>(split_buf);
-  unsigned* counters = reinterpret_cast<unsigned*>(ws);
-  __nv_bfloat16* split = reinterpret_cast<__nv_bfloat16*>(ws + up256((size_t)ntiles * 4));
-  float* part = reinterpret_cast<float*>(ws + up256((size_t)ntiles * 4) + up256(n * 2 * 3));
+  __nv_bfloat16* split = reinterpret_cast<__nv_bfloat16*>(ws + 256);
   const int nsm = sm_count_route();
   QSM_CUDA_TRY(launch_pdl(split_kernel, dim3(nsm), dim3(256), 0, stream, w_router,
                           split, n));
@@ -410,8 +292,6 @@ qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
   p.renorm = renormalize;
   p.ntiles = ntiles;
   p.ks = k_slices(H);
-  p.part = part;
-  p.counters = counters;
   p.topk_idx = topk_idx;
   p.topk_w = topk_w;
   p.status = dev_status;
@@ -420,7 +300,9 @@ qsm_status route_tc_launch(const uint16_t* x, const float* w_router,
                          : (p.ks == 2 ? route_tc_kernel<2> : route_tc_kernel<1>);
   QSM_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem));
-  QSM_CUDA_TRY(launch_pdl(kern, dim3(ntiles * p.ks), dim3(kThreads), smem, stream, p));
+  // the ks CTAs of a tile are one cluster (they exchange their slices)
+  QSM_CUDA_TRY(
+      launch_pdl_cluster(kern, dim3(ntiles * p.ks), dim3(kThreads), p.ks, smem, stream, p));
   return QSM_OK;
 }
 

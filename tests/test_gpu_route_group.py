@@ -24,6 +24,10 @@ ROUTE_CASES = [
     (synth.QWEN, 300, None, False),          # tensor-core router, full softmax
     (synth.QWEN, 1000, "noise", True),
     (synth.QWEN, 4096, "noise", True),
+    # tensor-core router with 2 slices of H per tile (H % 256 != 0), a
+    # ragged last tile, and the full softmax
+    (synth.LayerShape(H=384, E=64, k=4, I=128), 200, None, True),
+    (synth.LayerShape(H=384, E=64, k=4, I=128), 129, None, False),
 ]
 
 
