@@ -493,16 +493,34 @@ class MoEForward:
         self.y_f32 = (torch.empty((T, H), dtype=torch.float32, device=device)
                       if want_f32 else None)
         self.dev_status = torch.zeros(1, **i32)
-
-    def __call__(self, x: torch.Tensor, stream=None) -> torch.Tensor:
-        L = self.layer
         if self.decode_ws is not None:
-            _check(lib().moe_decode_layer(
-                ctypes.byref(L.c), _p(_u16(x)), self.T, _p(L.w_router),
-                _p(L.logit_bias), self.renormalize, _p(self.topk_idx), _p(self.topk_w),
-                _p(self.y), _p(self.y_f32), _p(self.decode_ws), self.decode_ws.numel(),
-                _p(self.dev_status), _stream(stream)), "moe_decode_layer")
-            return self.y
+            # the one-launch call's arguments, marshalled once (per call only x,
+            # y and the stream change)
+            self._dl_fn = lib().moe_decode_layer
+            self._dl_head = (ctypes.byref(layer.c),)
+            self._dl_mid = (T, _p(layer.w_router), _p(layer.logit_bias), self.renormalize,
+                            _p(self.topk_idx), _p(self.topk_w))
+            self._dl_tail = (_p(self.y_f32), _p(self.decode_ws), self.decode_ws.numel(),
+                             _p(self.dev_status))
+
+    def __call__(self, x: torch.Tensor, stream=None, out=None) -> torch.Tensor:
+        """Run the layer on x [T, H] bf16; the result goes to out (a [T, H]
+        bf16 tensor, contiguous) when given, else to self.y.  Returns it."""
+        L = self.layer
+        y = self.y if out is None else out
+        if out is not None and (out.dtype != torch.bfloat16 or out.shape != self.y.shape
+                                or not out.is_contiguous()):
+            raise QSMError("MoEForward: out must be a contiguous [T, H] bf16 tensor")
+        if self.decode_ws is not None:
+            if x.dtype != torch.bfloat16 or not x.is_contiguous():
+                raise QSMError("MoEForward: x must be a contiguous bf16 tensor")
+            st = (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+            rc = self._dl_fn(*self._dl_head, ctypes.c_void_p(x.data_ptr()), *self._dl_mid,
+                             ctypes.c_void_p(y.data_ptr()), *self._dl_tail,
+                             ctypes.c_void_p(st))
+            if rc:
+                _check(rc, "moe_decode_layer")
+            return y
         fused = None
         if self.fuse_route_group and self.T <= 8:
             fused = moe_route_group(x, L.w_router, L.k, self.grouping,
@@ -517,9 +535,9 @@ class MoEForward:
             moe_group_tokens(self.topk_idx, L.E, self.grouping.tile_rows,
                              self.grouping, self.dev_status, stream)
         moe_ffn_forward(L, x, self.topk_idx, self.topk_w, self.grouping,
-                        self.y, self.y_f32 if self.y_f32 is not None else False,
+                        y, self.y_f32 if self.y_f32 is not None else False,
                         self.ffn_ws, self.dev_status, stream)
-        return self.y
+        return y
 
 
 def q8_quantize_x(x: torch.Tensor, qx=None, dx=None, dev_status=None, stream=None):

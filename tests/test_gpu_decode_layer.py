@@ -134,3 +134,22 @@ def test_decode_layer_barrier_timeout_is_reported(qsm):
     assert np.array_equal(idx.cpu().numpy(), idx_o)
     err, _ = check_layer_output(y, y32, x.cpu(), idx_o, w_o, q)
     assert err <= TOL
+
+
+@pytest.mark.parametrize("one_launch", [True, False])
+def test_moe_forward_out_argument(qsm, one_launch):
+    """MoEForward writes into a caller's tensor when given out= (both paths),
+    with the same bits as into its own buffer."""
+    shape = synth.QWEN
+    Lg, _, wr, bias = layer(shape, 0, None)
+    L = qsm.Layer.from_synth(Lg)
+    x = x_for(shape, 3, 31, Lg, wr, bias).cuda()
+    f = qsm.MoEForward(L, 3, one_launch=one_launch)
+    own = f(x).clone()
+    out = torch.empty((2, 3, shape.H), dtype=torch.bfloat16, device="cuda")
+    r = f(x, out=out[1])
+    torch.cuda.synchronize()
+    assert r.data_ptr() == out[1].data_ptr()
+    assert torch.equal(out[1], own)
+    with pytest.raises(qsm.QSMError):
+        f(x, out=torch.empty((3, shape.H), dtype=torch.float32, device="cuda"))
