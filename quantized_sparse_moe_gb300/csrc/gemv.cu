@@ -408,8 +408,9 @@ q8_gemv_tma_kernel(const __grid_constant__ CUtensorMap cmap,
 // weights in flight for the whole call instead of relaunching a CTA per tile.
 // The activation is staged once in shared memory (fp16, or the int8 codes
 // and block scales).  Two groups of eight consumer warps take alternate
-// tiles; in a group each warp takes one chain (half a segment) of a stage,
-// and a tile's chains and segments are added in the order above.
+// tiles (a tile of one stage) or alternate stages (a tile of several
+// stages); in a group each warp takes one chain (half a segment) of a
+// stage, and a tile's chains and segments are added in the order above.
 
 constexpr int kStreamS = 5;
 constexpr int kStreamSeg = 4;  // segments per stage
@@ -418,7 +419,7 @@ constexpr int kStreamGW = 2 * kStreamSeg;  // warps of a consumer group: one per
 constexpr int kStreamCW = 2 * kStreamGW;   // two groups, alternate tiles
 constexpr int kStreamWarps = kStreamCW + 1;
 
-template <bool kI8>
+template <bool kI8, bool kByTile>  // kByTile: one stage per tile (K <= 2048)
 __global__ void __launch_bounds__(kStreamWarps * 32, 1)
 q8_gemv_stream_kernel(const __grid_constant__ CUtensorMap cmap,
                       const __grid_constant__ CUtensorMap smap,
@@ -427,7 +428,9 @@ q8_gemv_stream_kernel(const __grid_constant__ CUtensorMap cmap,
                       uint16_t* __restrict__ y, int32_t* dev_status) {
   extern __shared__ unsigned char gemv_dyn[];
   __shared__ __align__(8) uint64_t full[kStreamS], empty[kStreamS];
-  __shared__ float red[2][2][kTmaMaxSeg][2][16];  // [group][tile parity][seg][chain][row]
+  // [buffer][tile parity][seg][chain][row]; buffer = the tile's group when
+  // tiles alternate, 0 when stages alternate
+  __shared__ float red[2][2][kTmaMaxSeg][2][16];
   __shared__ volatile int s_bad;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -502,27 +505,34 @@ q8_gemv_stream_kernel(const __grid_constant__ CUtensorMap cmap,
   const float* xd = kI8 ? reinterpret_cast<const float*>(xsm + K) : nullptr;
   const int grp = warp / kStreamGW, gw = warp % kStreamGW;
   const int sw = gw >> 1, half = gw & 1;  // segment of the stage, chain of the segment
+  constexpr bool by_tile = kByTile;       // groups alternate tiles, else stages
   for (int p = 0; p < total; ++p) {
     const int slot = p % kStreamS, i = p / nst, seg = (p % nst) * kStreamSeg + sw;
-    if ((i & 1) != grp) continue;  // the other group's tile
-    wait(&full[slot], (p / kStreamS) & 1);
-    const unsigned char* st = ring + slot * kStageBytes;
-    if (seg < nseg) {
-      float pg, ph;
-      chain_partial<kI8, true>(st + sw * kTmaSegBytes,
-                               st + kStreamSeg * kTmaSegBytes + sw * kTmaScaleBytes, xa, xd,
-                               seg * kSeg, K, half, g, q, pg, ph);
-      if (q == 0) {
-        red[grp][(i >> 1) & 1][seg][half][g] = pg;
-        red[grp][(i >> 1) & 1][seg][half][g + 8] = ph;
+    const int b = by_tile ? grp : 0, par = by_tile ? (i >> 1) & 1 : i & 1;
+    if (((by_tile ? i : p) & 1) == grp) {  // this group's stage
+      wait(&full[slot], (p / kStreamS) & 1);
+      const unsigned char* st = ring + slot * kStageBytes;
+      if (seg < nseg) {
+        float pg, ph;
+        chain_partial<kI8, true>(st + sw * kTmaSegBytes,
+                                 st + kStreamSeg * kTmaSegBytes + sw * kTmaScaleBytes, xa, xd,
+                                 seg * kSeg, K, half, g, q, pg, ph);
+        if (q == 0) {
+          red[b][par][seg][half][g] = pg;
+          red[b][par][seg][half][g + 8] = ph;
+        }
       }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
     }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&empty[slot]);
-    if (p % nst == nst - 1) {  // the tile's last stage: add its segments
-      asm volatile("barrier.sync %0, %1;" ::"r"(2 + grp), "r"(kStreamGW * 32) : "memory");
-      if (gw == 0 && lane < 16) {
-        const float(*rr)[2][16] = red[grp][(i >> 1) & 1];
+    if (p % nst == nst - 1 && (!by_tile || (i & 1) == grp)) {  // tile end: add its segments
+      // alternating tiles: the tile's group; alternating stages: both groups
+      if (by_tile)
+        asm volatile("barrier.sync %0, %1;" ::"r"(2 + grp), "r"(kStreamGW * 32) : "memory");
+      else
+        asm volatile("barrier.sync 1, %0;" ::"r"(nct) : "memory");
+      if (gw == 0 && lane < 16 && (by_tile || grp == 0)) {
+        const float(*rr)[2][16] = red[b][par];
         float sum = 0.f;
         for (int s2 = 0; s2 < nseg; ++s2) sum += rr[s2][0][lane] + rr[s2][1][lane];
         const int n = ((int)blockIdx.x + i * G) * 16 + lane;
@@ -558,17 +568,18 @@ bool launch_tma(const uint16_t* x, const int8_t* qx, const float* dx, const int8
   int nsm = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (nsm > 0 && tiles >= 8L * nsm && tiles < (1L << 30)) {  // persistent streaming
-    static bool attr[2] = {false, false};  // sized for K <= 16384
+  if (nsm > 0 && tiles >= 16 && tiles < (1L << 30)) {  // persistent streaming
+    static bool attr[2][2] = {{false, false}, {false, false}};  // sized for K <= 16384
     const size_t smem = 1024 + (size_t)kStreamS * kStageBytes + (size_t)K * 2;
-    if (!attr[kI8]) {
-      cudaFuncSetAttribute(q8_gemv_stream_kernel<kI8>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool by_tile = nseg <= kStreamSeg;  // one stage per tile
+    auto* kern = by_tile ? q8_gemv_stream_kernel<kI8, true> : q8_gemv_stream_kernel<kI8, false>;
+    if (!attr[kI8][by_tile]) {
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)(1024 + (size_t)kStreamS * kStageBytes + 16384 * 2));
-      attr[kI8] = true;
+      attr[kI8][by_tile] = true;
     }
-    *err = launch_pdl(q8_gemv_stream_kernel<kI8>, dim3(nsm), dim3(kStreamWarps * 32), smem,
-                      s, cmap, smap, x, qx, dx, N, K, (int)tiles, y, status);
+    *err = launch_pdl(kern, dim3(tiles < nsm ? (int)tiles : nsm), dim3(kStreamWarps * 32),
+                      smem, s, cmap, smap, x, qx, dx, N, K, (int)tiles, y, status);
     return true;
   }
   const int spc = gemv_tma_spc(tiles, nseg);
