@@ -22,6 +22,9 @@ CASES = [
     (synth.QWEN_A4, 8, 6, None, True),
     (synth.TINY, 1, 7, None, True),       # H = 256: 16 CTAs, E = 16, k = 2
     (synth.TINY, 8, 8, None, False),
+    # E > 256: 32 candidates per lane and 8 consumer warps; 32 experts per CTA
+    (synth.LayerShape(H=256, E=512, k=8, I=128), 2, 9, None, True),
+    (synth.LayerShape(H=256, E=512, k=8, I=128), 5, 10, None, False),
 ]
 
 
