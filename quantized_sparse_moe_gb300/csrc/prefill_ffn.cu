@@ -582,22 +582,34 @@ prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, in
   if (bad) set_status(status, QSM_DEV_FP16_RANGE);
 }
 
-// y = bf16(y_acc) (and the fp32 copy).
+// y = bf16(y_acc) (and the fp32 copy).  Four 16-byte loads per thread in
+// flight per step.
+__device__ __forceinline__ void finalize_one(float4 v, size_t i, uint16_t* __restrict__ y,
+                                             float* __restrict__ y32) {
+  const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+  const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
+  reinterpret_cast<uint2*>(y)[i] = make_uint2(lo, hi);
+  if (y32) reinterpret_cast<float4*>(y32)[i] = v;
+}
+
 __global__ void __launch_bounds__(256)
 finalize_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y,
                 float* __restrict__ y32, size_t n4) {
   pdl_wait();
   pdl_launch_dependents();
+  const float4* src = reinterpret_cast<const float4*>(yacc);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(yacc) + i);
-    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
-                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
-    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
-                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
-    reinterpret_cast<uint2*>(y)[i] = make_uint2(lo, hi);
-    if (y32) reinterpret_cast<float4*>(y32)[i] = v;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldcg(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) finalize_one(v[u], i + u * stride, y, y32);
   }
+  for (; i < n4; i += stride) finalize_one(__ldcg(src + i), i, y, y32);
 }
 
 // (code ring, token ring, dequantised ring) depths
@@ -749,7 +761,7 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   const qsm_status st = a4 ? launch_gemms<QSM_AFFINE4_G64>(p1, p2, stream)
                            : launch_gemms<QSM_Q8_0>(p1, p2, stream);
   if (st != QSM_OK) return st;
-  QSM_CUDA_TRY(launch_pdl(finalize_kernel, dim3(2 * nsm), dim3(256), 0, stream,
+  QSM_CUDA_TRY(launch_pdl(finalize_kernel, dim3(4 * nsm), dim3(256), 0, stream,
                           (const float*)yacc, y, y32, (size_t)T * H / 4));
   return QSM_OK;
 }
