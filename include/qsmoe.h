@@ -279,26 +279,30 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
                                      cudaStream_t stream);
 
 /* The whole layer for a few tokens (1 <= T <= 8) in one launch: router,
- * selection, gate_up + SwiGLU, down + combine, separated by two grid-wide
- * barriers instead of three dependent launches [Perplexity page, "Keeping
- * expert routing on the GPU", "Reducing intermediate and state traffic",
- * "Overlapping independent GPU work"].  Results: topk_idx and topk_w
+ * selection, gate_up + SwiGLU, down + combine, separated by a grid-wide
+ * exchange of call-tagged logits and by per-slot completion counters
+ * between gate_up and down, instead of three dependent launches
+ * [Perplexity page, "Keeping expert routing on the GPU", "Reducing
+ * intermediate and state traffic", "Overlapping independent GPU work"].  Results: topk_idx and topk_w
  * bit-identical to moe_route's; y the layer output as moe_ffn_forward
  * computes it (same arithmetic per product; the combine's fp32 additions in
  * another order).
  *   Arguments as for moe_layer_forward, without a chunk size.
  *   Supported: Q8_0 or affine-4 (all four weight planes alike), H % 256 ==
  *   0, H / 16 <= the device's SM count (one CTA per 16 output rows, all
- *   resident for the barriers), I % 128 == 0 (Q8_0) or % 256 == 0
+ *   resident for the logit exchange and the counters), I % 128 == 0 (Q8_0) or % 256 == 0
  *   (affine-4), E <= 1024, k <= 32; all pointers 16-byte aligned except
  *   topk_idx, topk_w, y, y_f32 and logit_bias (4 bytes).  Otherwise
  *   QSM_ERR_UNSUPPORTED (moe_layer_forward serves every shape).
  *   workspace  >= moe_decode_layer_workspace_bytes(L, T) bytes, zeros before
- *              its first use.  Its first 8 bytes count barrier arrivals
- *              across calls: the calls that share a workspace must have the
- *              same H, and after a QSM_DEV_TIMEOUT it must be zeroed again.
- * Every wait in the kernel is bounded: a barrier or copy that does not
- * complete sets QSM_DEV_TIMEOUT and the call's results are invalid. */
+ *              its first use.  Its first 8 bytes count calls (H / 16 per
+ *              call): the calls that share a workspace must have the same
+ *              H, and after a QSM_DEV_TIMEOUT it must be zeroed again.
+ *              Bytes 256..2311 hold two banks of 32-bit slot counters (a
+ *              call counts in one and zeroes the other).
+ * Every wait in the kernel is bounded: an exchange, counter or copy that
+ * does not complete sets QSM_DEV_TIMEOUT and the call's results are
+ * invalid. */
 QSM_API size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T);
 QSM_API qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x, int32_t T,
                                     const float* w_router, const float* logit_bias,
@@ -388,12 +392,12 @@ QSM_API uint64_t qsm_launch_count(void);
  * kernels, 2 = always the prefill kernels (when T allows).  Process-wide. */
 QSM_API qsm_status qsm_debug_force_path(int32_t mode);
 
-/* Test hook for the bounded waits: raise the targets of moe_decode_layer's
- * grid barriers by `skew` arrivals (0 = off, the default), so that no call
- * can complete them: every wait runs out, the kernel sets QSM_DEV_TIMEOUT
+/* Test hook for the bounded waits: make moe_decode_layer's logit exchange
+ * wait for a call tag `skew` ahead of the call's own (0 = off, the
+ * default), so that no call can complete it: every wait runs out, the kernel sets QSM_DEV_TIMEOUT
  * in *dev_status, finishes with invalid results and returns, and the
- * context stays usable.  The barrier counter stays consistent (every CTA
- * still arrives once per barrier).  Process-wide; skew in [0, 1024]. */
+ * context stays usable.  The call ticket stays consistent (every CTA still
+ * arrives once).  Process-wide; skew in [0, 1024]. */
 QSM_API qsm_status qsm_debug_barrier_skew(int32_t skew);
 
 #ifdef __cplusplus

@@ -435,7 +435,8 @@ def moe_decode_layer(layer: Layer, x: torch.Tensor, renormalize=True,
 
 
 def debug_barrier_skew(skew: int) -> None:
-    """Test hook: raise the decode layer's grid-barrier targets (0 = off)."""
+    """Test hook: the decode layer's logit exchange waits for a call tag
+    `skew` ahead of its own, so that every wait runs out (0 = off)."""
     _check(lib().qsm_debug_barrier_skew(int(skew)), "qsm_debug_barrier_skew")
 
 

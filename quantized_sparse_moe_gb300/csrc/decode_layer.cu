@@ -9,39 +9,53 @@
 // "Overlapping independent GPU work"; the fused [gate; up] rows of "oMLX MoE
 // gate/up 融合优化", section "融合原理".  The dependent launches of the
 // decode path (router + grouping, gate_up, down) become three phases of one
-// launch, separated by two grid-wide barriers.  No grouping is needed: every
-// CTA derives its work from the selection itself.
+// launch: a grid-wide barrier after the logits, and per-slot completion
+// counters between gate_up and down.  No grouping is needed: every CTA
+// derives its work from the selection itself.
 //
 //   A  CTA c computes the logits of its experts for the T tokens, with the
 //      arithmetic of moe_route (router rows fetched before the
-//      programmatic-launch wait), into the workspace.          grid barrier
-//   B  Every CTA selects each token's experts from the logits with the code
+//      programmatic-launch wait), into the workspace, tagged with the call.
+//   B  Every CTA waits for the tagged logits of all experts, selects each
+//      token's experts from them with the code
 //      of moe_route (ids and weights bit-identical to it), forms the sorted
 //      set U of selected experts and computes gate_up + SwiGLU for its
 //      tiles.  Tile tau = (slot, 8 intermediates): slot 0 is the shared
 //      expert, slot s >= 1 the s-th expert of U; a tile covers all T tokens
 //      (pairs that are not routed are computed and never read).  h goes to
-//      the workspace.                                           grid barrier
+//      the workspace, and the slot's counter counts the tile.
 //   C  CTA c computes rows 16c..16c+15 of y: for every slot, the down rows
 //      times the slot's h, times the token's weight for the slot's expert
 //      (the shared expert's gate, or 1; pairs with weight 0 are skipped),
-//      summed over the slots in a fixed order.
+//      summed over the slots in a fixed order.  The slots go a few at a
+//      time, each group as soon as the counters of its slots are complete,
+//      so a CTA with fewer tiles starts on the first slots while others
+//      still compute the last gate_up tiles.  (Placing groups between a
+//      CTA's own tiles, as soon as those it needs are done, made every group
+//      a grid-wide wait and was slower.)
 //
-// Weights stream through a two-slot shared-memory ring filled by TMA from
-// one producer thread: B tiles (gate and up halves of 8 rows, each one copy
-// of the 3D row view with the 128-byte swizzle) and then C items (the down
-// tiles of up to m slots, 16 rows each).  As soon as the selection is known
-// the producer requests into L2 every weight byte its CTA will read, so HBM
-// streams the whole layer at once and the ring mostly reads L2.  The shared
+// Weights stream through a shared-memory ring of up to five slots, filled
+// by TMA from one producer thread: B tiles (gate and up halves of 8 rows,
+// each one copy of the 3D row view with the 128-byte swizzle) and then C
+// items (the down tiles of up to m slots, 16 rows each).  As soon as the
+// selection is known the producer requests into L2 the weights of the next
+// ~320 KB of its sequence past the ring (all of them for a few tokens), so
+// HBM streams the layer at once and the ring mostly reads L2.  The shared
 // expert's first tile and its down rows are requested before the wait.
 //
-// The grid barriers need all G = H / 16 CTAs resident at once: G is at most
-// the SM count and a launch's CTAs are all running once the launch lets its
-// dependents start (every CTA triggers).  Every wait is bounded; when one
-// runs out the kernel sets QSM_DEV_TIMEOUT, keeps its control flow (later
-// waits are short), lets its own copies land and returns.  The barrier
-// counter is a 64-bit ticket in the workspace: calls that share a workspace
-// must use the same H, and a workspace is zeroed again after a timeout.
+// The logit exchange and the counters need all G = H / 16 CTAs resident at
+// once: G is at most the SM count and a launch's CTAs are all running once
+// the launch lets its dependents start (every CTA triggers).  Every wait is
+// bounded; when one runs out the kernel sets QSM_DEV_TIMEOUT, keeps its
+// control flow (later waits are short), lets its own copies land and
+// returns.  A 64-bit ticket in the workspace counts calls: every CTA adds 1
+// per call, so before its own arrival it reads (calls so far) * G plus the
+// arrivals of this call, and the call's tag is calls so far + 1 (calls that
+// share a workspace must use the same H).  A logit travels as one 64-bit
+// word (tag, value): a reader waits until every word of its token carries
+// this call's tag, which is the barrier and the data in one round trip.
+// The slot counters come in two banks: a call counts in bank tag & 1 and
+// zeroes the other one, which the previous call used.
 #include "gemv_core.cuh"
 #include "route_select.cuh"
 #include "tc_common.cuh"
@@ -64,6 +78,7 @@ constexpr float kHScale = 1.0f / 16.0f;
 constexpr float kHScaleInv = 16.0f;
 constexpr int kBarCons = 1;               // named barrier of the consumer warps
 constexpr uint32_t kShortWait = 1u << 10; // waits after a timeout
+constexpr int kMaxSlots = kMaxT * 32 + 1; // shared expert + up to T k experts
 
 struct Params {
   CUtensorMap gu, gu_sh;  // gate_up codes, 3D row views, box {128, 8, hb/128}
@@ -88,17 +103,17 @@ struct Params {
   int hb, hsb, ib, isb;   // code / scale bytes per gate_up row and per down row
   int m;                  // down tiles per C item
   int ns;                 // ring slots
-  int hall;               // all of h fits one shared-memory copy
   int slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off, wm_off;
-  unsigned long long* gbar;
-  float* logits;          // [T, E]
+  unsigned long long* gbar;  // call ticket: G arrivals per call
+  unsigned* scnt;         // [2][kMaxSlots] gate_up tiles counted per slot
+  unsigned long long* logits;  // [T, E] (call tag << 32) | logit bits
   __half* hbuf;           // [slots, T, I], h / 16
   int32_t* topk_idx;
   float* topk_w;
   uint16_t* y;
   float* y32;
   int32_t* status;
-  int skew;               // test hook: added to the barrier targets (0)
+  int skew;               // test hook: added to the awaited call tag (0)
 };
 
 // Barrier over n threads (a multiple of 32) of the CTA; the non-aligned form,
@@ -107,23 +122,66 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-// One thread per CTA: count this CTA's arrival (release: the CTA's earlier
-// writes, ordered before by a CTA barrier, become visible first) and wait
-// until the counter reaches `target`.  False when the wait ran out.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* ctr,
-                                             unsigned long long target, uint32_t iters) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until the counter reaches `target` (acquire).  False when the wait ran out.
+__device__ __forceinline__ bool counter_wait(const unsigned* ctr, unsigned target,
+                                             uint32_t iters) {
   for (uint32_t i = 0; i < iters; ++i) {
-    if ((long long)(ld_acquire_u64(ctr) - target) >= 0) return true;
+    if (ld_acquire_u32(ctr) >= target) return true;
     if (i > 64) __nanosleep(32);
   }
   return false;
+}
+
+// One warp: the E tagged logits of a token into dst (shared memory), once
+// every word carries tag `want`.  All loads of a pass are in flight together;
+// later passes reload only the words that were stale.  False when the wait
+// ran out (dst then holds whatever arrived).
+template <int kPer>
+__device__ __forceinline__ bool gather_tagged(const unsigned long long* src, float* dst, int E,
+                                              uint32_t want, uint32_t iters) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    v[i] = lane + 32 * i < E ? ld_relaxed_u64(src + lane + 32 * i) : 0ull;
+  uint32_t stale = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if ((uint32_t)(v[i] >> 32) == want) dst[e] = __uint_as_float((uint32_t)v[i]);
+      else stale |= 1u << i;
+    }
+  }
+  for (uint32_t n = 0; __any_sync(0xffffffffu, stale != 0); ++n) {
+    if (n >= iters) return false;
+    if (n > 16) __nanosleep(32);
+    for (uint32_t m = stale; m; m &= m - 1) {
+      const int i = __ffs(m) - 1, e = lane + 32 * i;
+      const unsigned long long w = ld_relaxed_u64(src + e);
+      if ((uint32_t)(w >> 32) == want) {
+        dst[e] = __uint_as_float((uint32_t)w);
+        stale &= ~(1u << i);
+      }
+    }
+  }
+  return true;
 }
 
 // 8 bytes at byte b (a multiple of 8) of 128-byte line `line`, 128-byte swizzle.
@@ -178,7 +236,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   constexpr int kSubs = kCW * 32 / kTPE;  // experts per router pass
   extern __shared__ unsigned char dl_dyn[];
   __shared__ __align__(8) uint64_t full[kMaxS], empty[kMaxS], hfull[2], hempty[2];
-  __shared__ __align__(8) uint64_t xbar, rdy, b2;
+  __shared__ __align__(8) uint64_t xbar, rdy;
   __shared__ float red[2][kCW][32][4];
   __shared__ float rsum[kSubs][kTPE / 32][kMaxT];
   __shared__ int sel_e[kMaxT][32];
@@ -186,6 +244,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   __shared__ unsigned bm[kMaxE / 32];
   __shared__ float sgv[kMaxT];
   __shared__ int s_nu;
+  __shared__ uint32_t s_tag;  // this call's tag
   __shared__ volatile int s_bad;  // a wait ran out: later waits are short
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -216,7 +275,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     }
     mbar_init(&xbar, 1);
     mbar_init(&rdy, 1);
-    mbar_init(&b2, 1);
     s_bad = 0;
     fence_mbar_init();
   }
@@ -233,6 +291,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   if (warp == kCW) {
     if (lane != 0) return;
     int nu = 0, nB = 0, items = 0;
+    const unsigned* bank = p.scnt;  // this call's slot counters
     auto expert_of_slot = [&](int s) { return s == 0 ? 0 : ulist[s - 1]; };
     // B tile tau -> ring buffer sb, barrier bar
     auto issue_b = [&](int tau, unsigned char* sb, uint64_t* bar) {
@@ -267,31 +326,53 @@ decode_layer_kernel(const __grid_constant__ Params p) {
                    16 * p.isb, bar);
       }
     };
+    // the same weights into L2 only
+    auto prefetch_b = [&](int tau) {
+      const int s = tau / tps, i0 = 8 * (tau % tps);
+      const int rg = (s == 0 ? 0 : expert_of_slot(s) * 2 * I) + i0, ru = rg + I;
+      const uint8_t* cd = s == 0 ? p.gush_c : p.gu_c;
+      const __half* sc = s == 0 ? p.gush_s : p.gu_s;
+      const __half* bi = s == 0 ? p.gush_b : p.gu_b;
+      bulk_prefetch_l2(cd + (size_t)rg * p.hb, 8 * p.hb);
+      bulk_prefetch_l2(cd + (size_t)ru * p.hb, 8 * p.hb);
+      bulk_prefetch_l2(sc + (size_t)rg * (p.hsb / 2), 8 * p.hsb);
+      bulk_prefetch_l2(sc + (size_t)ru * (p.hsb / 2), 8 * p.hsb);
+      if (QT != QSM_Q8_0) {
+        bulk_prefetch_l2(bi + (size_t)rg * (p.hsb / 2), 8 * p.hsb);
+        bulk_prefetch_l2(bi + (size_t)ru * (p.hsb / 2), 8 * p.hsb);
+      }
+    };
+    auto prefetch_c = [&](int it) {
+      const int cnt = min(p.m, nu + 1 - p.m * it);
+      for (int j = 0; j < cnt; ++j) {
+        const int s = p.m * it + j, r = down_row(s);
+        bulk_prefetch_l2((s == 0 ? p.dnsh_c : p.dn_c) + (size_t)r * p.ib, 16 * p.ib);
+        bulk_prefetch_l2((s == 0 ? p.dnsh_s : p.dn_s) + (size_t)r * (p.isb / 2), 16 * p.isb);
+        if (QT != QSM_Q8_0)
+          bulk_prefetch_l2((s == 0 ? p.dnsh_b : p.dn_b) + (size_t)r * (p.isb / 2),
+                           16 * p.isb);
+      }
+    };
     auto issue_pos = [&](int pos) {
       unsigned char* sb = ring + (pos % ns) * p.slot_bytes;
       if (pos < nB) issue_b(c + pos * G, sb, &full[pos % ns]);
       else issue_c(pos - nB, sb, &full[pos % ns]);
     };
-    bool b2_seen = false;
-    // h of C item `it` (or, with hall, of every slot at once)
+    // h of C item `it`, once every tile of its slots has been counted
     auto issue_h = [&](int it) {
-      if (!b2_seen) {
-        wait(&b2, 0);
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        b2_seen = true;
+      const int s0 = p.m * it, cnt = min(p.m, nu + 1 - s0);
+      for (int j = 0; j < cnt; ++j) {
+        if (!counter_wait(bank + s0 + j, (unsigned)tps, s_bad ? kShortWait : kWaitIters)) {
+          s_bad = 1;
+          set_status(p.status, QSM_DEV_TIMEOUT);
+        }
       }
-      if (p.hall) {
-        const uint32_t bytes = (uint32_t)(nu + 1) * T * I * 2;
-        mbar_arrive_expect_tx(&hfull[0], bytes);
-        bulk_g2s(hs, p.hbuf, bytes, &hfull[0]);
-        return items;
-      }
+      // h was written through the generic proxy; the bulk copy reads it
+      asm volatile("fence.proxy.async.global;" ::: "memory");
       if (it >= 2) wait(&hempty[it & 1], ((it >> 1) - 1) & 1);
-      const int cnt = min(p.m, nu + 1 - p.m * it);
       const uint32_t bytes = (uint32_t)cnt * T * I * 2;
       mbar_arrive_expect_tx(&hfull[it & 1], bytes);
-      bulk_g2s(hs + (it & 1) * p.hs_bytes, p.hbuf + (size_t)p.m * it * T * I, bytes,
-               &hfull[it & 1]);
+      bulk_g2s(hs + (it & 1) * p.hs_bytes, p.hbuf + (size_t)s0 * T * I, bytes, &hfull[it & 1]);
       return it + 1;
     };
 
@@ -320,26 +401,26 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     mbar_arrive_expect_tx(&xbar, (uint32_t)T * H * 2);
     bulk_g2s(ring + p.xs_off, p.x, T * H * 2, &xbar);
 
-    wait(&rdy, 0);  // the selection: s_nu, ulist
+    wait(&rdy, 0);  // the selection: s_nu, ulist (and s_tag)
     nu = s_nu;
+    bank = p.scnt + (s_tag & 1u) * kMaxSlots;
     const int NT = (nu + 1) * tps;
     nB = c < NT ? (NT - c + G - 1) / G : 0;
     items = (nu + 1 + p.m - 1) / p.m;
     const int total = nB + items;
     int pos = pre;
     for (; pos < total && pos < ns; ++pos) issue_pos(pos);
-    // the down tiles past the first fill -> L2 now (needed after barrier 2)
-    for (int it = ns > nB ? ns - nB : 0; it < items; ++it) {
-      const int cnt = min(p.m, nu + 1 - p.m * it);
-      for (int j = 0; j < cnt; ++j) {
-        const int s = p.m * it + j, r = down_row(s);
-        bulk_prefetch_l2((s == 0 ? p.dnsh_c : p.dn_c) + (size_t)r * p.ib, 16 * p.ib);
-        bulk_prefetch_l2((s == 0 ? p.dnsh_s : p.dn_s) + (size_t)r * (p.isb / 2), 16 * p.isb);
-        if (QT != QSM_Q8_0)
-          bulk_prefetch_l2((s == 0 ? p.dnsh_b : p.dn_b) + (size_t)r * (p.isb / 2),
-                           16 * p.isb);
+    // the positions past the first fill go to L2 now, up to a window of
+    // about 320 KB ahead of the ring (all of them for a few tokens)
+    const int win = max(2, 327680 / p.slot_bytes);
+    int fpos = pos;
+    auto prefetch_to = [&](int end) {
+      for (; fpos < total && fpos < end; ++fpos) {
+        if (fpos < nB) prefetch_b(c + fpos * G);
+        else prefetch_c(fpos - nB);
       }
-    }
+    };
+    prefetch_to(ns + win);
     int hi = 0;  // next C item whose h is copied
     for (; pos < total; ++pos) {
       // the slot's previous position must be consumed; if it was a C item,
@@ -349,6 +430,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
         while (hi <= prev - nB) hi = issue_h(hi);
       wait(&empty[pos % ns], ((pos / ns) - 1) & 1);
       issue_pos(pos);
+      prefetch_to(pos + 1 + win);
     }
     while (hi < items) hi = issue_h(hi);
     // normally every copy has been consumed; after a timeout, let the last
@@ -358,9 +440,8 @@ decode_layer_kernel(const __grid_constant__ Params p) {
         const int last = s + ((total - 1 - s) / ns) * ns;
         mbar_wait_bounded(&full[s], (last / ns) & 1, kWaitIters);
       }
-      const int nhb = p.hall ? 1 : 2;
-      for (int b = 0; b < nhb && b < items; ++b) {
-        const int last = p.hall ? 0 : b + ((items - 1 - b) / 2) * 2;
+      for (int b = 0; b < 2 && b < items; ++b) {
+        const int last = b + ((items - 1 - b) / 2) * 2;
         mbar_wait_bounded(&hfull[b], (last >> 1) & 1, kWaitIters);
       }
     }
@@ -374,12 +455,17 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   const int H4 = H / 4;
   pdl_wait();
   pdl_launch_dependents();
-  // barrier base: every earlier call on this workspace has completed, so the
-  // counter holds a multiple of G plus arrivals of this call.  The load is
-  // used only at barrier 1, so its latency hides behind phase A.
-  unsigned long long gread = 0;
-  if (tid == 0) gread = ld_acquire_u64(p.gbar);
+  // the call's tag: every earlier call on this workspace has completed, so
+  // before this CTA's arrival the ticket holds (calls so far) * G plus
+  // arrivals of this call
+  if (tid == 0) {
+    const unsigned long long t = ld_relaxed_u64(p.gbar);
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p.gbar) : "memory");
+    s_tag = (uint32_t)(t / (unsigned long long)G) + 1u;
+  }
   wait(&xbar, 0);  // router rows, x (and the shared-expert gate vector)
+  named_bar(kBarCons, kCW * 32);  // s_tag
+  const uint32_t tag = s_tag;
   for (int e0 = ea; e0 < eb; e0 += kSubs) {
     const int e = e0 + sub;
     const bool mine = e < eb;
@@ -431,7 +517,8 @@ decode_layer_kernel(const __grid_constant__ Params p) {
         float v = 0.f;
 #pragma unroll
         for (int wq = 0; wq < kTPE / 32; ++wq) v += rsum[s2][wq][i];
-        p.logits[(size_t)i * E + e2] = v;
+        st_relaxed_u64(p.logits + (size_t)i * E + e2,
+                       ((unsigned long long)tag << 32) | __float_as_uint(v));
       }
     }
     named_bar(kBarCons, kCW * 32);
@@ -448,23 +535,25 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     }
   }
 
-  // ---- grid barrier 1: all logits written
-  named_bar(kBarCons, kCW * 32);
-  const unsigned long long gbase = gread - gread % (unsigned long long)G;
-  if (tid == 0 &&
-      !grid_barrier(p.gbar, gbase + G + p.skew, s_bad ? kShortWait : kWaitIters)) {
-    s_bad = 1;
-    set_status(p.status, QSM_DEV_TIMEOUT);
-  }
-  __syncwarp();
-  named_bar(kBarCons, kCW * 32);
+  // the previous call's counters, zeroed for the next call
+  if (c == 0)
+    for (int i = tid; i < kMaxSlots; i += kCW * 32) p.scnt[((tag + 1u) & 1u) * kMaxSlots + i] = 0u;
 
   // ---- B: selection (one warp per token), the set U, weights per slot
+  // the logits go where the router rows were (phase A's last CTA barrier
+  // ordered every read of those before)
+  float* lsm = reinterpret_cast<float*>(ring + p.wr_off);  // [T][E]
   if (warp < T) {
+    if (!gather_tagged<kPer>(p.logits + (size_t)warp * E, lsm + (size_t)warp * E, E,
+                             tag + (uint32_t)p.skew, s_bad ? kShortWait : kWaitIters)) {
+      s_bad = 1;
+      set_status(p.status, QSM_DEV_TIMEOUT);
+    }
+    __syncwarp();
     int my_e;
     float my_l, my_w;
-    route_select_warp<kPer>(p.logits + (size_t)warp * E, p.bias, E, k, p.flags, p.status,
-                            my_e, my_l, my_w);
+    route_select_warp<kPer, true>(lsm + (size_t)warp * E, p.bias, E, k, p.flags, p.status,
+                                  my_e, my_l, my_w);
     if (lane < k) {
       sel_e[warp][lane] = my_e;
       sel_w[warp][lane] = my_w;
@@ -494,6 +583,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     if (lane == 31) s_nu = incl;
   }
   named_bar(kBarCons, kCW * 32);
+  if (tid == 0) tc::mbar_arrive(&rdy);  // the producer may start: s_nu, ulist
   const int nu = s_nu;
   for (int i = tid; i < (nu + 1) * T; i += kCW * 32) {
     const int s = i / T, t = i - s * T;
@@ -508,14 +598,15 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     wmat[i] = w;
   }
   named_bar(kBarCons, kCW * 32);
-  if (tid == 0) tc::mbar_arrive(&rdy);
 
   const int NT = (nu + 1) * tps;
   const int nB = c < NT ? (NT - c + G - 1) / G : 0;
 
-  // ---- B: gate_up + SwiGLU tiles
-  const int nch = H / 64;
+  const int items = (nu + 1 + p.m - 1) / p.m;
+  const int nch = H / 64, ich = I / 64;
   bool range_bad = false;
+  float yp[4] = {0.f, 0.f, 0.f, 0.f};
+  // ---- B: gate_up + SwiGLU tiles
   for (int j = 0; j < nB; ++j) {
     const int sl = j % ns;
     wait(&full[sl], (j / ns) & 1);
@@ -559,34 +650,24 @@ decode_layer_kernel(const __grid_constant__ Params p) {
           p.hbuf[((size_t)s * T + t) * I + i0 + g] = __float2half_rn(h);
         }
       }
+      // count the tile (release: the warp's h stores, ordered before by
+      // the warp barrier, become visible first)
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(
+                         p.scnt + (tag & 1u) * kMaxSlots + s)
+                     : "memory");
+      __syncwarp();  // converged before the next MMAs
     }
   }
-  if (range_bad) set_status(p.status, QSM_DEV_FP16_RANGE);
-
-  // ---- grid barrier 2: all h written
-  named_bar(kBarCons, kCW * 32);
-  if (tid == 0) {
-    if (!grid_barrier(p.gbar, gbase + 2ull * G + p.skew, s_bad ? kShortWait : kWaitIters)) {
-      s_bad = 1;
-      set_status(p.status, QSM_DEV_TIMEOUT);
-    }
-    tc::mbar_arrive(&b2);  // the producer may copy h
-  }
-  __syncwarp();  // warp 0 converges before its MMAs
-
   // ---- C: down rows n0..n0+15 of every slot, weighted per token
-  const int items = (nu + 1 + p.m - 1) / p.m;
-  const int ich = I / 64;
-  float yp[4] = {0.f, 0.f, 0.f, 0.f};
   for (int it = 0; it < items; ++it) {
     const int pos = nB + it, sl = pos % ns;
     wait(&full[sl], (pos / ns) & 1);
-    if (!p.hall) wait(&hfull[it & 1], (it >> 1) & 1);
-    else if (it == 0) wait(&hfull[0], 0);
     const unsigned char* sb = ring + sl * p.slot_bytes;
+    wait(&hfull[it & 1], (it >> 1) & 1);
     // h rows of the item's first slot
-    const __half* hb = reinterpret_cast<const __half*>(
-        p.hall ? hs + (size_t)p.m * it * T * I * 2 : hs + (it & 1) * p.hs_bytes);
+    const __half* hb = reinterpret_cast<const __half*>(hs + (it & 1) * p.hs_bytes);
     // the item's (slot, chunk) pairs, flattened and cut evenly over the warps
     const int cnt = min(p.m, nu + 1 - p.m * it);
     const int tot = cnt * ich, per = (tot + kCW - 1) / kCW;
@@ -624,19 +705,23 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     __syncwarp();
     if (lane == 0) {
       tc::mbar_arrive(&empty[sl]);
-      if (!p.hall) tc::mbar_arrive(&hempty[it & 1]);
+      tc::mbar_arrive(&hempty[it & 1]);
     }
+    __syncwarp();
   }
-  // per-warp partials, summed in warp order
+  if (range_bad) set_status(p.status, QSM_DEV_FP16_RANGE);
+  // per-warp partials, summed in warp order; in the half of `red` that the
+  // last gate_up tile did not use (warp 0 may still read that one)
+  const int rb = nB & 1;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) red[0][warp][lane][i] = yp[i];
+  for (int i = 0; i < 4; ++i) red[rb][warp][lane][i] = yp[i];
   named_bar(kBarCons, kCW * 32);
   if (tid < 16 * T) {
     const int r = tid & 15, t = tid >> 4;
     const int ln = 4 * (r & 7) + (t >> 1), ii = (r >= 8 ? 2 : 0) + (t & 1);
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) s += red[0][w][ln][ii];
+    for (int w = 0; w < kCW; ++w) s += red[rb][w][ln][ii];
     const size_t o = (size_t)t * H + n0 + r;
     p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
     if (p.y32) p.y32[o] = s;
@@ -661,7 +746,7 @@ int sm_count_dl() {
 constexpr size_t kSmemBudget = 227 * 1024 - 20 * 1024;
 
 struct Geo {
-  int hb, hsb, ib, isb, m, ns, hall, slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off,
+  int hb, hsb, ib, isb, m, ns, slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off,
       wm_off;
   size_t smem;
   int numax;
@@ -688,7 +773,6 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
   g.numax = T * k < E ? T * k : E;
   const int G = H / 16, epc = (E + G - 1) / G;
   // the deepest ring (then the largest C items) that fits
-  const size_t hall_bytes = (size_t)(g.numax + 1) * T * I * 2;
   const int mmax = (int)(g.slot_bytes / dtile) > 8 ? 8 : (int)(g.slot_bytes / dtile);
   bool fit = false;
   for (g.ns = kMaxS; g.ns >= 2 && !fit; --g.ns) {
@@ -698,11 +782,11 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
       off = up(off + (size_t)T * H * 2, 128);
       g.sg_off = (int)off;
       off = up(off + (L->shared_gate ? (size_t)H * 4 : 0), 128);
-      // the router rows (phase A) and the h copies (phase C) share a region
+      // the router rows (phase A: 4 ceil(E / G) H >= 64 E bytes), then the
+      // logits (4 T E <= 32 E bytes) and the h copies share a region
       g.wr_off = g.hs_off = (int)off;
       g.hs_bytes = (int)((size_t)g.m * T * I * 2);
-      g.hall = hall_bytes <= 32 * 1024 ? 1 : 0;
-      const size_t wr = (size_t)epc * H * 4, hsz = g.hall ? hall_bytes : 2 * (size_t)g.hs_bytes;
+      const size_t wr = (size_t)epc * H * 4, hsz = 2 * (size_t)g.hs_bytes;
       off = up(off + (wr > hsz ? wr : hsz), 128);
       g.ul_off = (int)off;
       off = up(off + (size_t)g.numax * 4, 16);
@@ -723,14 +807,19 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
 
 int g_barrier_skew = 0;  // qsm_debug_barrier_skew
 
+// The call ticket, then the two banks of slot counters (room for the most
+// slots of any T, so that their place does not depend on T), the tagged
+// logits and h.
+
 struct WsLayout {
-  size_t logits, hbuf, total;
+  size_t scnt, logits, hbuf, total;
 };
 
 WsLayout ws_layout(const qsm_moe_layer* L, int T, const Geo& g) {
   WsLayout w;
-  w.logits = 256;
-  w.hbuf = w.logits + up((size_t)T * L->E * 4, 256);
+  w.scnt = 256;
+  w.logits = w.scnt + up((size_t)2 * kMaxSlots * 4, 256);
+  w.hbuf = w.logits + up((size_t)T * L->E * 8, 256);
   w.total = w.hbuf + up((size_t)(g.numax + 1) * T * L->I * 2, 256);
   return w;
 }
@@ -835,7 +924,6 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.isb = g.isb;
   prm.m = g.m;
   prm.ns = g.ns;
-  prm.hall = g.hall;
   prm.slot_bytes = g.slot_bytes;
   prm.xs_off = g.xs_off;
   prm.sg_off = g.sg_off;
@@ -846,7 +934,8 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.wm_off = g.wm_off;
   char* ws = static_cast<char*>(workspace);
   prm.gbar = reinterpret_cast<unsigned long long*>(ws);
-  prm.logits = reinterpret_cast<float*>(ws + wl.logits);
+  prm.scnt = reinterpret_cast<unsigned*>(ws + wl.scnt);
+  prm.logits = reinterpret_cast<unsigned long long*>(ws + wl.logits);
   prm.hbuf = reinterpret_cast<__half*>(ws + wl.hbuf);
   prm.topk_idx = topk_idx;
   prm.topk_w = topk_w;

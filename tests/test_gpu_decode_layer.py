@@ -48,8 +48,10 @@ def test_decode_layer_matches_oracle(qsm, shape, T, seed, zipf, renorm):
 
 
 def test_decode_layer_repeat_on_one_workspace(qsm):
-    """Calls on one workspace give the same bits; each call adds two barrier
-    rounds of H / 16 arrivals to the ticket counter."""
+    """Calls on one workspace give the same bits; each call adds H / 16
+    arrivals to the call ticket, counts I / 8 tiles for each slot it uses
+    (the shared expert and the distinct selected experts) in the counter
+    bank of its tag's parity and zeroes the other bank."""
     shape = synth.QWEN
     Lg, _, wr, bias = layer(shape, 0, None)
     L = qsm.Layer.from_synth(Lg)
@@ -62,7 +64,27 @@ def test_decode_layer_repeat_on_one_workspace(qsm):
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert all(torch.equal(a, b) for a, b in zip(outs[0], o))
-    assert int(ws[:8].view(torch.int64).item()) == 3 * 2 * (shape.H // 16)
+    assert int(ws[:8].view(torch.int64).item()) == 3 * (shape.H // 16)
+    slots = 1 + len(set(idx.cpu().numpy().ravel().tolist()))
+    banks = ws[256:256 + 2 * 4 * 257].view(torch.int32).cpu().numpy().reshape(2, 257)
+    assert (banks[0] == 0).all()                  # the third call has tag 3
+    assert (banks[1, :slots] == shape.I // 8).all()
+    assert (banks[1, slots:] == 0).all()
+
+
+def test_decode_layer_workspace_shared_across_T(qsm):
+    """One workspace (sized for the largest T) serves calls of different T in
+    any order, with the bits of a fresh workspace per call."""
+    shape = synth.QWEN
+    Lg, _, wr, bias = layer(shape, 1, None)
+    L = qsm.Layer.from_synth(Lg)
+    ws = torch.zeros(qsm.decode_layer_workspace_bytes(L, 8), dtype=torch.uint8, device="cuda")
+    for T in (8, 1, 5, 1, 8, 3):
+        x = x_for(shape, T, 200 + T, Lg, wr, bias).cuda()
+        a = qsm.moe_decode_layer(L, x, y_f32=True, workspace=ws)
+        b = qsm.moe_decode_layer(L, x, y_f32=True)
+        torch.cuda.synchronize()
+        assert all(torch.equal(u, v) for u, v in zip(a, b)), T
 
 
 def test_decode_layer_all_tokens_on_same_experts(qsm):
@@ -113,8 +135,8 @@ def test_decode_layer_unsupported(qsm):
 
 
 def test_decode_layer_barrier_timeout_is_reported(qsm):
-    """A grid barrier that cannot complete (test hook: target raised by one)
-    makes every bounded wait run out: the call sets QSM_DEV_TIMEOUT and
+    """A logit exchange that cannot complete (test hook: the awaited call tag
+    raised by one) makes every bounded wait run out: the call sets QSM_DEV_TIMEOUT and
     returns; the context stays usable and the next call is exact."""
     shape = synth.TINY
     Lg, q, wr, bias = layer(shape, 7, None)
