@@ -289,15 +289,17 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
  * another order).
  *   Arguments as for moe_layer_forward, without a chunk size.
  *   Supported: Q8_0 or affine-4 (all four weight planes alike), H % 256 ==
- *   0, H / 16 <= the device's SM count (one CTA per 16 output rows, all
- *   resident for the logit exchange and the counters), I % 128 == 0 (Q8_0) or % 256 == 0
+ *   0, H / 16 <= the device's SM count (a CTA per SM, at least one per 16
+ *   output rows, all resident for the logit exchange and the counters),
+ *   I % 128 == 0 (Q8_0) or % 256 == 0
  *   (affine-4), E <= 1024, k <= 32; all pointers 16-byte aligned except
  *   topk_idx, topk_w, y, y_f32 and logit_bias (4 bytes).  Otherwise
  *   QSM_ERR_UNSUPPORTED (moe_layer_forward serves every shape).
  *   workspace  >= moe_decode_layer_workspace_bytes(L, T) bytes, zeros before
- *              its first use.  Its first 8 bytes count calls (H / 16 per
- *              call): the calls that share a workspace must have the same
- *              H, and after a QSM_DEV_TIMEOUT it must be zeroed again.
+ *              its first use.  Its first 8 bytes count calls (one arrival
+ *              per CTA): the calls that share a workspace must have the
+ *              same layer shape (H, I, E, k), and after a
+ *              QSM_DEV_TIMEOUT it must be zeroed again.
  *              Bytes 256..2311 hold two banks of 32-bit slot counters (a
  *              call counts in one and zeroes the other).
  * Every wait in the kernel is bounded: an exchange, counter or copy that

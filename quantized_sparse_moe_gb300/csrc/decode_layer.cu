@@ -24,10 +24,10 @@
 //      expert, slot s >= 1 the s-th expert of U; a tile covers all T tokens
 //      (pairs that are not routed are computed and never read).  h goes to
 //      the workspace, and the slot's counter counts the tile.
-//   C  CTA c computes rows 16c..16c+15 of y: for every slot, the down rows
-//      times the slot's h, times the token's weight for the slot's expert
-//      (the shared expert's gate, or 1; pairs with weight 0 are skipped),
-//      summed over the slots in a fixed order.  The slots go a few at a
+//   C  CTA c < H / 16 computes rows 16c..16c+15 of y: for every slot, the
+//      down rows times the slot's h, times the token's weight for the
+//      slot's expert (the shared expert's gate, or 1; pairs with weight 0
+//      are skipped), summed over the slots in a fixed order.  The slots go a few at a
 //      time, each group as soon as the counters of its slots are complete,
 //      so a CTA with fewer tiles starts on the first slots while others
 //      still compute the last gate_up tiles.  (Placing groups between a
@@ -43,19 +43,24 @@
 // HBM streams the layer at once and the ring mostly reads L2.  The shared
 // expert's first tile and its down rows are requested before the wait.
 //
-// The logit exchange and the counters need all G = H / 16 CTAs resident at
-// once: G is at most the SM count and a launch's CTAs are all running once
-// the launch lets its dependents start (every CTA triggers).  Every wait is
-// bounded; when one runs out the kernel sets QSM_DEV_TIMEOUT, keeps its
-// control flow (later waits are short), lets its own copies land and
-// returns.  A 64-bit ticket in the workspace counts calls: every CTA adds 1
-// per call, so before its own arrival it reads (calls so far) * G plus the
-// arrivals of this call, and the call's tag is calls so far + 1 (calls that
-// share a workspace must use the same H).  A logit travels as one 64-bit
-// word (tag, value): a reader waits until every word of its token carries
-// this call's tag, which is the barrier and the data in one round trip.
-// The slot counters come in two banks: a call counts in bank tag & 1 and
-// zeroes the other one, which the previous call used.
+// The grid has one CTA per SM (fewer when the layer has fewer gate_up
+// tiles): CTAs c < H / 16 also own rows of y, the others only gate_up tiles,
+// so that the tiles spread over every SM.  The logit exchange and the
+// counters need all G CTAs resident at once: G is at most the SM count and
+// a launch's CTAs are all running once the launch lets its dependents start
+// (every CTA triggers).  Every wait is bounded; when one runs out the kernel
+// sets QSM_DEV_TIMEOUT, keeps its control flow (later waits are short), lets
+// its own copies land and returns.  A 64-bit ticket in the workspace counts
+// calls: every CTA adds 1 per call, so before its own arrival it reads
+// (calls so far) * G plus the arrivals of this call, and the call's tag is
+// calls so far + 1 (calls that share a workspace must have the same layer
+// shape).  A logit travels as one 64-bit word (tag, value): a reader waits
+// until every word of its token carries this call's tag, which is the
+// barrier and the data in one round trip.  The slot counters come in two
+// banks: a call counts in bank tag & 1 and zeroes the other one, which the
+// previous call used.
+#include <algorithm>
+
 #include "gemv_core.cuh"
 #include "route_select.cuh"
 #include "tc_common.cuh"
@@ -100,13 +105,14 @@ struct Params {
   const float* bias;      // [E] or null
   const float* sgate;     // [H] or null
   int T, H, I, E, k, flags, G, epc;
+  int GC;                 // CTAs c < GC own rows 16c..16c+15 of y (GC = H / 16)
   int hb, hsb, ib, isb;   // code / scale bytes per gate_up row and per down row
   int m;                  // down tiles per C item
   int ns;                 // ring slots
   int slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off, wm_off;
   unsigned long long* gbar;  // call ticket: G arrivals per call
   unsigned* scnt;         // [2][kMaxSlots] gate_up tiles counted per slot
-  unsigned long long* logits;  // [T, E] (call tag << 32) | logit bits
+  unsigned long long* logits;  // [kMaxT, E] (call tag << 32) | logit bits
   __half* hbuf;           // [slots, T, I], h / 16
   int32_t* topk_idx;
   float* topk_w;
@@ -383,8 +389,10 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       issue_b(c + pre * G, ring + pre * p.slot_bytes, &full[pre]);
       ++pre;
     }
-    bulk_prefetch_l2(p.dnsh_c + (size_t)n0 * p.ib, 16 * p.ib);
-    bulk_prefetch_l2(p.dnsh_s + (size_t)n0 * (p.isb / 2), 16 * p.isb);
+    if (c < p.GC) {
+      bulk_prefetch_l2(p.dnsh_c + (size_t)n0 * p.ib, 16 * p.ib);
+      bulk_prefetch_l2(p.dnsh_s + (size_t)n0 * (p.isb / 2), 16 * p.isb);
+    }
     {  // this CTA's router rows; counted in xbar's phase without arriving
       const int ea = c * p.epc, ne = min(E, ea + p.epc) - ea;
       if (ne > 0) {
@@ -406,7 +414,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     bank = p.scnt + (s_tag & 1u) * kMaxSlots;
     const int NT = (nu + 1) * tps;
     nB = c < NT ? (NT - c + G - 1) / G : 0;
-    items = (nu + 1 + p.m - 1) / p.m;
+    items = c < p.GC ? (nu + 1 + p.m - 1) / p.m : 0;
     const int total = nB + items;
     int pos = pre;
     for (; pos < total && pos < ns; ++pos) issue_pos(pos);
@@ -510,13 +518,18 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       }
     }
     named_bar(kBarCons, kCW * 32);
+    // all kMaxT token rows carry this call's tag (rows i >= T the value
+    // 0), so that every word of the region holds the previous call's tag
+    // when a call starts: none can pass for the current one
     if (tid < kSubs * kMaxT) {
       const int s2 = tid / kMaxT, i = tid % kMaxT;
       const int e2 = e0 + s2;
-      if (e2 < eb && i < T) {
+      if (e2 < eb) {
         float v = 0.f;
+        if (i < T) {
 #pragma unroll
-        for (int wq = 0; wq < kTPE / 32; ++wq) v += rsum[s2][wq][i];
+          for (int wq = 0; wq < kTPE / 32; ++wq) v += rsum[s2][wq][i];
+        }
         st_relaxed_u64(p.logits + (size_t)i * E + e2,
                        ((unsigned long long)tag << 32) | __float_as_uint(v));
       }
@@ -602,7 +615,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   const int NT = (nu + 1) * tps;
   const int nB = c < NT ? (NT - c + G - 1) / G : 0;
 
-  const int items = (nu + 1 + p.m - 1) / p.m;
+  const int items = c < p.GC ? (nu + 1 + p.m - 1) / p.m : 0;  // C items (rows of y)
   const int nch = H / 64, ich = I / 64;
   bool range_bad = false;
   float yp[4] = {0.f, 0.f, 0.f, 0.f};
@@ -716,7 +729,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) red[rb][warp][lane][i] = yp[i];
   named_bar(kBarCons, kCW * 32);
-  if (tid < 16 * T) {
+  if (c < p.GC && tid < 16 * T) {
     const int r = tid & 15, t = tid >> 4;
     const int ln = 4 * (r & 7) + (t >> 1), ii = (r >= 8 ? 2 : 0) + (t & 1);
     float s = 0.f;
@@ -752,6 +765,15 @@ struct Geo {
   int numax;
 };
 
+// One CTA per SM, or as many as the most gate_up tiles a call of up to 8
+// tokens can have, but at least one per 16 rows of y.  Independent of T, so
+// that calls of any T share a workspace (the call tag divides by it).
+int grid_of(const qsm_moe_layer* L) {
+  const int numax = kMaxT * L->k < L->E ? kMaxT * L->k : L->E;
+  const int nt = (numax + 1) * (L->I / 8), gc = L->H / 16;
+  return std::max(gc, std::min(sm_count_dl(), nt));
+}
+
 bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
   const int qt = L->gate_up.qtype;
   const int H = L->H, I = L->I, E = L->E, k = L->k;
@@ -771,7 +793,7 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
   const size_t dtile = 16 * (size_t)g.ib + 16 * (size_t)g.isb * bi;
   g.slot_bytes = (int)up(btile > dtile ? btile : dtile, 1024);
   g.numax = T * k < E ? T * k : E;
-  const int G = H / 16, epc = (E + G - 1) / G;
+  const int G = grid_of(L), epc = (E + G - 1) / G;
   // the deepest ring (then the largest C items) that fits
   const int mmax = (int)(g.slot_bytes / dtile) > 8 ? 8 : (int)(g.slot_bytes / dtile);
   bool fit = false;
@@ -782,12 +804,12 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
       off = up(off + (size_t)T * H * 2, 128);
       g.sg_off = (int)off;
       off = up(off + (L->shared_gate ? (size_t)H * 4 : 0), 128);
-      // the router rows (phase A: 4 ceil(E / G) H >= 64 E bytes), then the
-      // logits (4 T E <= 32 E bytes) and the h copies share a region
+      // the router rows (phase A), then the logits and the h copies share
+      // a region
       g.wr_off = g.hs_off = (int)off;
       g.hs_bytes = (int)((size_t)g.m * T * I * 2);
-      const size_t wr = (size_t)epc * H * 4, hsz = 2 * (size_t)g.hs_bytes;
-      off = up(off + (wr > hsz ? wr : hsz), 128);
+      const size_t wr = (size_t)epc * H * 4, lg = (size_t)T * E * 4, hsz = 2 * (size_t)g.hs_bytes;
+      off = up(off + std::max(wr, std::max(lg, hsz)), 128);
       g.ul_off = (int)off;
       off = up(off + (size_t)g.numax * 4, 16);
       g.wm_off = (int)off;
@@ -807,9 +829,9 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
 
 int g_barrier_skew = 0;  // qsm_debug_barrier_skew
 
-// The call ticket, then the two banks of slot counters (room for the most
-// slots of any T, so that their place does not depend on T), the tagged
-// logits and h.
+// The call ticket, the two banks of slot counters and the tagged logits
+// (each sized for the largest T, so that their place does not depend on T
+// and the logit words never share bytes with h of another call), then h.
 
 struct WsLayout {
   size_t scnt, logits, hbuf, total;
@@ -819,7 +841,7 @@ WsLayout ws_layout(const qsm_moe_layer* L, int T, const Geo& g) {
   WsLayout w;
   w.scnt = 256;
   w.logits = w.scnt + up((size_t)2 * kMaxSlots * 4, 256);
-  w.hbuf = w.logits + up((size_t)T * L->E * 8, 256);
+  w.hbuf = w.logits + up((size_t)kMaxT * L->E * 8, 256);
   w.total = w.hbuf + up((size_t)(g.numax + 1) * T * L->I * 2, 256);
   return w;
 }
@@ -916,7 +938,8 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.E = E;
   prm.k = L->k;
   prm.flags = flags;
-  prm.G = H / 16;
+  prm.G = grid_of(L);
+  prm.GC = H / 16;
   prm.epc = (E + prm.G - 1) / prm.G;
   prm.hb = g.hb;
   prm.hsb = g.hsb;

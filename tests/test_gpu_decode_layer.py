@@ -48,8 +48,8 @@ def test_decode_layer_matches_oracle(qsm, shape, T, seed, zipf, renorm):
 
 
 def test_decode_layer_repeat_on_one_workspace(qsm):
-    """Calls on one workspace give the same bits; each call adds H / 16
-    arrivals to the call ticket, counts I / 8 tiles for each slot it uses
+    """Calls on one workspace give the same bits; each call adds one arrival
+    per CTA to the call ticket, counts I / 8 tiles for each slot it uses
     (the shared expert and the distinct selected experts) in the counter
     bank of its tag's parity and zeroes the other bank."""
     shape = synth.QWEN
@@ -64,7 +64,11 @@ def test_decode_layer_repeat_on_one_workspace(qsm):
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert all(torch.equal(a, b) for a, b in zip(outs[0], o))
-    assert int(ws[:8].view(torch.int64).item()) == 3 * (shape.H // 16)
+    # one arrival per CTA: a CTA per SM, at least H / 16, at most the tiles
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = (min(8 * shape.k, shape.E) + 1) * (shape.I // 8)  # of up to 8 tokens
+    G = max(shape.H // 16, min(sms, tiles))
+    assert int(ws[:8].view(torch.int64).item()) == 3 * G
     slots = 1 + len(set(idx.cpu().numpy().ravel().tolist()))
     banks = ws[256:256 + 2 * 4 * 257].view(torch.int32).cpu().numpy().reshape(2, 257)
     assert (banks[0] == 0).all()                  # the third call has tag 3
@@ -74,16 +78,21 @@ def test_decode_layer_repeat_on_one_workspace(qsm):
 
 def test_decode_layer_workspace_shared_across_T(qsm):
     """One workspace (sized for the largest T) serves calls of different T in
-    any order, with the bits of a fresh workspace per call."""
+    any order, with the bits of a fresh workspace per call.  (Leftover h of
+    a smaller call once sat where a larger call's tagged logits go: a stale
+    word that looked like the current call's tag changed one CTA's
+    selection.)"""
     shape = synth.QWEN
     Lg, _, wr, bias = layer(shape, 1, None)
     L = qsm.Layer.from_synth(Lg)
     ws = torch.zeros(qsm.decode_layer_workspace_bytes(L, 8), dtype=torch.uint8, device="cuda")
-    for T in (8, 1, 5, 1, 8, 3):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for T in (8, 1, 5, 1, 8, 3, 8, 2, 8):
         x = x_for(shape, T, 200 + T, Lg, wr, bias).cuda()
-        a = qsm.moe_decode_layer(L, x, y_f32=True, workspace=ws)
-        b = qsm.moe_decode_layer(L, x, y_f32=True)
+        a = qsm.moe_decode_layer(L, x, y_f32=True, workspace=ws, dev_status=st)
+        b = qsm.moe_decode_layer(L, x, y_f32=True, dev_status=st)
         torch.cuda.synchronize()
+        assert st.item() == 0, T
         assert all(torch.equal(u, v) for u, v in zip(a, b)), T
 
 
