@@ -82,6 +82,8 @@ constexpr int kWPer = 4;                  // float4 of a router row per thread a
 constexpr float kHScale = 1.0f / 16.0f;
 constexpr float kHScaleInv = 16.0f;
 constexpr int kBarCons = 1;               // named barrier of the consumer warps
+constexpr int kBarGrp = 2;                // + group: named barriers of the gate_up groups
+constexpr int kGW = 4;                    // warps per gate_up group
 constexpr uint32_t kShortWait = 1u << 10; // waits after a timeout
 constexpr int kMaxSlots = kMaxT * 32 + 1; // shared expert + up to T k experts
 
@@ -619,14 +621,28 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   const int nch = H / 64, ich = I / 64;
   bool range_bad = false;
   float yp[4] = {0.f, 0.f, 0.f, 0.f};
-  // ---- B: gate_up + SwiGLU tiles
+  // ---- B: gate_up + SwiGLU tiles.  The warps form groups of kGW; group gi
+  // owns the ring positions p with p % ngr == gi (gate_up tiles, then C
+  // items), so ngr of them are in flight at once.  A tile's kGW warps take
+  // nch / kGW chunks each and reduce behind the group's own named barrier.
+  // Every warp still waits for every position (and every h copy) in order
+  // and arrives on its empty barrier, the others right away: a ring slot's
+  // next phase then waits for all warps, and no warp waits on a phase two
+  // ahead of the barrier's (a parity wait would take that one as done).
+  constexpr int ngr = kCW / kGW;
+  const int gi = warp / kGW, wg = warp % kGW;
   for (int j = 0; j < nB; ++j) {
     const int sl = j % ns;
     wait(&full[sl], (j / ns) & 1);
+    if (j % ngr != gi) {
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[sl]);
+      continue;
+    }
     const unsigned char* sb = ring + sl * p.slot_bytes;
     const unsigned char* ss = sb + 16 * p.hb;  // gate scales, up scales (, biases)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int ch = warp; ch < nch; ch += kCW) {
+    for (int ch = wg; ch < nch; ch += kGW) {
       RawA r;
       load_tile_a<QT>(r, sb, sb + 8 * p.hb, 8, g, g, ss + g * p.hsb,
                       ss + 8 * p.hsb + g * p.hsb, ss + 16 * p.hsb + g * p.hsb,
@@ -641,16 +657,19 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&empty[sl]);
+    // the group's partials: buffer by the group's tile parity, so that the
+    // group's leader still reading the previous one is not overwritten
+    float (*gred)[32][4] = red[(j / ngr) & 1] + gi * kGW;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) red[j & 1][warp][lane][i] = acc[i];
-    named_bar(kBarCons, kCW * 32);
-    if (warp == 0) {
+    for (int i = 0; i < 4; ++i) gred[wg][lane][i] = acc[i];
+    named_bar(kBarGrp + gi, kGW * 32);
+    if (wg == 0) {
       float a[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) s += red[j & 1][w][lane][i];
+        for (int w = 0; w < kGW; ++w) s += gred[w][lane][i];
         a[i] = s;
       }
       const int tau = c + j * G, s = tau / tps, i0 = 8 * (tau % tps);
@@ -673,18 +692,27 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       __syncwarp();  // converged before the next MMAs
     }
   }
-  // ---- C: down rows n0..n0+15 of every slot, weighted per token
+  // ---- C: down rows n0..n0+15 of every slot, weighted per token; the
+  // group's own items, their (slot, chunk) pairs cut evenly over its warps
   for (int it = 0; it < items; ++it) {
     const int pos = nB + it, sl = pos % ns;
     wait(&full[sl], (pos / ns) & 1);
     const unsigned char* sb = ring + sl * p.slot_bytes;
     wait(&hfull[it & 1], (it >> 1) & 1);
+    if (pos % ngr != gi) {
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&empty[sl]);
+        tc::mbar_arrive(&hempty[it & 1]);
+      }
+      continue;
+    }
     // h rows of the item's first slot
     const __half* hb = reinterpret_cast<const __half*>(hs + (it & 1) * p.hs_bytes);
-    // the item's (slot, chunk) pairs, flattened and cut evenly over the warps
+    // the (slot, chunk) pairs of the item, flattened and cut over the group
     const int cnt = min(p.m, nu + 1 - p.m * it);
-    const int tot = cnt * ich, per = (tot + kCW - 1) / kCW;
-    const int lo = min(tot, warp * per), hi = min(tot, lo + per);
+    const int tot = cnt * ich, per = (tot + kGW - 1) / kGW;
+    const int lo = min(tot, wg * per), hi = min(tot, lo + per);
     for (int j = lo / ich; j * ich < hi; ++j) {
       const int s = p.m * it + j;
       const int c0 = max(lo, j * ich) - j * ich, c1 = min(hi, (j + 1) * ich) - j * ich;
@@ -723,18 +751,18 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     __syncwarp();
   }
   if (range_bad) set_status(p.status, QSM_DEV_FP16_RANGE);
-  // per-warp partials, summed in warp order; in the half of `red` that the
-  // last gate_up tile did not use (warp 0 may still read that one)
-  const int rb = nB & 1;
+  // per-warp partials, summed in warp order (after every group's leader has
+  // read its last gate_up partials)
+  named_bar(kBarCons, kCW * 32);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) red[rb][warp][lane][i] = yp[i];
+  for (int i = 0; i < 4; ++i) red[0][warp][lane][i] = yp[i];
   named_bar(kBarCons, kCW * 32);
   if (c < p.GC && tid < 16 * T) {
     const int r = tid & 15, t = tid >> 4;
     const int ln = 4 * (r & 7) + (t >> 1), ii = (r >= 8 ? 2 : 0) + (t & 1);
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) s += red[rb][w][ln][ii];
+    for (int w = 0; w < kCW; ++w) s += red[0][w][ln][ii];
     const size_t o = (size_t)t * H + n0 + r;
     p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
     if (p.y32) p.y32[o] = s;
