@@ -83,7 +83,7 @@ constexpr float kHScale = 1.0f / 16.0f;
 constexpr float kHScaleInv = 16.0f;
 constexpr int kBarCons = 1;               // named barrier of the consumer warps
 constexpr int kBarGrp = 2;                // + group: named barriers of the gate_up groups
-constexpr int kGW = 4;                    // warps per gate_up group
+constexpr int kGW = 8;                    // warps per gate_up group
 constexpr uint32_t kShortWait = 1u << 10; // waits after a timeout
 constexpr int kMaxSlots = kMaxT * 32 + 1; // shared expert + up to T k experts
 
