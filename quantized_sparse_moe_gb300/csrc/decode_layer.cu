@@ -324,6 +324,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     auto issue_c = [&](int it, unsigned char* sb, uint64_t* bar) {
       const int cnt = min(p.m, nu + 1 - p.m * it);
       mbar_arrive_expect_tx(bar, (uint32_t)cnt * (16u * p.ib + 16u * p.isb * kBi));
+#pragma unroll 1
       for (int j = 0; j < cnt; ++j) {
         const int s = p.m * it + j, r = down_row(s);
         tc::tma_load_3d(sb + j * 16 * p.ib, s == 0 ? &p.dn_sh : &p.dn, 0, r, 0, bar);
@@ -352,6 +353,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     };
     auto prefetch_c = [&](int it) {
       const int cnt = min(p.m, nu + 1 - p.m * it);
+#pragma unroll 1
       for (int j = 0; j < cnt; ++j) {
         const int s = p.m * it + j, r = down_row(s);
         bulk_prefetch_l2((s == 0 ? p.dnsh_c : p.dn_c) + (size_t)r * p.ib, 16 * p.ib);
@@ -369,6 +371,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     // h of C item `it`, once every tile of its slots has been counted
     auto issue_h = [&](int it) {
       const int s0 = p.m * it, cnt = min(p.m, nu + 1 - s0);
+#pragma unroll 1
       for (int j = 0; j < cnt; ++j) {
         if (!counter_wait(bank + s0 + j, (unsigned)tps, s_bad ? kShortWait : kWaitIters)) {
           s_bad = 1;
@@ -387,6 +390,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     // before the wait: static weights only (the shared expert's tiles at the
     // head of this CTA's sequence, its down rows, the shared-expert gate)
     int pre = 0;
+#pragma unroll 1
     while (pre < ns && c + pre * G < tps) {
       issue_b(c + pre * G, ring + pre * p.slot_bytes, &full[pre]);
       ++pre;
@@ -419,12 +423,14 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     items = c < p.GC ? (nu + 1 + p.m - 1) / p.m : 0;
     const int total = nB + items;
     int pos = pre;
+#pragma unroll 1
     for (; pos < total && pos < ns; ++pos) issue_pos(pos);
     // the positions past the first fill go to L2 now, up to a window of
     // about 320 KB ahead of the ring (all of them for a few tokens)
     const int win = max(2, 327680 / p.slot_bytes);
     int fpos = pos;
     auto prefetch_to = [&](int end) {
+#pragma unroll 1
       for (; fpos < total && fpos < end; ++fpos) {
         if (fpos < nB) prefetch_b(c + fpos * G);
         else prefetch_c(fpos - nB);
@@ -432,24 +438,29 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     };
     prefetch_to(ns + win);
     int hi = 0;  // next C item whose h is copied
+#pragma unroll 1
     for (; pos < total; ++pos) {
       // the slot's previous position must be consumed; if it was a C item,
       // its h has to be on its way first
       const int prev = pos - ns;
       if (prev >= nB)
+#pragma unroll 1
         while (hi <= prev - nB) hi = issue_h(hi);
       wait(&empty[pos % ns], ((pos / ns) - 1) & 1);
       issue_pos(pos);
       prefetch_to(pos + 1 + win);
     }
+#pragma unroll 1
     while (hi < items) hi = issue_h(hi);
     // normally every copy has been consumed; after a timeout, let the last
     // copy of each buffer land before the CTA's shared memory goes away
     if (s_bad) {
+#pragma unroll 1
       for (int s = 0; s < ns && s < total; ++s) {
         const int last = s + ((total - 1 - s) / ns) * ns;
         mbar_wait_bounded(&full[s], (last / ns) & 1, kWaitIters);
       }
+#pragma unroll 1
       for (int b = 0; b < 2 && b < items; ++b) {
         const int last = b + ((items - 1 - b) / 2) * 2;
         mbar_wait_bounded(&hfull[b], (last >> 1) & 1, kWaitIters);
@@ -480,44 +491,31 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     const int e = e0 + sub;
     const bool mine = e < eb;
     const float4* wrow = reinterpret_cast<const float4*>(wrs + (size_t)(mine ? e - ea : 0) * H);
-    float acc[kMaxT];
+    // one token at a time (a runtime loop: the kernel's code stays small);
+    // per token the products and sums in the order of moe_route
+#pragma unroll 1
+    for (int tt = 0; tt < T; ++tt) {
+      const uint2* xr = reinterpret_cast<const uint2*>(xs + (size_t)tt * H);
+      float a = 0.f;
+      for (int hb = 0; hb < H4; hb += kWPer * kTPE) {
+        float4 wv[kWPer];
+        uint2 xv[kWPer];
 #pragma unroll
-    for (int i = 0; i < kMaxT; ++i) acc[i] = 0.f;
-    for (int hb = 0; hb < H4; hb += kWPer * kTPE) {
-      float4 wv[kWPer];
+        for (int i = 0; i < kWPer; ++i) {
+          const int h4 = hb + st + i * kTPE;
+          wv[i] = (mine && h4 < H4) ? wrow[h4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          xv[i] = h4 < H4 ? xr[h4] : make_uint2(0u, 0u);
+        }
 #pragma unroll
-      for (int i = 0; i < kWPer; ++i) {
-        const int h4 = hb + st + i * kTPE;
-        wv[i] = (mine && h4 < H4) ? wrow[h4] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int tt = 0; tt < kMaxT; ++tt) {
-        if (tt < T) {
-          const uint2* xr = reinterpret_cast<const uint2*>(xs + (size_t)tt * H);
-          uint2 xv[kWPer];
-#pragma unroll
-          for (int i = 0; i < kWPer; ++i) {
-            const int h4 = hb + st + i * kTPE;
-            xv[i] = h4 < H4 ? xr[h4] : make_uint2(0u, 0u);
-          }
-          float a = acc[tt];
-#pragma unroll
-          for (int i = 0; i < kWPer; ++i) {
-            a = fmaf(wv[i].x, bf16_lo(xv[i].x), a);
-            a = fmaf(wv[i].y, bf16_hi(xv[i].x), a);
-            a = fmaf(wv[i].z, bf16_lo(xv[i].y), a);
-            a = fmaf(wv[i].w, bf16_hi(xv[i].y), a);
-          }
-          acc[tt] = a;
+        for (int i = 0; i < kWPer; ++i) {
+          a = fmaf(wv[i].x, bf16_lo(xv[i].x), a);
+          a = fmaf(wv[i].y, bf16_hi(xv[i].x), a);
+          a = fmaf(wv[i].z, bf16_lo(xv[i].y), a);
+          a = fmaf(wv[i].w, bf16_hi(xv[i].y), a);
         }
       }
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxT; ++i) {
-      if (i < T) {
-        const float s2 = warp_sum(acc[i]);
-        if (lane == 0) rsum[sub][st / 32][i] = s2;
-      }
+      const float s2 = warp_sum(a);
+      if (lane == 0) rsum[sub][st / 32][tt] = s2;
     }
     named_bar(kBarCons, kCW * 32);
     // all kMaxT token rows carry this call's tag (rows i >= T the value
@@ -721,7 +719,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       const unsigned char* bs = ss + p.m * 16 * p.isb;
       const __half* hr = hb + ((size_t)j * T + min(g, T - 1)) * I;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll 1
       for (int ch = c0; ch < c1; ++ch) {
         RawA r;
         load_tile_a<QT>(r, cd, cd, 16, g, g + 8, ss + g * p.isb, ss + (g + 8) * p.isb,
