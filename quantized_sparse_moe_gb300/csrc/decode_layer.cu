@@ -250,6 +250,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   __shared__ int sel_e[kMaxT][32];
   __shared__ float sel_w[kMaxT][32];
   __shared__ unsigned bm[kMaxE / 32];
+  __shared__ float szero[kPer * 32];  // the selection's warm-up input
   __shared__ float sgv[kMaxT];
   __shared__ int s_nu;
   __shared__ uint32_t s_tag;  // this call's tag
@@ -287,6 +288,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     fence_mbar_init();
   }
   for (int i = tid; i < kMaxE / 32; i += kThreads) bm[i] = 0u;
+  for (int i = tid; i < kPer * 32; i += kThreads) szero[i] = 0.f;
   __syncthreads();
 
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -556,18 +558,24 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   // the logits go where the router rows were (phase A's last CTA barrier
   // ordered every read of those before)
   float* lsm = reinterpret_cast<float*>(ring + p.wr_off);  // [T][E]
-  if (warp < T) {
-    if (!gather_tagged<kPer>(p.logits + (size_t)warp * E, lsm + (size_t)warp * E, E,
-                             tag + (uint32_t)p.skew, s_bad ? kShortWait : kWaitIters)) {
+  // Warps T..T+3 (one per scheduler) run the same selection code on a row
+  // of zeros while the token warps wait for the logits: the code is then in
+  // the instruction caches when the token warps reach it (every phase of
+  // this kernel runs once per launch, so its code is otherwise fetched
+  // cold).  Their results and status are dropped.
+  if (warp < min(kCW, T + 4)) {
+    const bool real = warp < T;
+    if (real && !gather_tagged<kPer>(p.logits + (size_t)warp * E, lsm + (size_t)warp * E, E,
+                                     tag + (uint32_t)p.skew, s_bad ? kShortWait : kWaitIters)) {
       s_bad = 1;
       set_status(p.status, QSM_DEV_TIMEOUT);
     }
     __syncwarp();
     int my_e;
     float my_l, my_w;
-    route_select_warp<kPer, true>(lsm + (size_t)warp * E, p.bias, E, k, p.flags, p.status,
-                                  my_e, my_l, my_w);
-    if (lane < k) {
+    route_select_warp<kPer, true>(real ? lsm + (size_t)warp * E : szero, p.bias, E, k, p.flags,
+                                  real ? p.status : nullptr, my_e, my_l, my_w);
+    if (real && lane < k) {
       sel_e[warp][lane] = my_e;
       sel_w[warp][lane] = my_w;
       if (c == 0) {
