@@ -9,30 +9,30 @@
 // "Overlapping independent GPU work"; the fused [gate; up] rows of "oMLX MoE
 // gate/up 融合优化", section "融合原理".  The dependent launches of the
 // decode path (router + grouping, gate_up, down) become three phases of one
-// launch: a grid-wide barrier after the logits, and per-slot completion
-// counters between gate_up and down.  No grouping is needed: every CTA
-// derives its work from the selection itself.
+// launch: an exchange of call-tagged logits after the router, and per-slot
+// completion counters between gate_up and down.  No grouping is needed:
+// every CTA derives its work from the selection itself.
 //
 //   A  CTA c computes the logits of its experts for the T tokens, with the
 //      arithmetic of moe_route (router rows fetched before the
 //      programmatic-launch wait), into the workspace, tagged with the call.
 //   B  Every CTA waits for the tagged logits of all experts, selects each
-//      token's experts from them with the code
-//      of moe_route (ids and weights bit-identical to it), forms the sorted
-//      set U of selected experts and computes gate_up + SwiGLU for its
-//      tiles.  Tile tau = (slot, 8 intermediates): slot 0 is the shared
-//      expert, slot s >= 1 the s-th expert of U; a tile covers all T tokens
-//      (pairs that are not routed are computed and never read).  h goes to
-//      the workspace, and the slot's counter counts the tile.
+//      token's experts from them with the code of moe_route (ids and
+//      weights bit-identical to it), forms the sorted set U of selected
+//      experts and computes gate_up + SwiGLU for its tiles.  Tile tau =
+//      (slot, 8 intermediates): slot 0 is the shared expert, slot s >= 1
+//      the s-th expert of U; a tile covers all T tokens (pairs that are not
+//      routed are computed and never read).  h goes to the workspace, and
+//      the slot's counter counts the tile.
 //   C  CTA c < H / 16 computes rows 16c..16c+15 of y: for every slot, the
 //      down rows times the slot's h, times the token's weight for the
 //      slot's expert (the shared expert's gate, or 1; pairs with weight 0
-//      are skipped), summed over the slots in a fixed order.  The slots go a few at a
-//      time, each group as soon as the counters of its slots are complete,
-//      so a CTA with fewer tiles starts on the first slots while others
-//      still compute the last gate_up tiles.  (Placing groups between a
-//      CTA's own tiles, as soon as those it needs are done, made every group
-//      a grid-wide wait and was slower.)
+//      are skipped), summed over the slots in a fixed order.  The slots go
+//      a few at a time (C items), each as soon as the counters of its slots
+//      are complete, so a CTA with fewer tiles starts on the first slots
+//      while others still compute the last gate_up tiles.  (Placing items
+//      between a CTA's own tiles, as soon as those they need are done, made
+//      every item a grid-wide wait and was slower.)
 //
 // Weights stream through a shared-memory ring of up to five slots, filled
 // by TMA from one producer thread: B tiles (gate and up halves of 8 rows,
@@ -41,7 +41,11 @@
 // selection is known the producer requests into L2 the weights of the next
 // ~320 KB of its sequence past the ring (all of them for a few tokens), so
 // HBM streams the layer at once and the ring mostly reads L2.  The shared
-// expert's first tile and its down rows are requested before the wait.
+// expert's first tile and its down rows are requested before the wait; x
+// is loaded by the consumer threads themselves (through L2: the previous
+// launch wrote it), which is quicker than a bulk copy's round trip.
+// The consumer warps form two groups that take alternate ring positions,
+// so two tiles (or items) are in flight at once.
 //
 // The grid has one CTA per SM (fewer when the layer has fewer gate_up
 // tiles): CTAs c < H / 16 also own rows of y, the others only gate_up tiles,
@@ -59,6 +63,10 @@
 // barrier and the data in one round trip.  The slot counters come in two
 // banks: a call counts in bank tag & 1 and zeroes the other one, which the
 // previous call used.
+//
+// Every phase runs once per launch, so the code is fetched cold each time:
+// loops that run once are not unrolled, and the selection's code is warmed
+// by idle warps while the token warps wait for the logits.
 #include <algorithm>
 
 #include "gemv_core.cuh"
@@ -414,8 +422,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     }
     pdl_wait();
     pdl_launch_dependents();
-    mbar_arrive_expect_tx(&xbar, (uint32_t)T * H * 2);
-    bulk_g2s(ring + p.xs_off, p.x, T * H * 2, &xbar);
+    tc::mbar_arrive(&xbar);  // x: the consumers load it
 
     wait(&rdy, 0);  // the selection: s_nu, ulist (and s_tag)
     nu = s_nu;
@@ -486,7 +493,12 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], 1;" ::"l"(p.gbar) : "memory");
     s_tag = (uint32_t)(t / (unsigned long long)G) + 1u;
   }
-  wait(&xbar, 0);  // router rows, x (and the shared-expert gate vector)
+  {  // x into shared memory through L2 (the previous launch wrote it)
+    const uint4* src = reinterpret_cast<const uint4*>(p.x);
+    uint4* dst = reinterpret_cast<uint4*>(ring + p.xs_off);
+    for (int i = tid; i < T * H / 8; i += kCW * 32) dst[i] = __ldcg(src + i);
+  }
+  wait(&xbar, 0);  // router rows (and the shared-expert gate vector)
   named_bar(kBarCons, kCW * 32);  // s_tag
   const uint32_t tag = s_tag;
   for (int e0 = ea; e0 < eb; e0 += kSubs) {
