@@ -74,9 +74,10 @@ typedef enum {
 #define QSM_DEV_BAD_EXPERT_ID 1 /* topk_idx entry outside [0, E) */
 #define QSM_DEV_NONFINITE 2     /* non-finite router logit */
 #define QSM_DEV_FP16_RANGE 4    /* a value staged in fp16 overflowed */
-#define QSM_DEV_TIMEOUT 8       /* a bounded wait (on a copy, or a grid
-                                   barrier of moe_decode_layer) ran out: the
-                                   kernel returned, its results are invalid */
+#define QSM_DEV_TIMEOUT 8       /* a bounded wait (on a copy, or on the
+                                   logit exchange or a slot counter of
+                                   moe_decode_layer) ran out: the kernel
+                                   returned, its results are invalid */
 
 typedef enum { QSM_Q8_0 = 0, QSM_AFFINE4_G64 = 1 } qsm_qtype;
 
