@@ -595,14 +595,34 @@ decode_layer_kernel(const __grid_constant__ Params p) {
         p.topk_w[(size_t)warp * k + lane] = my_w;
       }
     }
+    if (T == 1 && warp == 0) {
+      // one token: its k experts are distinct; the warp ranks them, writes
+      // the sorted set, the slot weights and the count, and lets the
+      // producer start (no bitmap, no scan, no CTA barriers)
+      int rank = 0;
+      for (int j = 0; j < k; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, my_e, j);
+        rank += ej < my_e ? 1 : 0;
+      }
+      if (lane < k) {
+        ulist[rank] = my_e;
+        wmat[rank + 1] = my_w;
+      }
+      if (lane == 0) {
+        wmat[0] = p.sgate ? sgv[0] : 1.f;
+        s_nu = k;
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&rdy);  // the producer may start: s_nu, ulist
+    }
   }
   named_bar(kBarCons, kCW * 32);
-  if (tid < T * k) {
+  if (T > 1 && tid < T * k) {
     const int e = sel_e[tid / k][tid % k];
     atomicOr(&bm[e >> 5], 1u << (e & 31));
   }
-  named_bar(kBarCons, kCW * 32);
-  if (warp == 0) {  // sorted distinct ids: prefix popcounts of the bitmap
+  if (T > 1) named_bar(kBarCons, kCW * 32);
+  if (T > 1 && warp == 0) {  // sorted distinct ids: prefix popcounts of the bitmap
     const unsigned word = lane < (E + 31) / 32 ? bm[lane] : 0u;
     const int cnt = __popc(word);
     int incl = cnt;
@@ -615,10 +635,12 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     for (unsigned w = word; w; w &= w - 1) ulist[pos++] = 32 * lane + (__ffs(w) - 1);
     if (lane == 31) s_nu = incl;
   }
-  named_bar(kBarCons, kCW * 32);
-  if (tid == 0) tc::mbar_arrive(&rdy);  // the producer may start: s_nu, ulist
+  if (T > 1) {
+    named_bar(kBarCons, kCW * 32);
+    if (tid == 0) tc::mbar_arrive(&rdy);  // the producer may start: s_nu, ulist
+  }
   const int nu = s_nu;
-  for (int i = tid; i < (nu + 1) * T; i += kCW * 32) {
+  for (int i = tid; T > 1 && i < (nu + 1) * T; i += kCW * 32) {
     const int s = i / T, t = i - s * T;
     float w = 0.f;
     if (s == 0) {
@@ -630,7 +652,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     }
     wmat[i] = w;
   }
-  named_bar(kBarCons, kCW * 32);
+  if (T > 1) named_bar(kBarCons, kCW * 32);
 
   const int NT = (nu + 1) * tps;
   const int nB = c < NT ? (NT - c + G - 1) / G : 0;
