@@ -206,14 +206,6 @@ __device__ __forceinline__ uint2 lds_sw(const unsigned char* t, int line, int b)
       t + line * 128 + ((((b >> 4) ^ (line & 7)) << 4) | (b & 15)));
 }
 
-// Ask L2 for `bytes` from `base`, one 128-byte line per thread and step.
-__device__ __forceinline__ void prefetch_lines(const void* base, uint32_t bytes, int t,
-                                               int nt) {
-  const char* b = static_cast<const char*>(base);
-  for (uint32_t off = (uint32_t)t * 128u; off < bytes; off += (uint32_t)nt * 128u)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(b + off));
-}
-
 // Raw A fragment of the 64-chunk ch of a tile whose rows g / g + 8 are lines
 // lg / lh (+ 128-byte chunk index x rows per chunk) of `codes`, with scales
 // (and biases) as fp16 rows of `spitch` bytes.
