@@ -577,8 +577,15 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     __syncwarp();
     int my_e;
     float my_l, my_w;
-    route_select_warp<kPer, true>(real ? lsm + (size_t)warp * E : szero, p.bias, E, k, p.flags,
-                                  real ? p.status : nullptr, my_e, my_l, my_w);
+    // the common shape (all 32 kPer candidates, top 8) with its sizes known
+    // to the compiler: the rounds unroll and the bounds checks fold away
+    const float* lrow = real ? lsm + (size_t)warp * E : szero;
+    if (E == 32 * kPer && k == 8)
+      route_select_warp<kPer, true>(lrow, p.bias, 32 * kPer, 8, p.flags,
+                                    real ? p.status : nullptr, my_e, my_l, my_w);
+    else
+      route_select_warp<kPer, true>(lrow, p.bias, E, k, p.flags, real ? p.status : nullptr,
+                                    my_e, my_l, my_w);
     if (real && lane < k) {
       sel_e[warp][lane] = my_e;
       sel_w[warp][lane] = my_w;
