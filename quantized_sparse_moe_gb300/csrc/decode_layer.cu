@@ -681,7 +681,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     const unsigned char* sb = ring + sl * p.slot_bytes;
     const unsigned char* ss = sb + 16 * p.hb;  // gate scales, up scales (, biases)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int ch = wg; ch < nch; ch += kGW) {
+    auto chunk = [&](int ch) {
       RawA r;
       load_tile_a<QT>(r, sb, sb + 8 * p.hb, 8, g, g, ss + g * p.hsb,
                       ss + 8 * p.hsb + g * p.hsb, ss + 16 * p.hsb + g * p.hsb,
@@ -693,6 +693,12 @@ decode_layer_kernel(const __grid_constant__ Params p) {
         X1 = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(xr + b_off1<QT>(q)));
       }
       chunk_mma<QT>(acc, r, X0, X1);
+    };
+    if (nch == 4 * kGW) {  // H = 2048: four chunks per warp, unrolled
+#pragma unroll
+      for (int u = 0; u < 4; ++u) chunk(wg + u * kGW);
+    } else {
+      for (int ch = wg; ch < nch; ch += kGW) chunk(ch);
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&empty[sl]);
