@@ -766,8 +766,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       const unsigned char* bs = ss + p.m * 16 * p.isb;
       const __half* hr = hb + ((size_t)j * T + min(g, T - 1)) * I;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int ch = c0; ch < c1; ++ch) {
+      auto dchunk = [&](int ch) {
         RawA r;
         load_tile_a<QT>(r, cd, cd, 16, g, g + 8, ss + g * p.isb, ss + (g + 8) * p.isb,
                         bs + g * p.isb, bs + (g + 8) * p.isb, ch, q);
@@ -777,6 +776,13 @@ decode_layer_kernel(const __grid_constant__ Params p) {
           X1 = *reinterpret_cast<const uint4*>(hr + 64 * ch + b_off1<QT>(q));
         }
         chunk_mma<QT>(acc, r, X0, X1);
+      };
+      if (c1 - c0 == 4) {  // the common share: four chunks of one slot, unrolled
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dchunk(c0 + u);
+      } else {
+#pragma unroll 1
+        for (int ch = c0; ch < c1; ++ch) dchunk(ch);
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
