@@ -64,9 +64,12 @@
 // banks: a call counts in bank tag & 1 and zeroes the other one, which the
 // previous call used.
 //
-// Every phase runs once per launch, so the code is fetched cold each time:
-// loops that run once are not unrolled, and the selection's code is warmed
-// by idle warps while the token warps wait for the logits.
+// Every phase runs once per launch, so code size matters: loops that run
+// once are not unrolled, and the selection's code is warmed by idle warps
+// while the token warps wait for the logits.  The hottest pieces have a
+// second copy for the common shape (the selection for all 32 kPer
+// candidates and top 8, the chunk loops for H = 2048 and for four chunks of
+// a down slot), with the same arithmetic in the same order.
 #include <algorithm>
 
 #include "gemv_core.cuh"
