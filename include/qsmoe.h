@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define QSM_ABI_VERSION 3
+#define QSM_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define QSM_API __attribute__((visibility("default")))
@@ -307,6 +307,21 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
  * does not complete sets QSM_DEV_TIMEOUT and the call's results are
  * invalid. */
 QSM_API size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T);
+
+/* The check moe_decode_layer makes before it launches, with the device's
+ * figures passed in: 1 when the layer and T are supported on a device of
+ * `sm_count` SMs and the kernel's whole grid (one CTA per SM, at least one
+ * per 16 rows of y) can be resident at once with `blocks_per_sm` CTAs per
+ * SM, else 0.  moe_decode_layer takes sm_count from the current device and
+ * blocks_per_sm from the occupancy calculator at the call's shared-memory
+ * size; when the check fails it returns QSM_ERR_UNSUPPORTED (and
+ * moe_decode_layer_workspace_bytes returns 0), so that callers take the
+ * route / group / FFN launches instead.  The check cannot see SMs that other
+ * work holds while the kernel runs (another stream, MPS limits): there the
+ * bounded waits run out and the call reports QSM_DEV_TIMEOUT with invalid
+ * results.  Pure host logic; needs no GPU. */
+QSM_API int32_t qsm_decode_layer_fits(const qsm_moe_layer* L, int32_t T, int32_t sm_count,
+                                      int32_t blocks_per_sm);
 QSM_API qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x, int32_t T,
                                     const float* w_router, const float* logit_bias,
                                     int32_t flags, int32_t* topk_idx, float* topk_w,
@@ -323,16 +338,21 @@ QSM_API qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x, i
  *   Arguments and results are those of moe_ffn_forward.  The scratch comes
  *   from an array inside the library (1 MiB per device, held by every GPU
  *   that loads the library until the process exits), so T must be <= 64 and
- *   the layer's decode scratch (moe_ffn_workspace_bytes(L, T): h, (T*k + T)
- *   * I * 2 bytes, and T fp32 shared-expert gates) must fit in 1 MiB;
- *   otherwise QSM_ERR_UNSUPPORTED is returned and nothing is enqueued.
- *   The call allocates nothing.  The first call on each device looks up that
- *   device's copy of the array (make the stream's device current); make that
- *   first call before any stream capture.  All calls on a device share the
- *   one array and it keeps the last call's contents (no value has to start
- *   at zero); calls whose work overlaps on the GPU (different streams, or
- *   different threads without ordering) race on it and must be serialised
- *   by the caller. */
+ *   the scratch that moe_ffn_forward would need for this call
+ *   (moe_ffn_workspace_bytes(L, T) on the path in force: the decode path's
+ *   h, (T*k + T) * I * 2 bytes, and T fp32 shared-expert gates) must fit in
+ *   1 MiB; otherwise QSM_ERR_UNSUPPORTED is returned and nothing is
+ *   enqueued.  T < 0 is QSM_ERR_INVALID_ARGUMENT; T == 0 enqueues nothing.
+ *   The call allocates nothing.  `stream` must belong to the current
+ *   device (else QSM_ERR_INVALID_ARGUMENT): the scratch used is that
+ *   device's copy.  The first call on each device looks up that device's
+ *   copy of the array; make that first call before any stream capture.  The
+ *   address found stays in use for the life of the device's context: calls
+ *   after cudaDeviceReset are not supported.  All calls on a device share
+ *   the one array and it keeps the last call's contents (no value has to
+ *   start at zero); calls whose work overlaps on the GPU (different
+ *   streams, or different threads without ordering) race on it and must be
+ *   serialised by the caller. */
 QSM_API qsm_status moe_ffn_forward_noalloc(const qsm_moe_layer* L,
                                            const uint16_t* x, int32_t T,
                                            const int32_t* topk_idx,
@@ -402,6 +422,24 @@ QSM_API qsm_status qsm_debug_force_path(int32_t mode);
  * context stays usable.  The call ticket stays consistent (every CTA still
  * arrives once).  Process-wide; skew in [0, 1024]. */
 QSM_API qsm_status qsm_debug_barrier_skew(int32_t skew);
+
+/* Test hook for the per-row identity of the fused gate_up projection
+ * ("oMLX MoE gate/up 融合优化", "融合原理": the rows of the [gate; up]
+ * concatenation come out bit-identical to separate gate and up
+ * projections).  With buf set (a device buffer of n_floats fp32), every
+ * kernel that computes gate_up also writes, before SwiGLU, the fp32 gate
+ * value of intermediate i to buf[row * 2I + i] and the up value to
+ * buf[row * 2I + I + i], where row is the row of h the kernel writes:
+ *   moe_ffn_forward (decode and prefill paths): the sorted assignment row
+ *     (< T*k), then T*k + t for token t of the shared expert: at least
+ *     (T*k + T) * 2I floats;
+ *   moe_decode_layer: slot * T + t, slot 0 the shared expert and slots
+ *     1.. the distinct selected experts in ascending id order: at least
+ *     (min(E, T*k) + 1) * T * 2I floats.
+ * A call whose buffer is too small returns QSM_ERR_INVALID_ARGUMENT.
+ * buf = NULL, n_floats = 0 turns the hook off.  Process-wide, not
+ * thread-safe; for tests only. */
+QSM_API qsm_status qsm_debug_gu_dump(float* buf, size_t n_floats);
 
 #ifdef __cplusplus
 }

@@ -118,6 +118,10 @@ def lib() -> ctypes.CDLL:
             L.moe_decode_layer.restype = st
             L.qsm_debug_barrier_skew.argtypes = [i32]
             L.qsm_debug_barrier_skew.restype = st
+            L.qsm_debug_gu_dump.argtypes = [P, sz]
+            L.qsm_debug_gu_dump.restype = st
+            L.qsm_decode_layer_fits.argtypes = [ctypes.POINTER(MoELayerC), i32, i32, i32]
+            L.qsm_decode_layer_fits.restype = i32
             L.qsm_launch_count.argtypes = []
             L.qsm_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -438,6 +442,16 @@ def debug_barrier_skew(skew: int) -> None:
     """Test hook: the decode layer's logit exchange waits for a call tag
     `skew` ahead of its own, so that every wait runs out (0 = off)."""
     _check(lib().qsm_debug_barrier_skew(int(skew)), "qsm_debug_barrier_skew")
+
+
+def debug_gu_dump(buf: torch.Tensor | None) -> None:
+    """Test hook: the gate_up kernels also write their fp32 gate and up
+    values to buf (a CUDA float32 tensor), or stop when buf is None."""
+    if buf is None:
+        _check(lib().qsm_debug_gu_dump(None, 0), "qsm_debug_gu_dump")
+    else:
+        assert buf.dtype == torch.float32 and buf.is_cuda and buf.is_contiguous()
+        _check(lib().qsm_debug_gu_dump(_p(buf), buf.numel()), "qsm_debug_gu_dump")
 
 
 def force_path(mode: str | int) -> None:

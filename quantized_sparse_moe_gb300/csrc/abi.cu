@@ -18,6 +18,8 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
                               int32_t* dev_status, cudaStream_t stream);
 
 std::atomic<unsigned long long> g_launch_count{0};
+float* g_gu_dump = nullptr;
+size_t g_gu_dump_floats = 0;
 
 namespace {
 
@@ -136,5 +138,13 @@ extern "C" uint64_t qsm_launch_count(void) {
 extern "C" qsm_status qsm_debug_force_path(int32_t mode) {
   if (mode < 0 || mode > 2) return QSM_ERR_INVALID_ARGUMENT;
   qsm::g_force_path.store(mode);
+  return QSM_OK;
+}
+
+extern "C" qsm_status qsm_debug_gu_dump(float* buf, size_t n_floats) {
+  if ((buf == nullptr) != (n_floats == 0)) return QSM_ERR_INVALID_ARGUMENT;
+  if (buf && !qsm::aligned4(buf)) return QSM_ERR_INVALID_ARGUMENT;
+  qsm::g_gu_dump = buf;
+  qsm::g_gu_dump_floats = n_floats;
   return QSM_OK;
 }

@@ -133,7 +133,7 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
                   const int32_t* __restrict__ tile_map, int shared_slots,
                   int xrows, __half* __restrict__ hbuf,
                   const float* __restrict__ sgate, float* __restrict__ gbuf,
-                  int32_t* dev_status) {
+                  float* __restrict__ gu_dump, int32_t* dev_status) {
   extern __shared__ __align__(128) unsigned char d1_smem[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ float red[kD1Split][32][4];
@@ -305,6 +305,10 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
       if (!(fabsf(h) <= 65504.f)) bad = true;
       const int hrow = shared_slot ? T * k + row0 + c : row0 + c;
       hbuf[(size_t)hrow * I + i0 + g] = __float2half_rn(h);
+      if (gu_dump) {  // test hook: the fused projection's values per h row
+        gu_dump[(size_t)hrow * 2 * I + i0 + g] = gate;
+        gu_dump[(size_t)hrow * 2 * I + I + i0 + g] = up;
+      }
     }
   }
   if (bad) set_status(dev_status, QSM_DEV_FP16_RANGE);
@@ -514,6 +518,11 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
   using namespace decode;
   const int H = L->H, I = L->I, k = L->k;
   const int shared_slots = (T + kTok - 1) / kTok;
+  float* gu_dump = nullptr;
+  if (g_gu_dump) {
+    if (g_gu_dump_floats < ((size_t)T * k + T) * 2 * I) return QSM_ERR_INVALID_ARGUMENT;
+    gu_dump = g_gu_dump;
+  }
   const dim3 g1(I / kTok, shared_slots + g->max_tiles);
   const int xrows = T < kTok ? T : kTok;
   const int crow = QT == QSM_Q8_0 ? H : H / 2;
@@ -533,7 +542,8 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
                           stream, L->gate_up, L->shared_gate_up, L->down,
                           L->shared_down, x, T, H, I, k, (const int32_t*)g->perm,
                           (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
-                          shared_slots, xrows, hbuf, L->shared_gate, gbuf, dev_status));
+                          shared_slots, xrows, hbuf, L->shared_gate, gbuf, gu_dump,
+                          dev_status));
   QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem2));

@@ -71,6 +71,8 @@
 // candidates and top 8, the chunk loops for H = 2048 and for four chunks of
 // a down slot), with the same arithmetic in the same order.
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "gemv_core.cuh"
 #include "route_select.cuh"
@@ -133,6 +135,7 @@ struct Params {
   float* y32;
   int32_t* status;
   int skew;               // test hook: added to the awaited call tag (0)
+  float* gu_dump;         // test hook: [slots * T, 2I] gate and up values, or null
 };
 
 // Barrier over n threads (a multiple of 32) of the CTA; the non-aligned form,
@@ -703,6 +706,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     } else {
       for (int ch = wg; ch < nch; ch += kGW) chunk(ch);
     }
+    consumed(acc);
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&empty[sl]);
     // the group's partials: buffer by the group's tile parity, so that the
@@ -728,6 +732,10 @@ decode_layer_kernel(const __grid_constant__ Params p) {
           const float h = silu(a[cc]) * a[2 + cc] * kHScale;
           if (!(fabsf(h) <= 65504.f)) range_bad = true;
           p.hbuf[((size_t)s * T + t) * I + i0 + g] = __float2half_rn(h);
+          if (p.gu_dump) {  // test hook: the fused projection's values per h row
+            p.gu_dump[((size_t)s * T + t) * 2 * I + i0 + g] = a[cc];
+            p.gu_dump[((size_t)s * T + t) * 2 * I + I + i0 + g] = a[2 + cc];
+          }
         }
       }
       // count the tile (release: the warp's h stores, ordered before by
@@ -787,6 +795,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
 #pragma unroll 1
         for (int ch = c0; ch < c1; ++ch) dchunk(ch);
       }
+      consumed(acc);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int t = 2 * q + cc;
@@ -828,13 +837,11 @@ decode_layer_kernel(const __grid_constant__ Params p) {
 inline size_t up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int sm_count_dl() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  }
-  return n;
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!n[dev]) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+  return n[dev];
 }
 
 // dynamic shared memory per CTA: the per-block maximum minus the static part
@@ -850,13 +857,19 @@ struct Geo {
 // One CTA per SM, or as many as the most gate_up tiles a call of up to 8
 // tokens can have, but at least one per 16 rows of y.  Independent of T, so
 // that calls of any T share a workspace (the call tag divides by it).
-int grid_of(const qsm_moe_layer* L) {
+int grid_of(const qsm_moe_layer* L, int nsm) {
   const int numax = kMaxT * L->k < L->E ? kMaxT * L->k : L->E;
   const int nt = (numax + 1) * (L->I / 8), gc = L->H / 16;
-  return std::max(gc, std::min(sm_count_dl(), nt));
+  return std::max(gc, std::min(nsm, nt));
 }
 
-bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
+// The logit exchange and the slot counters need every CTA of the grid
+// resident at once: G CTAs on nsm SMs holding blocks_per_sm CTAs each.
+bool grid_fits(int G, int nsm, int blocks_per_sm) {
+  return G >= 1 && nsm >= 1 && blocks_per_sm >= 1 && (long long)G <= (long long)nsm * blocks_per_sm;
+}
+
+bool geo_of(const qsm_moe_layer* L, int T, int nsm, Geo* o) {
   const int qt = L->gate_up.qtype;
   const int H = L->H, I = L->I, E = L->E, k = L->k;
   if (T < 1 || T > kMaxT || E < 1 || E > kMaxE || k < 1 || k > 32 || k > E) return false;
@@ -864,7 +877,7 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
   if (L->down.qtype != qt || L->shared_gate_up.qtype != qt || L->shared_down.qtype != qt)
     return false;
   if (H % 256 || I % (qt == QSM_Q8_0 ? 128 : 256)) return false;
-  if (H / 16 > sm_count_dl() || H > 16384 || I > 16384) return false;
+  if (H / 16 > nsm || H > 16384 || I > 16384) return false;
   const int bi = qt == QSM_Q8_0 ? 1 : 2;
   Geo g;
   g.hb = qt == QSM_Q8_0 ? H : H / 2;
@@ -875,7 +888,7 @@ bool geo_of(const qsm_moe_layer* L, int T, Geo* o) {
   const size_t dtile = 16 * (size_t)g.ib + 16 * (size_t)g.isb * bi;
   g.slot_bytes = (int)up(btile > dtile ? btile : dtile, 1024);
   g.numax = T * k < E ? T * k : E;
-  const int G = grid_of(L), epc = (E + G - 1) / G;
+  const int G = grid_of(L, nsm), epc = (E + G - 1) / G;
   // the deepest ring (then the largest C items) that fits
   const int mmax = (int)(g.slot_bytes / dtile) > 8 ? 8 : (int)(g.slot_bytes / dtile);
   bool fit = false;
@@ -928,16 +941,56 @@ WsLayout ws_layout(const qsm_moe_layer* L, int T, const Geo& g) {
   return w;
 }
 
+// The kernel instance for the layer's weight type and expert count.
+template <int QT, int kPer>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(decode_layer_kernel<QT, kPer>);
+}
+void* kernel_of(const qsm_moe_layer* L) {
+  const bool a4 = L->gate_up.qtype == QSM_AFFINE4_G64;
+  if (L->E <= 256) return a4 ? kernel_ptr<QSM_AFFINE4_G64, 8>() : kernel_ptr<QSM_Q8_0, 8>();
+  return a4 ? kernel_ptr<QSM_AFFINE4_G64, 32>() : kernel_ptr<QSM_Q8_0, 32>();
+}
+int threads_of(const qsm_moe_layer* L) {
+  return ((L->E <= 256 ? consumer_warps<8>() : consumer_warps<32>()) + 1) * 32;
+}
+
+// CTAs of the kernel that fit one SM of the current device at `smem` bytes
+// of dynamic shared memory (the occupancy calculator; cached per device,
+// kernel and size).  0 when the query fails.
+int blocks_per_sm(void* kernel, int threads, size_t smem) {
+  struct Key {
+    int dev;
+    void* k;
+    size_t smem;
+  };
+  static std::mutex mu;
+  static std::vector<std::pair<Key, int>> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& c : cache)
+    if (c.first.dev == dev && c.first.k == kernel && c.first.smem == smem) return c.second;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBudget) != cudaSuccess)
+    return 0;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess)
+    nb = 0;
+  cache.push_back({Key{dev, kernel, smem}, nb});
+  return nb;
+}
+
+// The layer and T are supported on the current device, and the whole grid
+// can be resident at once.
+bool supported_here(const qsm_moe_layer* L, int T, Geo* g) {
+  const int nsm = sm_count_dl();
+  if (!geo_of(L, T, nsm, g)) return false;
+  return grid_fits(grid_of(L, nsm), nsm, blocks_per_sm(kernel_of(L), threads_of(L), g->smem));
+}
+
 template <int QT, int kPer>
 cudaError_t launch(const Params& prm, size_t smem, cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<QT, kPer>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBudget);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
   return launch_pdl(decode_layer_kernel<QT, kPer>, dim3(prm.G),
                     dim3((consumer_warps<kPer>() + 1) * 32), smem, stream,
                     prm);
@@ -954,8 +1007,17 @@ extern "C" qsm_status qsm_debug_barrier_skew(int32_t skew) {
 
 extern "C" size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T) {
   qsm::dlayer::Geo g;
-  if (!L || !qsm::dlayer::geo_of(L, T, &g)) return 0;
+  if (!L || !qsm::dlayer::supported_here(L, T, &g)) return 0;
   return qsm::dlayer::ws_layout(L, T, g).total;
+}
+
+extern "C" int32_t qsm_decode_layer_fits(const qsm_moe_layer* L, int32_t T, int32_t sm_count,
+                                         int32_t blocks_per_sm) {
+  qsm::dlayer::Geo g;
+  if (!L || !qsm::dlayer::geo_of(L, T, sm_count, &g)) return 0;
+  return qsm::dlayer::grid_fits(qsm::dlayer::grid_of(L, sm_count), sm_count, blocks_per_sm)
+             ? 1
+             : 0;
 }
 
 extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x, int32_t T,
@@ -972,7 +1034,7 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   if (!x || !w_router || !topk_idx || !topk_w || !y || !workspace || !dev_status)
     return QSM_ERR_INVALID_ARGUMENT;
   Geo g;
-  if (!geo_of(L, T, &g)) return QSM_ERR_UNSUPPORTED;
+  if (!supported_here(L, T, &g)) return QSM_ERR_UNSUPPORTED;
   const WsLayout wl = ws_layout(L, T, g);
   if (workspace_bytes < wl.total) return QSM_ERR_WORKSPACE_TOO_SMALL;
   const qsm_qweights *gu = &L->gate_up, *gs = &L->shared_gate_up, *dn = &L->down,
@@ -1020,7 +1082,7 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.E = E;
   prm.k = L->k;
   prm.flags = flags;
-  prm.G = grid_of(L);
+  prm.G = grid_of(L, sm_count_dl());
   prm.GC = H / 16;
   prm.epc = (E + prm.G - 1) / prm.G;
   prm.hb = g.hb;
@@ -1048,6 +1110,11 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.y32 = y_f32;
   prm.status = dev_status;
   prm.skew = g_barrier_skew;
+  prm.gu_dump = nullptr;
+  if (g_gu_dump) {
+    if (g_gu_dump_floats < (size_t)(g.numax + 1) * T * 2 * I) return QSM_ERR_INVALID_ARGUMENT;
+    prm.gu_dump = g_gu_dump;
+  }
   cudaError_t err;
   if (E <= 256)
     err = a4 ? launch<QSM_AFFINE4_G64, 8>(prm, g.smem, stream)

@@ -32,11 +32,13 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of this device's copy of g_ffn_scratch (looked up once).
-qsm_status scratch_of_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return QSM_ERR_CUDA;
+// Device address of this device's copy of g_ffn_scratch (looked up once per
+// device, on the first call made with that device current).  The address
+// stays valid for the life of the device's primary context: after
+// cudaDeviceReset the module is loaded again, possibly elsewhere, and calls
+// are not supported.
+qsm_status scratch_of_current_device(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return QSM_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
@@ -56,14 +58,26 @@ extern "C" qsm_status moe_ffn_forward_noalloc(
     uint16_t* y, float* y_f32, int32_t* dev_status, cudaStream_t stream) {
   if (T < 0) return QSM_ERR_INVALID_ARGUMENT;
   if (T > kNoAllocMaxT) return QSM_ERR_UNSUPPORTED;
+  if (T == 0) return moe_ffn_forward(L, x, T, topk_idx, topk_w, g, y, y_f32, nullptr, 0,
+                                     dev_status, stream);
   const size_t need = moe_ffn_workspace_bytes(L, T);
-  if (need == 0 && T > 0) return QSM_ERR_INVALID_ARGUMENT;  // bad layer
+  if (need == 0) return QSM_ERR_INVALID_ARGUMENT;  // bad layer
   if (need > kNoAllocScratchBytes) return QSM_ERR_UNSUPPORTED;
+  // The scratch belongs to the current device: a stream of another device
+  // would hand that device's kernels this device's address.
+  int dev = -1, sdev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QSM_ERR_CUDA;
+  if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return QSM_ERR_CUDA;
+  if (sdev != dev) return QSM_ERR_INVALID_ARGUMENT;
   void* scratch = nullptr;
-  const qsm_status s = scratch_of_current_device(&scratch);
+  const qsm_status s = scratch_of_current_device(dev, &scratch);
   if (s != QSM_OK) return s;
   // Nothing in the scratch has to start at zero: every value the FFN reads
-  // back was written earlier in the same call.
-  return moe_ffn_forward(L, x, T, topk_idx, topk_w, g, y, y_f32, scratch,
-                         kNoAllocScratchBytes, dev_status, stream);
+  // back was written earlier in the same call.  The size check above and
+  // the call below each consult the path in force; a test hook that switched
+  // it in between could make the scratch too small, which is reported as
+  // unsupported like any other size beyond it.
+  const qsm_status r = moe_ffn_forward(L, x, T, topk_idx, topk_w, g, y, y_f32, scratch,
+                                       kNoAllocScratchBytes, dev_status, stream);
+  return r == QSM_ERR_WORKSPACE_TOO_SMALL ? QSM_ERR_UNSUPPORTED : r;
 }

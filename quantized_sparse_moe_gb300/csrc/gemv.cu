@@ -521,6 +521,8 @@ q8_gemv_stream_kernel(const __grid_constant__ CUtensorMap cmap,
           red[b][par][seg][half][g] = pg;
           red[b][par][seg][half][g + 8] = ph;
         }
+        consumed(pg);
+        consumed(ph);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&empty[slot]);

@@ -46,6 +46,13 @@ inline void max_smem_carveout(const void* kernel) {
 // graph under capture), process-wide.  Read through qsm_launch_count().
 extern std::atomic<unsigned long long> g_launch_count;
 
+// Test hook (qsm_debug_gu_dump): when set, the kernels that compute the
+// fused gate_up projection also write its fp32 gate and up values, before
+// SwiGLU, to this device buffer of g_gu_dump_floats floats (layout per
+// kernel family in include/qsmoe.h).
+extern float* g_gu_dump;
+extern size_t g_gu_dump_floats;
+
 // Launch with programmatic dependent launch enabled: the kernel may start
 // while its predecessor on the stream drains; it must execute
 // pdl_wait() before touching anything the predecessor writes (or reads).
@@ -323,6 +330,16 @@ __device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Orders the computation of v before everything after this point: a
+// consumer that releases a shared-memory slot puts the values computed from
+// the slot here first, so that no load from the slot can still be in flight
+// when the release is issued (the compiler may otherwise move the
+// arithmetic, and with it the wait for the loads, past the release).
+__device__ __forceinline__ void consumed(float v) { asm volatile("" ::"f"(v) : "memory"); }
+__device__ __forceinline__ void consumed(const float (&v)[4]) {
+  asm volatile("" ::"f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]) : "memory");
 }
 
 // Make an initialised mbarrier visible to the async (TMA) proxy.

@@ -56,3 +56,14 @@ def check_layer_output(y, y32, x, idx_o, w_o, q, tokens=None, shared_gate=None):
     assert torch.equal(yb.view(torch.int16), rne.view(torch.int16)), \
         "bf16 output is not the round-to-nearest-even of the fp32 output"
     return err, ref
+
+
+def check_against(y, y32, ref):
+    """check_layer_output against a precomputed oracle output of all tokens
+    (one oracle run serving several GPU runs of the same inputs)."""
+    y32n = y32.cpu().numpy().astype(np.float64)
+    err = tol_metric(y32n, ref)
+    rne = torch.from_numpy(y32n.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(y.cpu().view(torch.int16), rne.view(torch.int16)), \
+        "bf16 output is not the round-to-nearest-even of the fp32 output"
+    return err

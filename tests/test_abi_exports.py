@@ -46,7 +46,7 @@ def test_library_builds_loads_and_exports_everything():
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared but not exported"
     lib.qsm_abi_version.restype = ctypes.c_int32
-    assert lib.qsm_abi_version() == 3
+    assert lib.qsm_abi_version() == 4
     lib.qsm_status_str.restype = ctypes.c_char_p
     assert lib.qsm_status_str(0) == b"ok"
     # host-only helpers need no device
@@ -61,3 +61,35 @@ def test_library_builds_loads_and_exports_everything():
         exported = {l.split()[-1] for l in out.splitlines()
                     if " T " in l}
         assert set(declared_functions()) <= exported
+
+
+@pytest.mark.skipif(shutil.which("nvcc") is None and
+                    not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                    reason="nvcc missing")
+def test_decode_layer_coresidency_check():
+    """qsm_decode_layer_fits: the one-launch decode layer runs only when its
+    whole grid can be resident (host logic, no GPU)."""
+    import quantized_sparse_moe_gb300 as qsm
+    from quantized_sparse_moe_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    f = lib.qsm_decode_layer_fits
+    f.argtypes = [ctypes.POINTER(qsm.MoELayerC), ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_int32]
+    f.restype = ctypes.c_int32
+
+    def layer(qtype, H=2048, I=512, E=256, k=8):
+        def qw(experts, rows, cols):
+            return qsm.QWeightsC(qtype, experts, rows, cols, None, None, None)
+        return qsm.MoELayerC(H, I, E, k, qw(E, 2 * I, H), qw(E, H, I), qw(1, 2 * I, H),
+                             qw(1, H, I), None)
+
+    q8 = layer(qsm.Q8_0)
+    assert f(ctypes.byref(q8), 1, 152, 1) == 1      # GB300: 152 SMs, one CTA each
+    assert f(ctypes.byref(q8), 8, 152, 1) == 1
+    assert f(ctypes.byref(q8), 1, 152, 0) == 0      # no CTA fits an SM
+    assert f(ctypes.byref(q8), 1, 120, 1) == 0      # fewer SMs than 16-row blocks of y
+    assert f(ctypes.byref(q8), 9, 152, 1) == 0      # more than 8 tokens
+    assert f(ctypes.byref(q8), 0, 152, 1) == 0
+    a4 = layer(qsm.AFFINE4_G64)
+    assert f(ctypes.byref(a4), 4, 152, 1) == 1
+    assert f(ctypes.byref(layer(qsm.Q8_0, E=512)), 2, 152, 1) == 1

@@ -146,7 +146,9 @@ def test_decode_layer_unsupported(qsm):
 def test_decode_layer_barrier_timeout_is_reported(qsm):
     """A logit exchange that cannot complete (test hook: the awaited call tag
     raised by one) makes every bounded wait run out: the call sets QSM_DEV_TIMEOUT and
-    returns; the context stays usable and the next call is exact."""
+    returns; the context stays usable.  The timed-out call's results are
+    invalid and, as the header requires, its workspace is zeroed before the
+    next call, which is exact."""
     shape = synth.TINY
     Lg, q, wr, bias = layer(shape, 7, None)
     L = qsm.Layer.from_synth(Lg)
@@ -161,6 +163,7 @@ def test_decode_layer_barrier_timeout_is_reported(qsm):
         qsm.debug_barrier_skew(0)
     assert st.item() & qsm.DEV_TIMEOUT
     st.zero_()
+    ws.zero_()
     y, y32, idx, w = qsm.moe_decode_layer(L, x, y_f32=True, workspace=ws, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0

@@ -183,10 +183,11 @@ def test_cross_path_same_tokens(qsm, T):
     assert tol_metric(outs["decode"], outs["prefill"]) <= TOL
 
 
-def test_prefill_zipf_t4096_sampled(qsm):
+def test_prefill_zipf_t4096_all_tokens(qsm):
     """The prefill workload at full size: T=4096, Zipf-offset routing (many
-    empty experts, a few very large groups); all routing bit-exact, the
-    layer output checked on sampled tokens."""
+    empty experts, a few very large groups); all routing bit-exact, and every
+    output of every token against the oracle (447 blocks: every row position
+    of every 128-row block, short blocks of every 16-row size)."""
     shape = synth.QWEN
     Lg, q, wr, bias = layer(shape, 3, "noise")
     x = x_for(shape, 4096, 4096, Lg, wr, bias)
@@ -196,15 +197,9 @@ def test_prefill_zipf_t4096_sampled(qsm):
     assert np.array_equal(fwd.topk_idx.cpu().numpy(), idx_o)
     counts = np.bincount(idx_o.ravel(), minlength=shape.E)
     assert (counts == 0).sum() > 0          # some experts are empty
+    assert counts.max() > 128               # some experts span several blocks
     assert np.array_equal(fwd.grouping.counts.cpu().numpy(), counts)
-    # tokens that use the largest and the smallest non-empty groups, plus random
-    big = np.argmax(counts)
-    small = np.where(counts == counts[counts > 0].min())[0][0]
-    pick = {int(np.where((idx_o == big).any(1))[0][0]),
-            int(np.where((idx_o == small).any(1))[0][0])}
-    pick |= set(np.random.default_rng(1).choice(4096, 30, replace=False).tolist())
-    toks = np.array(sorted(pick), np.int32)
-    err, _ = check_layer_output(fwd.y, fwd.y_f32, x, idx_o, w_o, q, toks)
+    err, _ = check_layer_output(fwd.y, fwd.y_f32, x, idx_o, w_o, q)
     assert err <= TOL
 
 
@@ -258,9 +253,9 @@ def test_affine4_cross_path(qsm, T):
     assert tol_metric(outs["decode"], outs["prefill"]) <= TOL
 
 
-def test_affine4_prefill_zipf_t2048_sampled(qsm):
+def test_affine4_prefill_zipf_t2048_all_tokens(qsm):
     """Affine-4 prefill with uneven groups (Zipf offset): routing bit-exact,
-    the output checked on tokens of the largest and smallest groups."""
+    every output of every token against the oracle."""
     shape = synth.QWEN_A4
     Lg, q, wr, bias = layer(shape, 6, "noise")
     T = 2048
@@ -270,11 +265,6 @@ def test_affine4_prefill_zipf_t2048_sampled(qsm):
     idx_o, w_o = oracle_route(x, wr, bias, shape.k)
     assert np.array_equal(fwd.topk_idx.cpu().numpy(), idx_o)
     counts = np.bincount(idx_o.ravel(), minlength=shape.E)
-    big = np.argmax(counts)
-    small = np.where(counts == counts[counts > 0].min())[0][0]
-    pick = {int(np.where((idx_o == big).any(1))[0][0]),
-            int(np.where((idx_o == small).any(1))[0][0])}
-    pick |= set(np.random.default_rng(2).choice(T, 24, replace=False).tolist())
-    toks = np.array(sorted(pick), np.int32)
-    err, _ = check_layer_output(fwd.y, fwd.y_f32, x, idx_o, w_o, q, toks)
+    assert (counts == 0).sum() > 0 and counts.max() > 128
+    err, _ = check_layer_output(fwd.y, fwd.y_f32, x, idx_o, w_o, q)
     assert err <= TOL

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import synth
-from _gpu_cases import TOL, TOPK_W_ATOL, check_layer_output, layer, oracle_route, x_for
+from _gpu_cases import (TOL, TOPK_W_ATOL, check_against, check_layer_output, layer,
+                        oracle_route, x_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -17,12 +18,16 @@ def _rel(a, b):
 
 @pytest.mark.parametrize("shape", [synth.QWEN, synth.QWEN_A4], ids=["q8", "a4"])
 def test_chunked_layer_matches_oracle_and_unchunked(qsm, shape):
+    """Every token and every output of a 1000-token layer (Zipf-offset
+    routing), for each chunking, against one oracle run of all tokens."""
+    import oracle
+    from _helpers import bits16
     T = 1000
     Lg, q, wr, bias = layer(shape, 8, "noise")
     x = x_for(shape, T, 800, Lg, wr, bias)
     L = qsm.Layer.from_synth(Lg)
     idx_o, w_o = oracle_route(x, wr, bias, shape.k)
-    toks = np.sort(np.random.default_rng(3).choice(T, 40, replace=False)).astype(np.int32)
+    ref = oracle.moe_layer(bits16(x), idx_o, w_o, *q)
     outs = {}
     for chunk in (T, 512, 300, 64, 7):
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -32,7 +37,7 @@ def test_chunked_layer_matches_oracle_and_unchunked(qsm, shape):
         assert st.item() == 0, chunk
         assert np.array_equal(ti.cpu().numpy(), idx_o), chunk
         np.testing.assert_allclose(tw.cpu().numpy(), w_o, atol=TOPK_W_ATOL)
-        err, _ = check_layer_output(y, y32, x, idx_o, w_o, q, toks)
+        err = check_against(y, y32, ref)
         assert err <= TOL, (chunk, err)
         outs[chunk] = y32.cpu().numpy().astype(np.float64)
     # prefill-sized chunkings differ only in the fp32 combine order
