@@ -9,6 +9,17 @@ step time.  Inputs are synthetic, seeded, drawn on the device before the
 timed region; the 1.3 GB of expert weights a step touches is ~10x the L2,
 so no flush is needed.
 
+The metric is quoted on T=1 decode and on T=4096 prefill: the default line
+also carries a "prefill" object for one T=4096 layer (Zipf-offset routing,
+Q8_0), measured in the same run with the same protocol.
+
+Protocol per workload: W warm-up replays, then exactly K graph replays
+between two events (ms_per_step, value), then --replays further replays
+each timed alone ("replays": median and spread), with the routing ids
+hashed after every replay and required identical (the output-hash check of
+"Ember: packed Q8 decode"); the oracle is timed on the host at all cores and
+at one thread (cpu_baseline).
+
 Other workloads (--workload): prefill (T=4096, Zipf-skewed routing, one
 layer), batched16 / batched64 / batched1 (affine 4-bit, 40 layers), gemv
 (Llama-3.2-1B Q8_0 projections).
@@ -150,6 +161,44 @@ class ClockSampler:
 
 # ------------------------------------------------------------------- ours
 
+def fnv1a64(data: bytes) -> str:
+    """FNV-1a 64-bit hash (the output hash of the Ember page's method)."""
+    h = 0xcbf29ce484222325
+    for b in data:
+        h = ((h ^ b) * 0x100000001b3) & 0xFFFFFFFFFFFFFFFF
+    return f"fnv1a64:{h:016x}"
+
+
+def replay_stats(graph, stream, fwds, n):
+    """Each of n further graph replays timed alone (its own event pair on the
+    launching stream), and the routing ids of every layer hashed after each
+    replay: all replays must route identically ("Ember: packed Q8 decode",
+    method paragraph: every accepted trial shares one output hash).  The
+    check compares a BLAKE2b digest of each replay's ids; the FNV-1a 64 hash
+    of the first replay's ids is reported as the output hash."""
+    import hashlib
+    times, digests, first = [], set(), None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        stream.synchronize()
+        ids = torch.cat([f.topk_idx.reshape(-1) for f in fwds]).cpu().numpy().tobytes()
+        digests.add(hashlib.blake2b(ids, digest_size=16).hexdigest())
+        if first is None:
+            first = ids
+        times.append(a.elapsed_time(b))
+    if len(digests) != 1:
+        raise RuntimeError(f"routing differed across replays: {len(digests)} distinct outputs")
+    t = np.array(times)
+    return {"n": n, "median_ms": float(np.median(t)), "p10_ms": float(np.percentile(t, 10)),
+            "p90_ms": float(np.percentile(t, 90)), "routing_hash": fnv1a64(first),
+            "hash_equal_over_replays": True}
+
+
 def build_layers(qsm, wl, device, seed, fuse=True, gated=False, sel_only=False):
     shape = wl["shape"]
     layers, xs, fwds, syn = [], [], [], []
@@ -259,6 +308,7 @@ def run_ours(args, wl, rank, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = t.item()
     value = world * T * nL / (ms / 1e3)
+    replays = replay_stats(graph, stream, fwds, args.replays)
 
     # dominant launch pair: the expert FFN (gate_up+SwiGLU, down+combine),
     # bracketed per layer by event nodes inside a captured graph so the
@@ -404,6 +454,7 @@ def run_ours(args, wl, rank, world):
                 "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
+        "replays": dict(replays, tokens_per_s_at_median=world * T * nL / (replays["median_ms"] / 1e3)),
     }
     return result, (syn, fwds, xs)
 
@@ -435,9 +486,19 @@ class OracleSampler:
                 bias=None if Lg.logit_bias is None else Lg.logit_bias.cpu().numpy(),
                 k=Lg.shape.k, E=Lg.shape.E, toks=toks))
 
-    def run(self, budget_s):
+    def run(self, budget_s, threads=None):
         """Calls cycling over the sampled layers until budget_s seconds of
-        oracle time; returns (tokens/s, seconds, calls)."""
+        oracle time; returns (tokens/s, seconds, calls).  threads: OpenMP
+        threads for this run (default: all host cores)."""
+        orc = self.oracle
+        all_cores = orc.max_threads()
+        orc.set_threads(threads or all_cores)
+        try:
+            return self._run(budget_s)
+        finally:
+            orc.set_threads(all_cores)
+
+    def _run(self, budget_s):
         orc = self.oracle
         tokens, t_used, calls = 0, 0.0, 0
         while t_used < budget_s:
@@ -450,6 +511,17 @@ class OracleSampler:
             tokens += len(L["toks"])
             calls += 1
         return tokens / t_used, t_used, calls
+
+    def baseline(self, budget_s, budget_1t_s):
+        """cpu_baseline object: all host cores, and one thread."""
+        cores = self.oracle.max_threads()
+        v, t, calls = self.run(budget_s)
+        v1, t1, calls1 = self.run(budget_1t_s, threads=1)
+        return {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": self.describe(t, calls),
+                "one_thread": {"value": v1, "unit": "tokens/s", "cores": 1,
+                               "sample": self.describe(t1, calls1)},
+                "speedup_all_cores": v / v1 if v1 > 0 else None}
 
     def describe(self, seconds, calls):
         return (f"{len(self.layers)} layer(s) of the workload, {calls} call(s) cycling "
@@ -476,7 +548,24 @@ def run_reference(args, wl, rank, world):
             secs += t
             calls += c
     value = statistics.median(vals)
-    return {
+    prefill = None
+    if args.workload == "decode" and not args.no_prefill:
+        # the prefill workload of the same metric, on a bounded sample
+        pwl = WORKLOADS["prefill"]
+        PL = [synth.draw_layer(pwl["shape"], dev, seed=0, layer=0, zipf=pwl["zipf"])]
+        px = [synth.draw_x(pwl["T"], pwl["shape"].H, dev, 0, 0)]
+        psampler = OracleSampler(pwl, PL, px, max_layers=1)
+        del PL
+        pv, pt, pc = psampler.run(min(20.0, max(5.0, step_s * args.steps)))
+        prefill = {"value": pv, "unit": "tokens/s", "config": {"workload": pwl["desc"],
+                                                               "tokens_per_layer": pwl["T"],
+                                                               "layers": 1},
+                   "cpu_baseline": {"value": pv, "unit": "tokens/s",
+                                    "cores": psampler.oracle.max_threads(), "kind": "oracle",
+                                    "sample": psampler.describe(pt, pc)},
+                   "e2e": {"value": pv, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}}
+    out = {
         "impl": "reference", "metric": "MoE-layer tokens/s", "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
@@ -490,6 +579,9 @@ def run_reference(args, wl, rank, world):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    if prefill is not None:
+        out["prefill"] = prefill
+    return out
 
 
 
@@ -680,6 +772,11 @@ def main():
                          "this many tokens (chunked prefill)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (profiling runs only)")
+    ap.add_argument("--replays", type=int, default=100,
+                    help="graph replays timed one by one after the K timed steps "
+                         "(median and routing-hash check)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode workload: leave out the T=4096 prefill object")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -724,10 +821,22 @@ def main():
         res, (syn, fwds, xs) = run_ours(args, wl, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
             sampler = OracleSampler(wl, syn, xs, max_layers=4)
-            v, t, calls = sampler.run(12.0)
-            res["cpu_baseline"] = {
-                "value": v, "unit": "tokens/s", "cores": sampler.oracle.max_threads(),
-                "kind": "oracle", "sample": sampler.describe(t, calls)}
+            res["cpu_baseline"] = sampler.baseline(10.0, 4.0)
+        del syn, fwds, xs
+        if args.workload == "decode" and not args.no_prefill and not args.layers:
+            # the metric is quoted on T=1 decode and T=4096 prefill: the
+            # prefill layer is measured in the same run, same protocol
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            pwl = dict(WORKLOADS["prefill"])
+            pres, (psyn, pfwds, pxs) = run_ours(args, pwl, rank, world)
+            if rank == 0 and not args.no_cpu_baseline:
+                psampler = OracleSampler(pwl, psyn, pxs, max_layers=1)
+                pres["cpu_baseline"] = psampler.baseline(10.0, 4.0)
+            for key in ("metric", "n_gpus", "steps", "warmup", "higher_is_better",
+                        "scaling", "vs_baseline", "data"):
+                pres.pop(key, None)
+            res["prefill"] = pres
     if rank == 0 and res is not None:
         print(json.dumps(res))
     if world > 1:

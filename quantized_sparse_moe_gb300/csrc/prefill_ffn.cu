@@ -7,49 +7,44 @@
 // multiply them with the routed activation rows, accumulates in fp32, and
 // never writes the expanded weight matrix to memory; section "Keeping
 // expert routing on the GPU": the block map of the grouping drives the
-// tiles, with no host round trip; section "Matching tile size to expert
-// load": the MMA's token dimension is sized to each expert's block; "oMLX
-// MoE gate/up 融合优化", "融合原理": one pass over the fused [gate; up]
-// weight.
+// tiles, with no host round trip; "oMLX MoE gate/up 融合优化", "融合原理":
+// one pass over the fused [gate; up] weight.
 //
 // Launch sequence (stream ordered, programmatic dependent launch):
 //   prep      the token operand of gate_up as one fp16 matrix (exact for
 //             the bf16 inputs): the routed rows in grouped order (sorted
 //             row r holds the token of assignment perm[r]), then the T
-//             tokens in order for the shared expert; with a gated shared
-//             expert, its gates
-//   gate_up   per work item (a block of <= 128 token rows of one expert and
-//             128 intermediate indices): two accumulators D_gate, D_up
-//             (128 weight rows x N tokens, fp32 in tensor memory) +=
-//             [W_gate tile | W_up tile] x token rows^T, N = the block's
-//             rows rounded up to 16; epilogue (one intermediate index per
-//             thread) h = silu(gate) * up, stored fp16 (scaled by 1/16) per
-//             sorted row.  Warp 3 zeroes the fp32 output accumulator.
-//   down      per work item (same token block, 256 output rows as two
-//             128-row tiles): D = W_down tiles x h rows^T; epilogue
-//             y_acc[token][row] += routing weight * D (fp32 reduce-adds, a
-//             warp's 32 rows of one token in one 128-byte request)
+//             tokens in order for the shared expert; zero the fp32 output
+//             accumulator
+//   gate_up   per work item (block of <= 128 token rows of one expert,
+//             128 intermediate indices): D (128 token rows x 256, fp32 in
+//             tensor memory) += token rows x [W_gate tile; W_up tile]^T, one
+//             N = 256 MMA per 16-wide K step; epilogue (one token row per
+//             thread) h = silu(gate) * up, stored fp16 (scaled by 1/16) in
+//             16-byte pieces per sorted row
+//   down      per work item (same token block, 256 output rows):
+//             D (128 token rows x 256) = h rows x W_down tiles^T; epilogue
+//             y_acc[token] += routing weight * D row (16-byte fp32
+//             reduce-adds, one token per thread)
+// Rows of a short tile beyond its tokens hold stale data: their D rows are
+// never read.
 //   finalize  y = bf16(y_acc) (and the fp32 copy)
 //
 // Roles in a persistent CTA (one per SM, 16 warps):
-//   warp 0       TMA producer of the int8 / uint4 code tiles (2D tensor map,
-//                64- or 32-byte swizzle)
+//   warp 0       TMA producer of the int8 code tiles (2D tensor map)
 //   warp 1       allocates tensor memory; lane 0 issues the MMAs
-//   warp 2       TMA producer of the token tiles: 2D boxes of the grouped
-//                fp16 x (gate_up) or of h (down), 128 rows or a 64/32/16-row
-//                decomposition of a short block, 128-byte swizzled, K-major
-//   warp 3       gate_up: zeroes its slice of y_acc
-//   warps 4-11   dequantise the code tiles, one weight row per thread, into
-//                the A operand in tensor memory (tcgen05.st): fp16(code *
-//                block scale) (Q8_0) or fp16(scale * code + bias) (affine-4)
+//   warp 2       TMA producer of the token-row tiles: 2D boxes of the
+//                grouped fp16 x (gate_up) or of h (down), 128 rows or a
+//                64/32/16-row decomposition of a short tile's rows
+//   warps 4-11   dequantise the code tiles: fp16(code * block scale) written
+//                in the 128-byte-swizzled K-major layout the MMA reads
 //   warps 12-15  epilogue, one warp per quarter of the tensor-memory lanes
-// Rings: code tiles in shared memory (freed once dequantised), token tiles
-// in shared memory (freed by the MMA commit), dequantised weight tiles in
-// tensor memory (freed by the MMA commit).  The weights are the MMA's A
-// operand and never pass through shared memory, which leaves its bandwidth
-// to the token tiles.  One accumulator pair (tensor-memory columns 0..255)
-// connects MMA and epilogue; the dequantised ring (columns 256..511) runs
-// ahead into the next item while the epilogue drains.
+// Three shared-memory rings, each with full / empty mbarriers: code tiles
+// (freed as soon as the dequantising warps have read them), token tiles
+// (freed by the MMA commit) and dequantised weight tiles (freed by the MMA
+// commit).  Keeping the rings apart lets each run as many stages ahead as
+// its own latency needs.  Two accumulator buffers in tensor memory
+// (mbarriers: full / empty) connect MMA and epilogue.
 //
 // Weights: Q8_0 (int8 codes, an fp16 scale per 32) or affine-4 (8 codes
 // per 32-bit word, lowest nibble first along K, fp16 scale and bias per 64:
@@ -64,28 +59,21 @@
 namespace qsm {
 namespace prefill {
 
-constexpr int BW = 128;   // weight rows per MMA tile (the MMA's M)
-constexpr int BK = 64;    // K per stage: 128 bytes of fp16 token row
-constexpr int BN = 128;   // token rows per block (the MMA's N <= BN) = the path's tile_rows
+constexpr int BM = 128;   // weight rows per weight tile (two tiles form the MMA's N = 256)
+constexpr int BK = 64;    // K per stage: 128 bytes of fp16
+constexpr int BN = 128;   // token rows per tile (the MMA's M) = the path's tile_rows
 constexpr int kThreads = 512;
 constexpr int kDeqThreads = 256;  // warps 4..11
-constexpr int kEpiThreads = 128;  // warps 12..15
 constexpr float kHScale = 1.0f / 16.0f;
 constexpr float kHScaleInv = 16.0f;
-// Tensor memory: the two accumulators at columns 0 and BN, then the ring of
-// dequantised weight stages (two 128-row tiles of 64 K = 2 x 32 columns).
-constexpr int kAst = 4;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcol = 2 * BN;
-static_assert(kAcol + kAst * 64 <= kTmemCols, "tensor memory columns");
 
 enum { kGateUp = 1, kDown = 2 };
 
 struct Params {
-  CUtensorMap codes;      // routed experts' codes [E*R, K code bytes] u8, box {KB, 128}
-  CUtensorMap codes_sh;   // shared expert's codes [R, K code bytes]
-  CUtensorMap bmap[4];    // token rows [T*k + T, K] fp16 (gate_up: grouped x; down:
-                          // h), boxes {64, 128 / 64 / 32 / 16}
+  CUtensorMap codes;      // routed experts' codes [E*R, K] u8, box {64, 128}
+  CUtensorMap codes_sh;   // shared expert's codes [R, K] u8, box {64, 128}
+  CUtensorMap bmap[4];    // token rows [T*k + T, K] fp16 (gate_up: grouped
+                          // x; down: h), boxes {64, 128 / 64 / 32 / 16}
   const __half* scales;   // [E*R, K/32] (Q8_0) or [E*R, K/64] (affine-4)
   const __half* scales_sh;
   const __half* biases;   // [E*R, K/64] (affine-4)
@@ -98,7 +86,7 @@ struct Params {
   const int32_t* n_tiles;
   const float* topk_w;
   int shared_tiles;       // ceil(T / BN)
-  int nsub;               // weight-tile pairs per block
+  int nsub;               // weight blocks (two 128-row tiles each) per tile
   __half* hbuf;           // [T*k + T, I]
   float* yacc;            // [T, H]
   const float* gate;      // [T] shared-expert gates, or NULL (weight 1)
@@ -109,7 +97,7 @@ struct Params {
 struct TileInfo {
   int e;     // expert, -1 = shared expert
   int row0;  // first sorted row (routed) or first token (shared)
-  int cnt;   // rows in the block
+  int cnt;   // rows in the tile
   int n;     // MMA N: cnt rounded up to 16
 };
 
@@ -125,8 +113,7 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int tau) {
     t.row0 = te.y;
     t.cnt = min(BN, __ldcg(p.offsets + t.e + 1) - t.row0);
   }
-  t.cnt = max(t.cnt, 0);
-  t.n = max(16, (t.cnt + 15) & ~15);  // an empty block still issues a valid MMA
+  t.n = (t.cnt + 15) & ~15;
   return t;
 }
 
@@ -146,7 +133,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
 }
 
 // The abort flag as one decision for the whole warp (roles whose lanes run
-// .sync.aligned tensor-memory instructions or warp shuffles together).
+// .sync.aligned tensor-memory instructions together).
 __device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
   return __any_sync(0xffffffffu, *abort_flag != 0);
 }
@@ -167,11 +154,15 @@ __device__ __forceinline__ void drain_stages(uint64_t* full, int depth, uint32_t
 // gate_up pairs the gate rows and the up rows of intermediates sub*128..,
 // down takes output rows sub*256 + a*128...
 __device__ __forceinline__ int weight_row0(const Params& p, int mode, int sub, int a) {
-  return mode == kGateUp ? a * p.I + sub * BW : (2 * sub + a) * BW;
+  return mode == kGateUp ? a * p.I + sub * BM : (2 * sub + a) * BM;
 }
 
-__device__ __forceinline__ void red_add(float* y, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(y), "f"(v) : "memory");
+// y[0..3] += v0..v3 in one 16-byte reduction (16-byte aligned address).
+__device__ __forceinline__ void red_add_v4(float* y, float v0, float v1, float v2,
+                                           float v3) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(y), "f"(v0),
+               "f"(v1), "f"(v2), "f"(v3)
+               : "memory");
 }
 
 // One 32-bit word of affine-4 codes (K order k..k+7, lowest nibble first)
@@ -194,20 +185,24 @@ __device__ __forceinline__ uint4 a4_word_to_f16x8(uint32_t w, __half2 s2, __half
   return make_uint4(v[0], v[1], v[2], v[3]);
 }
 
-template <int MODE, int QT, int CR, int BR>
+template <int MODE, int QT, int CR, int BR, int AST>
 __global__ void __launch_bounds__(kThreads, 1)
 moe_prefill_gemm(const __grid_constant__ Params p) {
+  constexpr int NA = 2;                        // weight tiles per K step
+  constexpr int A_BYTES = BM * BK * 2;         // fp16, 128B swizzle
+  constexpr int B_BYTES = BN * BK * 2;
   constexpr int KB = QT == QSM_Q8_0 ? BK : BK / 2;  // code bytes per row and K step
-  constexpr int C_BYTES = BW * KB;                  // one weight tile's codes
-  constexpr int C_STAGE = 2 * C_BYTES;
-  constexpr int B_BYTES = BN * BK * 2;              // token tile, fp16, 128B swizzle
+  constexpr int C_BYTES = BM * KB;
+  constexpr int A_STAGE = NA * A_BYTES;        // dequantised ring
+  constexpr int C_STAGE = NA * C_BYTES;        // code ring
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* bring = smem;                     // [BR][B_BYTES]
+  unsigned char* aring = smem;                     // [AST][A_STAGE]
+  unsigned char* bring = aring + AST * A_STAGE;    // [BR][B_BYTES]
   unsigned char* cring = bring + BR * B_BYTES;     // [CR][C_STAGE]
   __shared__ __align__(8) uint64_t c_full[CR], c_empty[CR], b_full[BR], b_empty[BR],
-      a_full[kAst], a_empty[kAst], acc_full, acc_empty, mma_done;
+      a_full[AST], a_empty[AST], accf_bar[2], acce_bar[2], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -221,12 +216,14 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);  // MMA commit
     }
-    for (int s = 0; s < kAst; ++s) {
+    for (int s = 0; s < AST; ++s) {
       mbar_init(&a_full[s], kDeqThreads);
-      mbar_init(&a_empty[s], 1);  // MMA commit
+      mbar_init(&a_empty[s], 1);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, kEpiThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 128);
+    }
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -237,7 +234,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) tc::prefetch_map(&p.bmap[m]);
   }
-  if (warp == 1) tc::tmem_alloc(&tmem_base, kTmemCols);
+  if (warp == 1) tc::tmem_alloc(&tmem_base, 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -260,8 +257,8 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
         const TileInfo ti = tile_info(p, tau);
         const CUtensorMap* cm = ti.e < 0 ? &p.codes_sh : &p.codes;
         const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
-        const int arow0 = ebase + weight_row0(p, MODE, sub, 0);
-        const int arow1 = ebase + weight_row0(p, MODE, sub, 1);
+        int arow[2];
+        for (int a = 0; a < NA; ++a) arow[a] = ebase + weight_row0(p, MODE, sub, a);
         bool ok = true;
         for (int ks = 0; ks < ksteps; ++ks) {
           if (f >= CR && !wait_bar(&c_empty[c], ((f / CR) - 1) & 1, abort_p, p.status)) {
@@ -270,8 +267,9 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
           }
           unsigned char* cdst = cring + c * C_STAGE;
           mbar_arrive_expect_tx(&c_full[c], C_STAGE);
-          tc::tma_load_2d(cdst, cm, ks * KB, arow0, &c_full[c]);
-          tc::tma_load_2d(cdst + C_BYTES, cm, ks * KB, arow1, &c_full[c]);
+#pragma unroll
+          for (int a = 0; a < NA; ++a)
+            tc::tma_load_2d(cdst + a * C_BYTES, cm, ks * KB, arow[a], &c_full[c]);
           ++f;
           c = (c + 1 == CR) ? 0 : c + 1;
         }
@@ -319,51 +317,43 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
       drain_stages(b_full, BR, f);
     }
     __syncwarp();
-  } else if (warp == 3) {
-    // ---------------------------------------- gate_up: zero the accumulator
-    if (MODE == kGateUp) {
-      float4* y4 = reinterpret_cast<float4*>(p.yacc);
-      const size_t n4 = (size_t)p.T * p.H / 4;
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (size_t i = (size_t)blockIdx.x * 32 + lane; i < n4; i += (size_t)gridDim.x * 32)
-        y4[i] = z;
-    }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
+      int b = 0, a = 0, j = 0;
       uint32_t f = 0;
-      int j = 0;
       for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x, ++j) {
         const int tau = item / p.nsub;
         const TileInfo ti = tile_info(p, tau);
-        if (j >= 1 && !wait_bar(&acc_empty, (j - 1) & 1, abort_p, p.status)) break;
+        const int ab = j & 1;  // accumulator buffer
+        if (j >= 2 && !wait_bar(&acce_bar[ab], ((j >> 1) - 1) & 1, abort_p, p.status)) break;
         tc::tc_fence_after();
-        // D[weight row, token]: M = 128 weight rows per tile, N = the block
-        const uint32_t idesc = tc::idesc_f16_m128(ti.n);
+        // D[token row, weight row]: M = 128 token rows, N = 256 weight rows
+        const uint32_t idesc = tc::idesc_f16_m128(NA * BM);
+        const uint32_t dbase = tmem + ab * 256;
         bool ok = true;
         for (int ks = 0; ks < ksteps; ++ks) {
-          const int b = (int)(f % BR), s = (int)(f % kAst);
           if (!wait_bar(&b_full[b], (f / BR) & 1, abort_p, p.status) ||
-              !wait_bar(&a_full[s], (f / kAst) & 1, abort_p, p.status)) {
+              !wait_bar(&a_full[a], (f / AST) & 1, abort_p, p.status)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
+          const uint32_t a0 = smem_u32(aring + a * A_STAGE);
           const uint32_t b0 = smem_u32(bring + b * B_BYTES);
-          const uint32_t a0 = tmem + kAcol + (uint32_t)s * 64;
+          // the two weight tiles of a stage are one 256-row K-major operand
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bd = tc::sw128_desc(b0 + kk * 32);
-            const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
-            tc::mma_f16_tmem_a(tmem, a0 + kk * 8, bd, idesc, acc);
-            tc::mma_f16_tmem_a(tmem + BN, a0 + 32 + kk * 8, bd, idesc, acc);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16(dbase, tc::sw128_desc(b0 + kk * 32), tc::sw128_desc(a0 + kk * 32),
+                        idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&b_empty[b]);
-          tc::mma_commit(&a_empty[s]);
+          tc::mma_commit(&a_empty[a]);
           ++f;
+          b = (b + 1 == BR) ? 0 : b + 1;
+          a = (a + 1 == AST) ? 0 : a + 1;
         }
         if (!ok) break;
-        tc::mma_commit(&acc_full);
+        tc::mma_commit(&accf_bar[ab]);
       }
       // every MMA issued has completed before tensor memory is freed
       tc::mma_commit(&mma_done);
@@ -373,17 +363,16 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------- dequant
     const int d = threadIdx.x - 128;
-    const int am = d >> 7;        // weight tile
-    const int m = d & 127;        // row of the tile = tensor-memory lane
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    int c = 0;
+    const int am = d >> 7;   // weight tile
+    const int rw = d & 127;  // row of the tile
+    constexpr int kInChunks = 4;  // 16 codes per chunk
+    int c = 0, a = 0;
     uint32_t f = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      if (warp_aborted(abort_p)) break;
+    for (int item = blockIdx.x; item < total && !*abort_p; item += gridDim.x) {
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
       const int ebase = ti.e < 0 ? 0 : ti.e * p.R;
-      const int row = ebase + weight_row0(p, MODE, sub, am) + m;
+      const int row = ebase + weight_row0(p, MODE, sub, am) + rw;
       // this row's block constants, one 32-bit word per K step, fetched one
       // group of 8 K steps ahead: Q8_0 the two block scales (4-byte aligned
       // for any K % 64 == 0), affine-4 the group's scale | bias << 16
@@ -411,69 +400,59 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           if (kg + jj >= ksteps) break;
-          const int s = (int)(f % kAst);
-          const bool got =
-              wait_bar(&c_full[c], (f / CR) & 1, abort_p, p.status) &&
-              (f < kAst || wait_bar(&a_empty[s], ((f / kAst) - 1) & 1, abort_p, p.status));
-          if (!__all_sync(0xffffffffu, got)) {
+          if (!wait_bar(&c_full[c], (f / CR) & 1, abort_p, p.status) ||
+              (f >= AST && !wait_bar(&a_empty[a], ((f / AST) - 1) & 1, abort_p, p.status))) {
             ok = false;
             break;
           }
-          tc::tc_fence_after();
           const uint32_t sc2 = cur[jj];
-          const unsigned char* tile = cring + c * C_STAGE + am * C_BYTES;
-          uint32_t w[32];
+          const unsigned char* codes = cring + c * C_STAGE + am * C_BYTES + rw * KB;
+          unsigned char* arow_s = aring + a * A_STAGE + am * A_BYTES + (rw >> 3) * 1024 +
+                                  (rw & 7) * 128;
           if (QT == QSM_AFFINE4_G64) {
-            // 32 bytes a row, 32-byte swizzle: 16-byte unit u at u ^ ((m >> 2) & 1)
-            const unsigned char* rp = tile + m * 32;
-            const int sw = (m >> 2) & 1;
-            const uint4 w0 = *reinterpret_cast<const uint4*>(rp + ((0 ^ sw) << 4));
-            const uint4 w1 = *reinterpret_cast<const uint4*>(rp + ((1 ^ sw) << 4));
+            // word i holds K 8i..8i+7: one 16-byte output chunk each
             const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(sc2 & 0xffffu)));
             const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(sc2 >> 16)));
+            const uint4 w0 = *reinterpret_cast<const uint4*>(codes);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(codes + 16);
             const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint4 o = a4_word_to_f16x8(wv[i], s2, b2);
-              w[4 * i] = o.x;
-              w[4 * i + 1] = o.y;
-              w[4 * i + 2] = o.z;
-              w[4 * i + 3] = o.w;
-            }
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(arow_s + ((i ^ (rw & 7)) << 4)) =
+                  a4_word_to_f16x8(wv[i], s2, b2);
           } else {
-            // 64 bytes a row, 64-byte swizzle: 16-byte unit u at u ^ ((m >> 1) & 3)
-            const unsigned char* rp = tile + m * 64;
-            const int sw = (m >> 1) & 3;
-            uint4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(rp + ((u ^ sw) << 4));
+          for (int j = 0; j < kInChunks; ++j) {
+            // chunk order per row: conflict-free shared-memory banks for the
+            // code reads (8 rows per quarter warp, 64-byte row pitch) and the
+            // swizzled fp16 writes alike
+            const int ci = j ^ (int)((0x5FA0u >> (2 * (rw & 7))) & 3u);
+            const uint4 v = *reinterpret_cast<const uint4*>(codes + ci * 16);
+            const uint32_t sbits = (ci < 2) ? (sc2 & 0xffffu) : (sc2 >> 16);
+            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sbits));
+            uint32_t o[8];
+            s8x4_to_f16x2x2(v.x, o[0], o[1]);
+            s8x4_to_f16x2x2(v.y, o[2], o[3]);
+            s8x4_to_f16x2x2(v.z, o[4], o[5]);
+            s8x4_to_f16x2x2(v.w, o[6], o[7]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t sbits = (u < 2) ? (sc2 & 0xffffu) : (sc2 >> 16);
-              const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)sbits));
-              s8x4_to_f16x2x2(v[u].x, w[8 * u + 0], w[8 * u + 1]);
-              s8x4_to_f16x2x2(v[u].y, w[8 * u + 2], w[8 * u + 3]);
-              s8x4_to_f16x2x2(v[u].z, w[8 * u + 4], w[8 * u + 5]);
-              s8x4_to_f16x2x2(v[u].w, w[8 * u + 6], w[8 * u + 7]);
-#pragma unroll
-              for (int t = 0; t < 8; ++t) {
-                __half2 h = __hmul2(*reinterpret_cast<__half2*>(&w[8 * u + t]), s2);
-                w[8 * u + t] = *reinterpret_cast<uint32_t*>(&h);
-              }
+            for (int t = 0; t < 8; ++t) {
+              __half2 h = __hmul2(*reinterpret_cast<__half2*>(&o[t]), s2);
+              o[t] = *reinterpret_cast<uint32_t*>(&h);
             }
+            const int oc0 = 2 * ci, oc1 = 2 * ci + 1;  // 16-byte output chunks
+            *reinterpret_cast<uint4*>(arow_s + ((oc0 ^ (rw & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(arow_s + ((oc1 ^ (rw & 7)) << 4)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
           }
-          tc::tmem_st32(tmem + lane_base + kAcol + (uint32_t)s * 64 + (uint32_t)am * 32, w);
-          tc::tmem_wait_st(w);
-          // The code slot is released only after the store, whose operands
-          // are computed from every byte this thread loaded from it: an
-          // arrive placed right after the loads could be issued while a
-          // load is still in flight, and the next copy into the slot would
-          // then overwrite its first rows under the reader.
+          }
           tc::mbar_arrive(&c_empty[c]);
-          tc::tc_fence_before();
-          tc::mbar_arrive(&a_full[s]);
+          tc::fence_async_smem();
+          tc::mbar_arrive(&a_full[a]);
           ++f;
           c = (c + 1 == CR) ? 0 : c + 1;
+          a = (a + 1 == AST) ? 0 : a + 1;
         }
       }
       if (!ok) break;
@@ -481,76 +460,80 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
     const int q4 = warp & 3;
-    const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16);
+    const int et = threadIdx.x - 384;  // 0..127
     int j = 0;
     bool bad = false;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++j) {
       if (warp_aborted(abort_p)) break;
       const int tau = item / p.nsub, sub = item - tau * p.nsub;
       const TileInfo ti = tile_info(p, tau);
-      if (!__all_sync(0xffffffffu, wait_bar(&acc_full, j & 1, abort_p, p.status))) break;
+      const int b = j & 1;
+      // this thread's token row of the tile: its sorted row (gate_up) or
+      // its token and routing weight (down)
+      const bool live = et < ti.cnt;
+      const int srow = (ti.e < 0 ? p.T * p.k : 0) + ti.row0 + et;
+      int tok = 0;
+      float wt = 0.f;
+      if (MODE == kDown && live) {
+        if (ti.e < 0) {  // shared expert: weight 1, or its gate
+          tok = ti.row0 + et;
+          wt = (p.gate ? __ldcg(p.gate + tok) : 1.f) * kHScaleInv;
+        } else {
+          const int asg = __ldcg(p.perm + ti.row0 + et);
+          tok = asg / p.k;
+          wt = __ldcg(p.topk_w + asg) * kHScaleInv;
+        }
+      }
+      if (!__all_sync(0xffffffffu, wait_bar(&accf_bar[b], (j >> 1) & 1, abort_p, p.status)))
+        break;
       tc::tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + b * 256;
       if (MODE == kGateUp) {
-        // lane = intermediate index; columns = the block's tokens
-        const int ji = sub * BW + 32 * q4 + lane;
-        const int srow0 = (ti.e < 0 ? p.T * p.k : 0) + ti.row0;
-        for (int c0 = 0; c0 < ti.n; c0 += 16) {
-          uint32_t gr[16], ur[16];
-          tc::tmem_ld16_nowait(taddr + c0, gr);
-          tc::tmem_ld16_nowait(taddr + BN + c0, ur);
-          tc::tmem_wait_ld(gr, ur);
+        // columns 0..127 gate, 128..255 up of intermediates sub*128 + c
+        __half* dst = p.hbuf + (size_t)srow * p.I + sub * BM;
+        for (int c0 = 0; c0 < BM; c0 += 16) {
+          float gv[16], uv[16];
+          tc::tmem_ld16(taddr + c0, gv);
+          tc::tmem_ld16(taddr + BM + c0, uv);
+          if (live) {
+            uint32_t hw[8];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            if (c0 + t < ti.cnt) {
-              const float g = __uint_as_float(gr[t]), u = __uint_as_float(ur[t]);
-              const float h = silu(g) * u * kHScale;
-              if (!(fabsf(h) <= 65504.f)) bad = true;
-              const size_t r = (size_t)(srow0 + c0 + t);
-              p.hbuf[r * p.I + ji] = __float2half_rn(h);
-              if (p.gu_dump) {
-                p.gu_dump[r * 2 * p.I + ji] = g;
-                p.gu_dump[r * 2 * p.I + p.I + ji] = u;
+            if (p.gu_dump) {  // test hook: the fused projection's values per h row
+              float* dr = p.gu_dump + (size_t)srow * 2 * p.I + sub * BM + c0;
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                dr[c] = gv[c];
+                dr[p.I + c] = uv[c];
               }
             }
+            for (int c = 0; c < 16; c += 2) {
+              const float h0 = silu(gv[c]) * uv[c] * kHScale;
+              const float h1 = silu(gv[c + 1]) * uv[c + 1] * kHScale;
+              if (!(fabsf(h0) <= 65504.f) || !(fabsf(h1) <= 65504.f)) bad = true;
+              const __half2 hh = __floats2half2_rn(h0, h1);
+              hw[c / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+            d4[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            d4[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
       } else {
-        // lane = output row of each tile; columns = the block's tokens
-        const int r0 = 2 * sub * BW + 32 * q4 + lane;
-        for (int c0 = 0; c0 < ti.n; c0 += 16) {
-          // token and routing weight (x16: h is stored / 16) of block row
-          // c0 + lane, for lanes < 16, then shared across the warp
-          int tok_l = 0;
-          float wt_l = 0.f;
-          if (lane < 16 && c0 + lane < ti.cnt) {
-            const int i = c0 + lane;
-            if (ti.e < 0) {  // shared expert: weight 1, or its gate
-              tok_l = ti.row0 + i;
-              wt_l = (p.gate ? __ldcg(p.gate + tok_l) : 1.f) * kHScaleInv;
-            } else {
-              const int asg = __ldcg(p.perm + ti.row0 + i);
-              tok_l = asg >= 0 ? min(asg / p.k, p.T - 1) : 0;
-              wt_l = asg >= 0 ? __ldcg(p.topk_w + asg) * kHScaleInv : 0.f;
-            }
-          }
-          uint32_t d0[16], d1[16];
-          tc::tmem_ld16_nowait(taddr + c0, d0);
-          tc::tmem_ld16_nowait(taddr + BN + c0, d1);
-          tc::tmem_wait_ld(d0, d1);
+        // 16 consecutive output rows per load: four 16-byte reduce-adds
+        float* dst = p.yacc + (size_t)tok * p.H + sub * (NA * BM);
+        for (int c0 = 0; c0 < NA * BM; c0 += 16) {
+          float dv[16];
+          tc::tmem_ld16(taddr + c0, dv);
+          if (live) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const int tok = __shfl_sync(0xffffffffu, tok_l, t);
-            const float wt = __shfl_sync(0xffffffffu, wt_l, t);
-            if (c0 + t < ti.cnt) {
-              float* yr = p.yacc + (size_t)tok * p.H + r0;
-              red_add(yr, wt * __uint_as_float(d0[t]));
-              red_add(yr + BW, wt * __uint_as_float(d1[t]));
-            }
+            for (int v = 0; v < 4; ++v)
+              red_add_v4(dst + c0 + 4 * v, wt * dv[4 * v], wt * dv[4 * v + 1],
+                         wt * dv[4 * v + 2], wt * dv[4 * v + 3]);
           }
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(&acc_empty);
+      tc::mbar_arrive(&acce_bar[b]);
     }
     if (bad) set_status(p.status, QSM_DEV_FP16_RANGE);
   }
@@ -558,7 +541,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
 // The token operand of gate_up, fp16 [A + T, H] with A = T*k: row r < A
@@ -566,11 +549,12 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
 // valid expert), row A + t holds token t.  One warp per row, its 16-byte
 // chunks loaded four at a time before they are converted and stored.  With
 // a shared-expert gate, the warp of row A + t also forms sigmoid(x[t] .
-// shared_gate) in fp32.
+// shared_gate) in fp32.  Also zeroes the fp32 output accumulator.
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int T,
-            int k, int H, __half* __restrict__ xall, const float* __restrict__ sgate,
-            float* __restrict__ gbuf, int32_t* status) {
+            int k, int H, __half* __restrict__ xall, float* __restrict__ yacc,
+            const float* __restrict__ sgate, float* __restrict__ gbuf,
+            int32_t* status) {
   pdl_wait();
   pdl_launch_dependents();
   bool bad = false;
@@ -582,7 +566,7 @@ prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, in
     int t = r - A;
     if (r < A) {
       const int a = __ldcg(perm + r);
-      t = a >= 0 ? min(a / k, T - 1) : -1;
+      t = a >= 0 ? a / k : -1;
     }
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(t < 0 ? 0 : t) * H);
     uint4* dst = reinterpret_cast<uint4*>(xall + (size_t)r * H);
@@ -626,6 +610,10 @@ prep_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, in
       if (lane == 0) gbuf[t] = 1.0f / (1.0f + __expf(-z));
     }
   }
+  const size_t ny = (size_t)T * H / 4;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < ny; i += stride)
+    reinterpret_cast<float4*>(yacc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (bad) set_status(status, QSM_DEV_FP16_RANGE);
 }
 
@@ -659,16 +647,19 @@ finalize_kernel(const float* __restrict__ yacc, uint16_t* __restrict__ y,
   for (; i < n4; i += stride) finalize_one(__ldcg(src + i), i, y, y32);
 }
 
-// (code ring, token ring) depths in shared memory; the dequantised ring is
-// kAst stages of tensor memory
-constexpr int kGateUpC = 6, kGateUpB = 4;
-constexpr int kDownC = 6, kDownB = 4;
+// (code ring, token ring, dequantised ring) depths
+constexpr int kGateUpC = 4, kGateUpB = 3, kGateUpA = 3;
+constexpr int kDownC = 4, kDownB = 3, kDownA = 3;
 
-template <int QT, int CR, int BR>
+template <int QT, int CR, int BR, int AST>
 constexpr size_t gemm_smem() {
+  constexpr int NA = 2;
   constexpr int KB = QT == QSM_Q8_0 ? BK : BK / 2;
-  return (size_t)BR * BN * BK * 2 + (size_t)CR * 2 * BW * KB + 1024;
+  return (size_t)AST * NA * BM * BK * 2 + (size_t)BR * BN * BK * 2 +
+         (size_t)CR * NA * BM * KB + 1024;
 }
+
+
 
 int sm_count() {
   static int n[64] = {0};
@@ -685,11 +676,11 @@ int sm_count() {
 
 template <int QT>
 qsm_status launch_gemms(const Params& p1, const Params& p2, cudaStream_t stream) {
-  constexpr size_t smem1 = gemm_smem<QT, kGateUpC, kGateUpB>();
-  constexpr size_t smem2 = gemm_smem<QT, kDownC, kDownB>();
-  static_assert(smem1 <= 220 * 1024 && smem2 <= 220 * 1024, "shared memory");
-  auto* k1 = moe_prefill_gemm<kGateUp, QT, kGateUpC, kGateUpB>;
-  auto* k2 = moe_prefill_gemm<kDown, QT, kDownC, kDownB>;
+  constexpr size_t smem1 = gemm_smem<QT, kGateUpC, kGateUpB, kGateUpA>();
+  constexpr size_t smem2 = gemm_smem<QT, kDownC, kDownB, kDownA>();
+  static_assert(smem1 <= 225 * 1024 && smem2 <= 225 * 1024, "shared memory");
+  auto* k1 = moe_prefill_gemm<kGateUp, QT, kGateUpC, kGateUpB, kGateUpA>;
+  auto* k2 = moe_prefill_gemm<kDown, QT, kDownC, kDownB, kDownA>;
   QSM_CUDA_TRY(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem1));
   QSM_CUDA_TRY(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -749,21 +740,20 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   }
 
   QSM_CUDA_TRY(launch_pdl(prep_kernel, dim3(4 * nsm), dim3(256), 0, stream, x,
-                          (const int32_t*)g->perm, T, k, H, xall, L->shared_gate, gbuf,
-                          dev_status));
+                          (const int32_t*)g->perm, T, k, H, xall, yacc, L->shared_gate,
+                          gbuf, dev_status));
 
-  // code tiles: 64 K per step = 64 bytes (Q8_0, 64-byte swizzle) or 32 bytes
-  // (affine-4, 32-byte swizzle) a row, 128 rows
+  // code tiles: 64 K per step = 64 bytes (Q8_0) or 32 bytes (affine-4) a row
   const bool a4 = L->gate_up.qtype == QSM_AFFINE4_G64;
   const int kb = a4 ? BK / 2 : BK;
-  const CUtensorMapSwizzle csw = a4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
   auto code_cols = [&](int K) { return (uint64_t)(a4 ? K / 2 : K); };
   Params p1 = {};
   bool ok = true;
   ok &= tc::make_map_2d(&p1.codes, L->gate_up.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                        (uint64_t)E * 2 * I, code_cols(H), kb, BW, csw);
+                        (uint64_t)E * 2 * I, code_cols(H), kb, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok &= tc::make_map_2d(&p1.codes_sh, L->shared_gate_up.codes,
-                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, code_cols(H), kb, BW, csw);
+                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, 2 * I, code_cols(H), kb, BM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   for (int m = 0; m < 4; ++m)
     ok &= tc::make_map_2d(&p1.bmap[m], xall, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, H,
                           BK, BN >> m, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -784,7 +774,7 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   p1.n_tiles = g->n_tiles;
   p1.topk_w = topk_w;
   p1.shared_tiles = (T + BN - 1) / BN;
-  p1.nsub = I / BW;
+  p1.nsub = I / BM;
   p1.hbuf = hbuf;
   p1.yacc = yacc;
   p1.gate = L->shared_gate ? gbuf : nullptr;
@@ -793,9 +783,10 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
 
   Params p2 = p1;
   ok &= tc::make_map_2d(&p2.codes, L->down.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                        (uint64_t)E * H, code_cols(I), kb, BW, csw);
+                        (uint64_t)E * H, code_cols(I), kb, BM, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok &= tc::make_map_2d(&p2.codes_sh, L->shared_down.codes,
-                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, code_cols(I), kb, BW, csw);
+                        CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, H, code_cols(I), kb, BM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   for (int m = 0; m < 4; ++m)
     ok &= tc::make_map_2d(&p2.bmap[m], hbuf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rows_h, I,
                           BK, BN >> m, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -806,7 +797,7 @@ qsm_status prefill_ffn_launch(const qsm_moe_layer* L, const uint16_t* x, int T,
   p2.biases_sh = reinterpret_cast<const __half*>(L->shared_down.biases);
   p2.R = H;
   p2.K = I;
-  p2.nsub = H / (2 * BW);
+  p2.nsub = H / (2 * BM);
   p2.gu_dump = nullptr;
 
   const qsm_status st = a4 ? launch_gemms<QSM_AFFINE4_G64>(p1, p2, stream)
