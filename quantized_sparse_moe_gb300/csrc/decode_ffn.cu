@@ -94,8 +94,9 @@ __device__ __forceinline__ void load_batch(RawA (&r)[kPre], const QW& w, int rg,
 // arrive by TMA bulk copies (one per row, into rows padded by kRowPad bytes
 // so the MMA fragment reads are free of bank conflicts), tracked by one
 // mbarrier; the shared expert's CTAs start their copies before waiting on
-// the routing.  The CTA also asks L2 to prefetch its share of the expert's
-// down-projection rows, which the next launch streams.
+// the routing.  While the layer's weights fit in L2 beside each other, the
+// CTA also asks L2 to prefetch its share of the expert's down-projection
+// rows, which the next launch streams.
 
 constexpr int kRowPad = 32;
 
@@ -133,7 +134,7 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
                   const int32_t* __restrict__ tile_map, int shared_slots,
                   int xrows, __half* __restrict__ hbuf,
                   const float* __restrict__ sgate, float* __restrict__ gbuf,
-                  float* __restrict__ gu_dump, int32_t* dev_status) {
+                  float* __restrict__ gu_dump, int prefetch, int32_t* dev_status) {
   extern __shared__ __align__(128) unsigned char d1_smem[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ float red[kD1Split][32][4];
@@ -167,7 +168,7 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
   };
   // L2 prefetch of this CTA's 1/gridDim.x share of the expert's down rows.
   auto prefetch_down = [&](const QW& d) {
-    if (kw == 1 && lane == 0) {
+    if (prefetch && kw == 1 && lane == 0) {
       const int drow = code_row_bytes<QT>(I);
       const int rows = H / gridDim.x;  // H is a multiple of 16, grid = I/8
       if (rows > 0 && (rows * drow) % 16 == 0) {
@@ -523,6 +524,14 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
     if (g_gu_dump_floats < ((size_t)T * k + T) * 2 * I) return QSM_ERR_INVALID_ARGUMENT;
     gu_dump = g_gu_dump;
   }
+  // d1 asks L2 for the down rows of its experts, which d2 streams next, only
+  // while the layer's touched weights fit in L2 beside each other: past that
+  // the gate_up stream evicts them before d2 runs and they are read twice.
+  const size_t row_bytes_gu = QT == QSM_Q8_0 ? H + H / 32 * 2 : H / 2 + H / 64 * 4;
+  const size_t row_bytes_dn = QT == QSM_Q8_0 ? I + I / 32 * 2 : I / 2 + I / 64 * 4;
+  const size_t experts = (size_t)(T * k < L->E ? T * k : L->E) + 1;
+  const size_t touched = experts * (2 * (size_t)I * row_bytes_gu + (size_t)H * row_bytes_dn);
+  const int prefetch_down = touched <= ((size_t)48 << 20) ? 1 : 0;
   const dim3 g1(I / kTok, shared_slots + g->max_tiles);
   const int xrows = T < kTok ? T : kTok;
   const int crow = QT == QSM_Q8_0 ? H : H / 2;
@@ -543,7 +552,7 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
                           L->shared_down, x, T, H, I, k, (const int32_t*)g->perm,
                           (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
                           shared_slots, xrows, hbuf, L->shared_gate, gbuf, gu_dump,
-                          dev_status));
+                          prefetch_down, dev_status));
   QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem2));

@@ -165,10 +165,12 @@ group_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM, int max
   }
 }
 
-// Few assignments (decode): the per-warp histogram machinery above costs
-// more than the work.  Thread e owns expert e and walks the (at most
-// kSmallA) assignments in shared memory twice: once to count, once to place
-// its rows in assignment order (stable by construction).
+// Few assignments (decode): one CTA.  The ids go to shared memory, the
+// threads count them with shared-memory atomics, a block scan gives the
+// offsets and the block map (thread e owns expert e), and one warp places
+// the assignments 32 at a time in assignment order: the lanes holding the
+// same expert (match.any) take consecutive positions in lane order after
+// those the earlier groups placed, which keeps the permutation stable.
 constexpr int kSmallA = 1024;
 
 template <int NT>  // threads: a multiple of 32 and >= E
@@ -180,11 +182,13 @@ group_small_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
                    int32_t* __restrict__ tile_map,
                    int32_t* __restrict__ n_tiles, int32_t* dev_status) {
   __shared__ int sidx[kSmallA];
+  __shared__ int scnt[NT];   // per expert: count, then the next free position
   __shared__ int warp_tot[32];
   __shared__ int s_total, s_tiles;
   pdl_wait();
   pdl_launch_dependents();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  scnt[tid] = 0;
   bool bad = false;
   for (int a = tid; a < A; a += NT) {
     int v = __ldcg(topk_idx + a);
@@ -197,11 +201,12 @@ group_small_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
   }
   if (__syncthreads_or(bad) && tid == 0)
     set_status(dev_status, QSM_DEV_BAD_EXPERT_ID);
+  for (int a = tid; a < A; a += NT)
+    if (sidx[a] >= 0) atomicAdd(&scnt[sidx[a]], 1);
+  __syncthreads();
   const int e = tid;
-  int cnt = 0;
-  if (e < E)
-    for (int a = 0; a < A; ++a) cnt += (sidx[a] == e);
-  const int off = block_exclusive_scan(e < E ? cnt : 0, warp_tot, &s_total);
+  const int cnt = e < E ? scnt[e] : 0;
+  const int off = block_exclusive_scan(cnt, warp_tot, &s_total);
   const int nt = (e < E) ? (cnt + BM - 1) / BM : 0;
   const int t0 = block_exclusive_scan(nt, warp_tot, &s_tiles);
   if (e < E) {
@@ -211,13 +216,24 @@ group_small_kernel(const int32_t* __restrict__ topk_idx, int A, int E, int BM,
       tile_map[2 * (t0 + m)] = e;
       tile_map[2 * (t0 + m) + 1] = off + m * BM;
     }
-    int pos = off;
-    for (int a = 0; a < A && pos < off + cnt; ++a) {
-      if (sidx[a] == e) {
+    scnt[e] = off;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const unsigned lower = (1u << lane) - 1u;
+    for (int a0 = 0; a0 < A; a0 += 32) {
+      const int a = a0 + lane;
+      const int key = a < A ? sidx[a] : -2;  // -1: bad id, -2: past the end
+      const unsigned same = __match_any_sync(0xffffffffu, key);
+      const int base = key >= 0 ? scnt[key] : 0;
+      __syncwarp();  // every lane has read its expert's position
+      if (key >= 0) {
+        const int pos = base + __popc(same & lower);
         perm[pos] = a;
         inv_perm[a] = pos;
-        ++pos;
+        if (lane == 31 - __clz(same)) scnt[key] = base + __popc(same);
       }
+      __syncwarp();
     }
   }
   if (tid == 0) {
