@@ -70,6 +70,10 @@ WORKLOADS = {
                        desc="prefill T=4096, 1 layer, Zipf-offset routing, affine-4 g64"),
     "gemv": dict(gemv="f16", desc="Q8_0 GEMV batch 1, Llama-3.2-1B projection shapes "
                                   "(2048x2048, 512x2048, 8192x2048, 2048x8192, 128256x2048)"),
+    "gemv_layer": dict(gemv="f16", shapes="layer",
+                       desc="Q8_0 GEMV batch 1, one Llama-3.2-1B layer's projections with "
+                            "shared-activation stacking (QKV 3072x2048, O 2048x2048, gate_up "
+                            "16384x2048, down 2048x8192) and the LM head 128256x2048"),
     "gemv_i8": dict(gemv="i8", desc="Q8_0 GEMV batch 1 on the int8-quantized activation, "
                                     "Llama-3.2-1B projection shapes"),
 }
@@ -587,6 +591,13 @@ def run_reference(args, wl, rank, world):
 
 # --------------------------------------------------------------- GEMV sweep
 
+def gemv_metric(wl):
+    if wl.get("shapes") == "layer":
+        return ("Q8_0 GEMV weight GB/s (one GEMV per stacked projection of a layer and the "
+                "LM head per step)")
+    return "Q8_0 GEMV weight GB/s (one GEMV per projection shape per step)"
+
+
 def run_gemv(args, wl, rank, world):
     """One step = one batch-1 GEMV per Llama-3.2-1B projection shape.  The
     matrices that fit in L2 rotate over copies so a step's weights exceed
@@ -595,7 +606,8 @@ def run_gemv(args, wl, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     i8 = wl["gemv"] == "i8"
-    shapes = list(synth.GEMV_SHAPES.items())
+    shapes = list((synth.GEMV_LAYER_SHAPES if wl.get("shapes") == "layer"
+                   else synth.GEMV_SHAPES).items())
     small = sum(n * k for name, (n, k) in shapes if name != "lm_head") * 34 // 32
     R = max(1, -(-4 * 129_000_000 // small))  # copies of the L2-sized matrices
     mats = {}
@@ -698,7 +710,7 @@ def run_gemv(args, wl, rank, world):
             e_ms.append((time.perf_counter() - t0) * 1e3)
     e2e_ms = statistics.median(e_ms)
     result = {
-        "metric": "Q8_0 GEMV weight GB/s (one GEMV per projection shape per step)",
+        "metric": gemv_metric(wl),
         "value": world * step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -799,12 +811,14 @@ def main():
             if rank == 0:
                 import quantized_sparse_moe_gb300  # noqa: F401 (device init only)
                 dev = torch.device("cuda", 0)
+                shapes = (synth.GEMV_LAYER_SHAPES if wl.get("shapes") == "layer"
+                          else synth.GEMV_SHAPES)
                 mats = {name: [synth.draw_gemv(n, k, dev, seed=0, name=name)]
-                        for name, (n, k) in synth.GEMV_SHAPES.items()}
+                        for name, (n, k) in shapes.items()}
                 cb = gemv_cpu_baseline(wl, mats, budget_s=min(60.0, max(
                     5.0, 90.0 * args.steps / (args.steps + args.warmup))))
-                res = {"impl": "reference", "metric": "Q8_0 GEMV weight GB/s (one GEMV per "
-                       "projection shape per step)", "value": cb["value"], "unit": "GB/s",
+                res = {"impl": "reference", "metric": gemv_metric(wl),
+                       "value": cb["value"], "unit": "GB/s",
                        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                        "dtype": "f64", "data": "synthetic", "config": {"workload": wl["desc"]},

@@ -57,6 +57,17 @@ GEMV_SHAPES = {
     "lm_head": (128256, 2048),
 }
 
+# The same projections as one layer's calls, those that read the same
+# activation stacked into one matrix: Q, K and V (2048 + 512 + 512 rows) and
+# gate and up (8192 + 8192 rows); then O, down and the LM head.
+GEMV_LAYER_SHAPES = {
+    "qkv": (3072, 2048),
+    "o": (2048, 2048),
+    "gate_up": (16384, 2048),
+    "down": (2048, 8192),
+    "lm_head": (128256, 2048),
+}
+
 
 def sub_seed(seed: int, *parts) -> int:
     """A stable 63-bit seed for one named tensor."""

@@ -24,9 +24,15 @@ def assert_faithful_bf16(y, ref):
     assert tol_metric(y, ref) <= 2.0 ** -8
 
 
-@pytest.mark.parametrize("name", sorted(synth.GEMV_SHAPES))
+# the config's five shapes and the stacked ones of a layer (QKV, gate_up)
+_SHAPES = dict(synth.GEMV_SHAPES)
+_SHAPES.update({"layer_" + k: v for k, v in synth.GEMV_LAYER_SHAPES.items()
+                if v not in synth.GEMV_SHAPES.values()})
+
+
+@pytest.mark.parametrize("name", sorted(_SHAPES))
 def test_gemv_shapes(qsm, name):
-    N, K = synth.GEMV_SHAPES[name]
+    N, K = _SHAPES[name]
     x, q, d = synth.draw_gemv(N, K, "cuda", seed=3, name=name)
     y = qsm.q8_gemv(x, q, d)
     torch.cuda.synchronize()
@@ -60,6 +66,20 @@ def test_fused_gate_up_rows_bit_identical(qsm):
     u = qsm.q8_gemv(x, uq, ud)
     torch.cuda.synchronize()
     assert torch.equal(fused.view(torch.int16), torch.cat([g, u]).view(torch.int16))
+
+
+def test_stacked_qkv_rows_bit_identical(qsm):
+    """Projections that read the same activation, stacked into one matrix
+    (Q 2048, K 512 and V 512 rows of a Llama-3.2-1B layer), give per row the
+    bits of the separate calls."""
+    K = 2048
+    x, qq, qd = synth.draw_gemv(2048, K, "cuda", seed=7, name="q")
+    _, kq, kd = synth.draw_gemv(512, K, "cuda", seed=8, name="k")
+    _, vq, vd = synth.draw_gemv(512, K, "cuda", seed=9, name="v")
+    fused = qsm.q8_gemv(x, torch.cat([qq, kq, vq]), torch.cat([qd, kd, vd]))
+    parts = [qsm.q8_gemv(x, a, b) for a, b in ((qq, qd), (kq, kd), (vq, vd))]
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), torch.cat(parts).view(torch.int16))
 
 
 def test_gemv_ragged_rows(qsm):
