@@ -25,6 +25,7 @@
 // non-finite or out-of-range value sets QSM_DEV_FP16_RANGE.
 #include <utility>
 
+#include "decode_stream.cuh"
 #include "gemv_core.cuh"
 
 namespace qsm {
@@ -544,15 +545,23 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
   const size_t kSmemBudget = 200 * 1024;
   while (w2 > 1 && (size_t)w2 * (geo.slot + slab_bytes_per_warp) > kSmemBudget) --w2;
   const size_t smem2 = (size_t)w2 * (geo.slot + slab_bytes_per_warp);
-  QSM_CUDA_TRY(cudaFuncSetAttribute(d1_gate_up_swiglu<QT>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem1));
-  QSM_CUDA_TRY(launch_pdl(d1_gate_up_swiglu<QT>, g1, dim3(kD1Split * 32), smem1,
-                          stream, L->gate_up, L->shared_gate_up, L->down,
-                          L->shared_down, x, T, H, I, k, (const int32_t*)g->perm,
-                          (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
-                          shared_slots, xrows, hbuf, L->shared_gate, gbuf, gu_dump,
-                          prefetch_down, dev_status));
+  if (T > kTok && gate_up_stream_supported(L)) {
+    // several slots: one persistent pass streams every touched expert's
+    // gate_up rows once per slot, each slot's x rows staged once per CTA
+    const qsm_status st = gate_up_stream_launch(L, x, T, g, shared_slots, hbuf, gbuf, gu_dump,
+                                                dev_status, stream);
+    if (st != QSM_OK) return st;
+  } else {
+    QSM_CUDA_TRY(cudaFuncSetAttribute(d1_gate_up_swiglu<QT>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem1));
+    QSM_CUDA_TRY(launch_pdl(d1_gate_up_swiglu<QT>, g1, dim3(kD1Split * 32), smem1,
+                            stream, L->gate_up, L->shared_gate_up, L->down,
+                            L->shared_down, x, T, H, I, k, (const int32_t*)g->perm,
+                            (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
+                            shared_slots, xrows, hbuf, L->shared_gate, gbuf, gu_dump,
+                            prefetch_down, dev_status));
+  }
   QSM_CUDA_TRY(cudaFuncSetAttribute(d2_down_combine<QT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem2));
