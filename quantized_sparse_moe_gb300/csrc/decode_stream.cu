@@ -49,8 +49,8 @@ namespace dstream {
 
 using namespace gemv;
 
-constexpr int kGW = 8;                  // warps of a consumer group
-constexpr int kNG = 2;                  // consumer groups
+constexpr int kGW = 4;                  // warps of a consumer group
+constexpr int kNG = 4;                  // consumer groups
 constexpr int kCW = kGW * kNG;          // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;
 constexpr int kMaxS = 8;                // ring stages at most (a multiple of kNG)
@@ -59,7 +59,7 @@ constexpr int kTok = 8;                 // tokens per slot (the MMA's N)
 constexpr uint32_t kShortWait = 1u << 10;  // waits after a timeout
 constexpr float kHScale = 1.0f / 16.0f;
 constexpr size_t kSmemBudget = 208 * 1024;  // dynamic shared memory
-constexpr int kBarAll = 3;              // named barrier of all consumer warps
+constexpr int kBarAll = 15;             // named barrier of all consumer warps (groups: 1..kNG)
 
 // Padding (fp16 elements) after each staged x row: the eight rows of an MMA's
 // B fragment then fall in different shared-memory banks for the K offsets
