@@ -438,7 +438,8 @@ def run_ours(args, wl, rank, world):
         "roofline": ({
             "kernel": ("moe_decode_layer (router, selection, gate_up+SwiGLU, "
                        "down+combine in one launch)" if one_launch else
-                       "moe_ffn_forward (d1 gate_up+SwiGLU, d2 down+combine)"),
+                       "moe_ffn_forward (gate_up+SwiGLU "
+                       + ("streamed by one CTA per SM" if T > 8 else "d1") + ", d2 down+combine)"),
             "bound": "hbm", "achieved": achieved, "peak": hbm,
             "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
             "bytes_per_launch": ffn_bytes_per_layer,
