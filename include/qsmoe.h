@@ -75,7 +75,7 @@ typedef enum {
 #define QSM_DEV_NONFINITE 2     /* non-finite router logit */
 #define QSM_DEV_FP16_RANGE 4    /* a value staged in fp16 overflowed */
 #define QSM_DEV_TIMEOUT 8       /* a bounded wait (on a copy, or on the
-                                   logit exchange or a slot counter of
+                                   tagged logits or h of
                                    moe_decode_layer) ran out: the kernel
                                    returned, its results are invalid */
 
@@ -280,9 +280,9 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
                                      cudaStream_t stream);
 
 /* The whole layer for a few tokens (1 <= T <= 8) in one launch: router,
- * selection, gate_up + SwiGLU, down + combine, separated by a grid-wide
- * exchange of call-tagged logits and by per-slot completion counters
- * between gate_up and down, instead of three dependent launches
+ * selection, gate_up + SwiGLU, down + combine, separated by grid-wide
+ * exchanges of call-tagged words (the logits, then h between gate_up and
+ * down), instead of three dependent launches
  * [Perplexity page, "Keeping expert routing on the GPU", "Reducing
  * intermediate and state traffic", "Overlapping independent GPU work"].  Results: topk_idx and topk_w
  * bit-identical to moe_route's; y the layer output as moe_ffn_forward
@@ -291,7 +291,7 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
  *   Arguments as for moe_layer_forward, without a chunk size.
  *   Supported: Q8_0 or affine-4 (all four weight planes alike), H % 256 ==
  *   0, H / 16 <= the device's SM count (a CTA per SM, at least one per 16
- *   output rows, all resident for the logit exchange and the counters),
+ *   output rows, all resident for the two exchanges),
  *   I % 128 == 0 (Q8_0) or % 256 == 0
  *   (affine-4), E <= 1024, k <= 32; all pointers 16-byte aligned except
  *   topk_idx, topk_w, y, y_f32 and logit_bias (4 bytes).  Otherwise
@@ -301,9 +301,10 @@ QSM_API qsm_status moe_layer_forward(const qsm_moe_layer* L, const uint16_t* x,
  *              per CTA): the calls that share a workspace must have the
  *              same layer shape (H, I, E, k), and after a
  *              QSM_DEV_TIMEOUT it must be zeroed again.
- *              Bytes 256..2311 hold two banks of 32-bit slot counters (a
- *              call counts in one and zeroes the other).
- * Every wait in the kernel is bounded: an exchange, counter or copy that
+ *              From byte 256: the tagged logits [8, E] (64-bit words, the
+ *              call's tag in the high half), then h as 64-bit words (tag,
+ *              two fp16 values).
+ * Every wait in the kernel is bounded: an exchange or copy that
  * does not complete sets QSM_DEV_TIMEOUT and the call's results are
  * invalid. */
 QSM_API size_t moe_decode_layer_workspace_bytes(const qsm_moe_layer* L, int32_t T);

@@ -9,9 +9,9 @@
 // "Overlapping independent GPU work"; the fused [gate; up] rows of "oMLX MoE
 // gate/up 融合优化", section "融合原理".  The dependent launches of the
 // decode path (router + grouping, gate_up, down) become three phases of one
-// launch: an exchange of call-tagged logits after the router, and per-slot
-// completion counters between gate_up and down.  No grouping is needed:
-// every CTA derives its work from the selection itself.
+// launch: an exchange of call-tagged logits after the router, and
+// call-tagged h between gate_up and down.  No grouping is needed: every CTA
+// derives its work from the selection itself.
 //
 //   A  CTA c computes the logits of its experts for the T tokens, with the
 //      arithmetic of moe_route (router rows fetched before the
@@ -22,15 +22,17 @@
 //      experts and computes gate_up + SwiGLU for its tiles.  Tile tau =
 //      (slot, 8 intermediates): slot 0 is the shared expert, slot s >= 1
 //      the s-th expert of U; a tile covers all T tokens (pairs that are not
-//      routed are computed and never read).  h goes to the workspace, and
-//      the slot's counter counts the tile.
+//      routed are computed and never read).  h goes to the workspace as
+//      64-bit words (call tag, two fp16 values).
 //   C  CTA c < H / 16 computes rows 16c..16c+15 of y: for every slot, the
 //      down rows times the slot's h, times the token's weight for the
 //      slot's expert (the shared expert's gate, or 1; pairs with weight 0
 //      are skipped), summed over the slots in a fixed order.  The slots go
-//      a few at a time (C items), each as soon as the counters of its slots
-//      are complete, so a CTA with fewer tiles starts on the first slots
-//      while others still compute the last gate_up tiles.  (Placing items
+//      a few at a time (C items); the consumers read an item's h from the
+//      workspace, waiting until its words carry this call's tag (the data
+//      and its readiness in one round trip), so a CTA with fewer tiles
+//      starts on the first slots while others still compute the last
+//      gate_up tiles.  (Placing items
 //      between a CTA's own tiles, as soon as those they need are done, made
 //      every item a grid-wide wait and was slower.)
 //
@@ -49,8 +51,8 @@
 //
 // The grid has one CTA per SM (fewer when the layer has fewer gate_up
 // tiles): CTAs c < H / 16 also own rows of y, the others only gate_up tiles,
-// so that the tiles spread over every SM.  The logit exchange and the
-// counters need all G CTAs resident at once: G is at most the SM count and
+// so that the tiles spread over every SM.  The logit exchange and the h
+// hand-off need all G CTAs resident at once: G is at most the SM count and
 // a launch's CTAs are all running once the launch lets its dependents start
 // (every CTA triggers).  Every wait is bounded; when one runs out the kernel
 // sets QSM_DEV_TIMEOUT, keeps its control flow (later waits are short), lets
@@ -60,9 +62,9 @@
 // calls so far + 1 (calls that share a workspace must have the same layer
 // shape).  A logit travels as one 64-bit word (tag, value): a reader waits
 // until every word of its token carries this call's tag, which is the
-// barrier and the data in one round trip.  The slot counters come in two
-// banks: a call counts in bank tag & 1 and zeroes the other one, which the
-// previous call used.
+// barrier and the data in one round trip; h travels the same way.  Every h
+// word a call reads is written by that call (a gate_up tile covers all T
+// tokens of its slot), so a word of an earlier call never passes.
 //
 // Every phase runs once per launch, so code size matters: loops that run
 // once are not unrolled, and the selection's code is warmed by idle warps
@@ -98,7 +100,6 @@ constexpr int kBarCons = 1;               // named barrier of the consumer warps
 constexpr int kBarGrp = 2;                // + group: named barriers of the gate_up groups
 constexpr int kGW = 8;                    // warps per gate_up group
 constexpr uint32_t kShortWait = 1u << 10; // waits after a timeout
-constexpr int kMaxSlots = kMaxT * 32 + 1; // shared expert + up to T k experts
 
 struct Params {
   CUtensorMap gu, gu_sh;  // gate_up codes, 3D row views, box {128, 8, hb/128}
@@ -126,9 +127,8 @@ struct Params {
   int ns;                 // ring slots
   int slot_bytes, xs_off, sg_off, wr_off, hs_off, hs_bytes, ul_off, wm_off;
   unsigned long long* gbar;  // call ticket: G arrivals per call
-  unsigned* scnt;         // [2][kMaxSlots] gate_up tiles counted per slot
   unsigned long long* logits;  // [kMaxT, E] (call tag << 32) | logit bits
-  __half* hbuf;           // [slots, T, I], h / 16
+  unsigned long long* hbuf;  // [slots, T, I / 2]: (call tag << 32) | fp16 pair of h / 16
   int32_t* topk_idx;
   float* topk_w;
   uint16_t* y;
@@ -154,20 +154,45 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
-// Wait until the counter reaches `target` (acquire).  False when the wait ran out.
-__device__ __forceinline__ bool counter_wait(const unsigned* ctr, unsigned target,
-                                             uint32_t iters) {
-  for (uint32_t i = 0; i < iters; ++i) {
-    if (ld_acquire_u32(ctr) >= target) return true;
-    if (i > 64) __nanosleep(32);
+// One thread's share of an item's h: words src[i] for i = first, first +
+// stride, ... < n, each (call tag << 32) | fp16 pair, into dst[i] once it
+// carries tag `want`; eight loads in flight at a time, the stale ones
+// reloaded.  False when the wait ran out (dst then holds what arrived).
+__device__ __forceinline__ bool stage_h(const unsigned long long* src, uint32_t* dst, int n,
+                                        int first, int stride, uint32_t want, uint32_t iters) {
+  bool ok = true;
+  for (int i0 = first; i0 < n; i0 += 8 * stride) {
+    unsigned long long v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * stride;
+      v[u] = i < n ? ld_relaxed_u64(src + i) : ((unsigned long long)want << 32);
+    }
+    uint32_t stale = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if ((uint32_t)(v[u] >> 32) != want) stale |= 1u << u;
+    for (uint32_t k = 0; stale; ++k) {
+      if (k >= iters) {
+        ok = false;
+        break;
+      }
+      if (k > 8) __nanosleep(32);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (stale & (1u << u)) {
+          v[u] = ld_relaxed_u64(src + i0 + u * stride);
+          if ((uint32_t)(v[u] >> 32) == want) stale &= ~(1u << u);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * stride;
+      if (i < n) dst[i] = (uint32_t)v[u];
+    }
   }
-  return false;
+  return ok;
 }
 
 // One warp: the E tagged logits of a token into dst (shared memory), once
@@ -249,7 +274,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   constexpr int kThreads = (kCW + 1) * 32;
   constexpr int kSubs = kCW * 32 / kTPE;  // experts per router pass
   extern __shared__ unsigned char dl_dyn[];
-  __shared__ __align__(8) uint64_t full[kMaxS], empty[kMaxS], hfull[2], hempty[2];
+  __shared__ __align__(8) uint64_t full[kMaxS], empty[kMaxS];
   __shared__ __align__(8) uint64_t xbar, rdy;
   __shared__ float red[2][kCW][32][4];
   __shared__ float rsum[kSubs][kTPE / 32][kMaxT];
@@ -274,7 +299,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(ring + p.xs_off);  // bf16 [T][H]
   const float* sgs = reinterpret_cast<const float*>(ring + p.sg_off);       // [H]
   const float* wrs = reinterpret_cast<const float*>(ring + p.wr_off);       // [epc][H]
-  unsigned char* hs = ring + p.hs_off;
   int* ulist = reinterpret_cast<int*>(ring + p.ul_off);
   float* wmat = reinterpret_cast<float*>(ring + p.wm_off);  // [(slots)][T]
   constexpr int kBi = QT == QSM_Q8_0 ? 1 : 2;  // scale planes (scales, biases)
@@ -283,10 +307,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCW);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&hfull[b], 1);
-      mbar_init(&hempty[b], kCW);
     }
     mbar_init(&xbar, 1);
     mbar_init(&rdy, 1);
@@ -307,7 +327,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   if (warp == kCW) {
     if (lane != 0) return;
     int nu = 0, nB = 0, items = 0;
-    const unsigned* bank = p.scnt;  // this call's slot counters
     auto expert_of_slot = [&](int s) { return s == 0 ? 0 : ulist[s - 1]; };
     // B tile tau -> ring buffer sb, barrier bar
     auto issue_b = [&](int tau, unsigned char* sb, uint64_t* bar) {
@@ -376,25 +395,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       if (pos < nB) issue_b(c + pos * G, sb, &full[pos % ns]);
       else issue_c(pos - nB, sb, &full[pos % ns]);
     };
-    // h of C item `it`, once every tile of its slots has been counted
-    auto issue_h = [&](int it) {
-      const int s0 = p.m * it, cnt = min(p.m, nu + 1 - s0);
-#pragma unroll 1
-      for (int j = 0; j < cnt; ++j) {
-        if (!counter_wait(bank + s0 + j, (unsigned)tps, s_bad ? kShortWait : kWaitIters)) {
-          s_bad = 1;
-          set_status(p.status, QSM_DEV_TIMEOUT);
-        }
-      }
-      // h was written through the generic proxy; the bulk copy reads it
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      if (it >= 2) wait(&hempty[it & 1], ((it >> 1) - 1) & 1);
-      const uint32_t bytes = (uint32_t)cnt * T * I * 2;
-      mbar_arrive_expect_tx(&hfull[it & 1], bytes);
-      bulk_g2s(hs + (it & 1) * p.hs_bytes, p.hbuf + (size_t)s0 * T * I, bytes, &hfull[it & 1]);
-      return it + 1;
-    };
-
     // before the wait: static weights only (the shared expert's tiles at the
     // head of this CTA's sequence, its down rows, the shared-expert gate)
     int pre = 0;
@@ -424,7 +424,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
 
     wait(&rdy, 0);  // the selection: s_nu, ulist (and s_tag)
     nu = s_nu;
-    bank = p.scnt + (s_tag & 1u) * kMaxSlots;
     const int NT = (nu + 1) * tps;
     nB = c < NT ? (NT - c + G - 1) / G : 0;
     items = c < p.GC ? (nu + 1 + p.m - 1) / p.m : 0;
@@ -444,21 +443,12 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       }
     };
     prefetch_to(ns + win);
-    int hi = 0;  // next C item whose h is copied
 #pragma unroll 1
     for (; pos < total; ++pos) {
-      // the slot's previous position must be consumed; if it was a C item,
-      // its h has to be on its way first
-      const int prev = pos - ns;
-      if (prev >= nB)
-#pragma unroll 1
-        while (hi <= prev - nB) hi = issue_h(hi);
       wait(&empty[pos % ns], ((pos / ns) - 1) & 1);
       issue_pos(pos);
       prefetch_to(pos + 1 + win);
     }
-#pragma unroll 1
-    while (hi < items) hi = issue_h(hi);
     // normally every copy has been consumed; after a timeout, let the last
     // copy of each buffer land before the CTA's shared memory goes away
     if (s_bad) {
@@ -466,11 +456,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       for (int s = 0; s < ns && s < total; ++s) {
         const int last = s + ((total - 1 - s) / ns) * ns;
         mbar_wait_bounded(&full[s], (last / ns) & 1, kWaitIters);
-      }
-#pragma unroll 1
-      for (int b = 0; b < 2 && b < items; ++b) {
-        const int last = b + ((items - 1 - b) / 2) * 2;
-        mbar_wait_bounded(&hfull[b], (last >> 1) & 1, kWaitIters);
       }
     }
     return;
@@ -559,10 +544,6 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       if (lane == 0) sgv[t] = 1.0f / (1.0f + __expf(-z));
     }
   }
-
-  // the previous call's counters, zeroed for the next call
-  if (c == 0)
-    for (int i = tid; i < kMaxSlots; i += kCW * 32) p.scnt[((tag + 1u) & 1u) * kMaxSlots + i] = 0u;
 
   // ---- B: selection (one warp per token), the set U, weights per slot
   // the logits go where the router rows were (phase A's last CTA barrier
@@ -728,23 +709,21 @@ decode_layer_kernel(const __grid_constant__ Params p) {
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int t = 2 * q + cc;
+        const float h = silu(a[cc]) * a[2 + cc] * kHScale;
+        const uint32_t hv = __half_as_ushort(__float2half_rn(h));
+        // intermediates i0 + g (g even) and i0 + g + 1 (lane + 4) share a word
+        const uint32_t hn = __shfl_down_sync(0xffffffffu, hv, 4);
         if (t < T) {
-          const float h = silu(a[cc]) * a[2 + cc] * kHScale;
           if (!(fabsf(h) <= 65504.f)) range_bad = true;
-          p.hbuf[((size_t)s * T + t) * I + i0 + g] = __float2half_rn(h);
+          if ((g & 1) == 0)
+            st_relaxed_u64(p.hbuf + (((size_t)s * T + t) * I + i0 + g) / 2,
+                           ((unsigned long long)tag << 32) | (hn << 16) | hv);
           if (p.gu_dump) {  // test hook: the fused projection's values per h row
             p.gu_dump[((size_t)s * T + t) * 2 * I + i0 + g] = a[cc];
             p.gu_dump[((size_t)s * T + t) * 2 * I + I + i0 + g] = a[2 + cc];
           }
         }
       }
-      // count the tile (release: the warp's h stores, ordered before by
-      // the warp barrier, become visible first)
-      __syncwarp();
-      if (lane == 0)
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(
-                         p.scnt + (tag & 1u) * kMaxSlots + s)
-                     : "memory");
       __syncwarp();  // converged before the next MMAs
     }
   }
@@ -754,19 +733,25 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     const int pos = nB + it, sl = pos % ns;
     wait(&full[sl], (pos / ns) & 1);
     const unsigned char* sb = ring + sl * p.slot_bytes;
-    wait(&hfull[it & 1], (it >> 1) & 1);
     if (pos % ngr != gi) {
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&empty[sl]);
-        tc::mbar_arrive(&hempty[it & 1]);
-      }
+      if (lane == 0) tc::mbar_arrive(&empty[sl]);
       continue;
     }
-    // h rows of the item's first slot
-    const __half* hb = reinterpret_cast<const __half*>(hs + (it & 1) * p.hs_bytes);
-    // the (slot, chunk) pairs of the item, flattened and cut over the group
     const int cnt = min(p.m, nu + 1 - p.m * it);
+    // the item's h (its slots' words are contiguous) into the group's
+    // buffer as fp16, by all of the group's warps, once this call wrote it:
+    // the group's barrier first, so no warp still reads the previous item's
+    uint32_t* hsw = reinterpret_cast<uint32_t*>(ring + p.hs_off + gi * p.hs_bytes);
+    named_bar(kBarGrp + gi, kGW * 32);
+    if (!stage_h(p.hbuf + (size_t)p.m * it * T * (I / 2), hsw, cnt * T * (I / 2), wg * 32 + lane,
+                 kGW * 32, tag, s_bad ? kShortWait : kWaitIters)) {
+      s_bad = 1;
+      set_status(p.status, QSM_DEV_TIMEOUT);
+    }
+    named_bar(kBarGrp + gi, kGW * 32);
+    const __half* hb = reinterpret_cast<const __half*>(hsw);
+    // the (slot, chunk) pairs of the item, flattened and cut over the group
     const int tot = cnt * ich, per = (tot + kGW - 1) / kGW;
     const int lo = min(tot, wg * per), hi = min(tot, lo + per);
     for (int j = lo / ich; j * ich < hi; ++j) {
@@ -807,10 +792,7 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      tc::mbar_arrive(&empty[sl]);
-      tc::mbar_arrive(&hempty[it & 1]);
-    }
+    if (lane == 0) tc::mbar_arrive(&empty[sl]);
     __syncwarp();
   }
   if (range_bad) set_status(p.status, QSM_DEV_FP16_RANGE);
@@ -863,7 +845,7 @@ int grid_of(const qsm_moe_layer* L, int nsm) {
   return std::max(gc, std::min(nsm, nt));
 }
 
-// The logit exchange and the slot counters need every CTA of the grid
+// The logit exchange and the h hand-off need every CTA of the grid
 // resident at once: G CTAs on nsm SMs holding blocks_per_sm CTAs each.
 bool grid_fits(int G, int nsm, int blocks_per_sm) {
   return G >= 1 && nsm >= 1 && blocks_per_sm >= 1 && (long long)G <= (long long)nsm * blocks_per_sm;
@@ -899,8 +881,8 @@ bool geo_of(const qsm_moe_layer* L, int T, int nsm, Geo* o) {
       off = up(off + (size_t)T * H * 2, 128);
       g.sg_off = (int)off;
       off = up(off + (L->shared_gate ? (size_t)H * 4 : 0), 128);
-      // the router rows (phase A), then the logits and the h copies share
-      // a region
+      // the router rows (phase A), then the logits and the two groups' h
+      // staging buffers share a region
       g.wr_off = g.hs_off = (int)off;
       g.hs_bytes = (int)((size_t)g.m * T * I * 2);
       const size_t wr = (size_t)epc * H * 4, lg = (size_t)T * E * 4, hsz = 2 * (size_t)g.hs_bytes;
@@ -924,20 +906,19 @@ bool geo_of(const qsm_moe_layer* L, int T, int nsm, Geo* o) {
 
 int g_barrier_skew = 0;  // qsm_debug_barrier_skew
 
-// The call ticket, the two banks of slot counters and the tagged logits
-// (each sized for the largest T, so that their place does not depend on T
-// and the logit words never share bytes with h of another call), then h.
+// The call ticket and the tagged logits (sized for the largest T, so that
+// their place does not depend on T and the logit words never share bytes
+// with h of another call), then the tagged h words.
 
 struct WsLayout {
-  size_t scnt, logits, hbuf, total;
+  size_t logits, hbuf, total;
 };
 
 WsLayout ws_layout(const qsm_moe_layer* L, int T, const Geo& g) {
   WsLayout w;
-  w.scnt = 256;
-  w.logits = w.scnt + up((size_t)2 * kMaxSlots * 4, 256);
+  w.logits = 256;
   w.hbuf = w.logits + up((size_t)kMaxT * L->E * 8, 256);
-  w.total = w.hbuf + up((size_t)(g.numax + 1) * T * L->I * 2, 256);
+  w.total = w.hbuf + up((size_t)(g.numax + 1) * T * (L->I / 2) * 8, 256);
   return w;
 }
 
@@ -1101,9 +1082,8 @@ extern "C" qsm_status moe_decode_layer(const qsm_moe_layer* L, const uint16_t* x
   prm.wm_off = g.wm_off;
   char* ws = static_cast<char*>(workspace);
   prm.gbar = reinterpret_cast<unsigned long long*>(ws);
-  prm.scnt = reinterpret_cast<unsigned*>(ws + wl.scnt);
   prm.logits = reinterpret_cast<unsigned long long*>(ws + wl.logits);
-  prm.hbuf = reinterpret_cast<__half*>(ws + wl.hbuf);
+  prm.hbuf = reinterpret_cast<unsigned long long*>(ws + wl.hbuf);
   prm.topk_idx = topk_idx;
   prm.topk_w = topk_w;
   prm.y = y;

@@ -49,14 +49,15 @@ def test_decode_layer_matches_oracle(qsm, shape, T, seed, zipf, renorm):
 
 def test_decode_layer_repeat_on_one_workspace(qsm):
     """Calls on one workspace give the same bits; each call adds one arrival
-    per CTA to the call ticket, counts I / 8 tiles for each slot it uses
-    (the shared expert and the distinct selected experts) in the counter
-    bank of its tag's parity and zeroes the other bank."""
+    per CTA to the call ticket and writes its tag (the number of calls so
+    far) into every logit word and into the h words of every slot it uses
+    (the shared expert and the distinct selected experts, all T tokens)."""
     shape = synth.QWEN
+    T = 4
     Lg, _, wr, bias = layer(shape, 0, None)
     L = qsm.Layer.from_synth(Lg)
-    x = x_for(shape, 4, 77, Lg, wr, bias).cuda()
-    ws = torch.zeros(qsm.decode_layer_workspace_bytes(L, 4), dtype=torch.uint8, device="cuda")
+    x = x_for(shape, T, 77, Lg, wr, bias).cuda()
+    ws = torch.zeros(qsm.decode_layer_workspace_bytes(L, T), dtype=torch.uint8, device="cuda")
     outs = []
     for _ in range(3):
         y, y32, idx, w = qsm.moe_decode_layer(L, x, y_f32=True, workspace=ws)
@@ -69,11 +70,14 @@ def test_decode_layer_repeat_on_one_workspace(qsm):
     tiles = (min(8 * shape.k, shape.E) + 1) * (shape.I // 8)  # of up to 8 tokens
     G = max(shape.H // 16, min(sms, tiles))
     assert int(ws[:8].view(torch.int64).item()) == 3 * G
+    # the tagged logits [8, E] after the 256-byte ticket, then h [slots, T, I / 2]
+    lw = ws[256:256 + 8 * shape.E * 8].view(torch.int64).cpu().numpy()
+    assert ((lw >> 32) == 3).all()
+    hb = 256 + (8 * shape.E * 8 + 255) // 256 * 256
     slots = 1 + len(set(idx.cpu().numpy().ravel().tolist()))
-    banks = ws[256:256 + 2 * 4 * 257].view(torch.int32).cpu().numpy().reshape(2, 257)
-    assert (banks[0] == 0).all()                  # the third call has tag 3
-    assert (banks[1, :slots] == shape.I // 8).all()
-    assert (banks[1, slots:] == 0).all()
+    n = slots * T * (shape.I // 2)
+    hw = ws[hb:hb + 8 * n].view(torch.int64).cpu().numpy()
+    assert ((hw >> 32) == 3).all()
 
 
 def test_decode_layer_workspace_shared_across_T(qsm):
