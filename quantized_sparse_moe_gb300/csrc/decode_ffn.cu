@@ -320,28 +320,31 @@ d1_gate_up_swiglu(qsm_qweights gu_w, qsm_qweights sgu_w, qsm_qweights dn_w,
 //
 // One CTA = 16 output rows n0..n0+15 of y for every token.  Work items are
 // the shared expert's blocks of 8 tokens and the block map's blocks; warp w
-// takes items w, w + warps, ...  Each warp owns one shared-memory slot:
-// the item's 16 down rows (padded), their scales and the item's h rows
-// arrive by bulk copies on the warp's mbarrier.  The weight copies of the
-// first item are issued before waiting on the gate_up launch (the routing
-// was complete before that launch let this one start, and the weights were
-// prefetched into L2 by it); only the h copies wait.  Each warp sums its
-// items into its own [T][16] fp32 slab; the slabs are added in warp order.
+// takes items w, w + warps, ...  Each warp has two shared-memory slots for
+// an item's 16 down rows (padded) and their block constants, filled by bulk
+// copies on the slot's mbarrier, so the next item's rows are in flight while
+// one is multiplied; the copies of a warp's first two items are issued
+// before waiting on the gate_up launch (the routing was complete before that
+// launch let this one start).  An item's h rows come from global memory (L2)
+// straight into registers, requested as soon as the previous item is done,
+// and each warp keeps its next item's slot, tokens and weights ahead of time
+// so those dependent lookups overlap a copy's wait.  Each warp sums its items
+// into its own [T][16] fp32 slab; the slabs are added in warp order.
+
+constexpr int kD2HCh = 8;  // 64-wide chunks of an item's h held in registers
 
 struct D2Geo {  // per-slot layout (bytes)
-  int crow, pitch, wbytes, sbytes, hpitch, hoff, slot;
+  int crow, pitch, wbytes, sbytes, slot;
 };
 
 template <int QT>
-__host__ __device__ __forceinline__ D2Geo d2_geo(int I, int hrows) {
+__host__ __device__ __forceinline__ D2Geo d2_geo(int I) {
   D2Geo g;
   g.crow = QT == QSM_Q8_0 ? I : I / 2;          // code bytes per row
   g.pitch = g.crow + kRowPad;
   g.wbytes = 16 * g.pitch;
   g.sbytes = QT == QSM_Q8_0 ? 16 * (I / 32) * 2 : 2 * 16 * (I / 64) * 2;
-  g.hpitch = 2 * I + 32;                        // bytes per staged h row
-  g.hoff = (g.wbytes + g.sbytes + 15) & ~15;
-  g.slot = (g.hoff + hrows * g.hpitch + 127) & ~127;
+  g.slot = (g.wbytes + g.sbytes + 127) & ~127;
   return g;
 }
 
@@ -353,22 +356,22 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
                 const int32_t* __restrict__ offsets,
                 const int32_t* __restrict__ tile_map,
                 const int32_t* __restrict__ n_tiles_p,
-                const float* __restrict__ topk_w, int shared_slots, int hrows,
+                const float* __restrict__ topk_w, int shared_slots,
                 const float* __restrict__ gbuf, uint16_t* __restrict__ y,
                 float* __restrict__ y32, int32_t* dev_status) {
   extern __shared__ __align__(128) unsigned char d2_smem[];
-  __shared__ __align__(8) uint64_t bars[kD2Warps];
+  __shared__ __align__(8) uint64_t bars[kD2Warps][2];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int nw = blockDim.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int n0 = 16 * blockIdx.x;
   const int nch = I / 64;
-  const D2Geo geo = d2_geo<QT>(I, hrows);
-  unsigned char* slot = d2_smem + (size_t)wid * geo.slot;
-  float* slab = reinterpret_cast<float*>(d2_smem + (size_t)nw * geo.slot);  // [nw][T][16]
-  uint64_t* bar = &bars[wid];
+  const D2Geo geo = d2_geo<QT>(I);
+  unsigned char* wslot = d2_smem + (size_t)wid * 2 * geo.slot;  // [2][slot]
+  float* slab = reinterpret_cast<float*>(d2_smem + (size_t)nw * 2 * geo.slot);  // [nw][T][16]
   if (lane == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bars[wid][0], 1);
+    mbar_init(&bars[wid][1], 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -378,84 +381,102 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
   const int items = shared_slots + n_tiles;
   for (int i = threadIdx.x; i < nw * T * 16; i += blockDim.x) slab[i] = 0.f;
 
-  auto issue_weights = [&](const Slot& sl) {
+  auto issue_weights = [&](const Slot& sl, int b) {
     const QW w = sl.e < 0 ? expert_of<QT>(sdn_w, 0) : expert_of<QT>(dn_w, sl.e);
-    if (lane == 0) mbar_expect_tx(bar, 16u * geo.crow + geo.sbytes);
+    unsigned char* slot = wslot + b * geo.slot;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[wid][b], 16u * geo.crow + geo.sbytes);
     __syncwarp();
     if (lane < 16)
-      bulk_g2s(slot + lane * geo.pitch, w.codes + (size_t)(n0 + lane) * geo.crow,
-               geo.crow, bar);
+      bulk_g2s(slot + lane * geo.pitch, w.codes + (size_t)(n0 + lane) * geo.crow, geo.crow,
+               &bars[wid][b]);
     if (lane == 16) {
       if (QT == QSM_Q8_0) {
-        bulk_g2s(slot + geo.wbytes, w.scales + (size_t)n0 * (I / 32), geo.sbytes, bar);
+        bulk_g2s(slot + geo.wbytes, w.scales + (size_t)n0 * (I / 32), geo.sbytes, &bars[wid][b]);
       } else {
-        bulk_g2s(slot + geo.wbytes, w.scales + (size_t)n0 * (I / 64), geo.sbytes / 2, bar);
+        bulk_g2s(slot + geo.wbytes, w.scales + (size_t)n0 * (I / 64), geo.sbytes / 2,
+                 &bars[wid][b]);
         bulk_g2s(slot + geo.wbytes + geo.sbytes / 2, w.biases + (size_t)n0 * (I / 64),
-                 geo.sbytes / 2, bar);
+                 geo.sbytes / 2, &bars[wid][b]);
       }
     }
   };
   auto h_row_of = [&](const Slot& sl, int c) {
     return sl.e < 0 ? T * k + sl.row0 + c : sl.row0 + c;
   };
-  auto issue_h = [&](const Slot& sl) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)sl.cnt * (2 * I));
-    __syncwarp();
-    if (lane < sl.cnt)
-      bulk_g2s(slot + geo.hoff + lane * geo.hpitch,
-               hbuf + (size_t)h_row_of(sl, lane) * I, 2 * I, bar);
+  // this thread's B operands of the item's first kD2HCh chunks (token g)
+  uint4 hx[2 * kD2HCh];
+  auto load_h = [&](const Slot& sl) {
+    const bool has = g < sl.cnt;
+    const __half* hr = hbuf + (size_t)h_row_of(sl, has ? g : 0) * I;
+#pragma unroll
+    for (int ci = 0; ci < kD2HCh; ++ci) {
+      const bool in = has && ci < nch;
+      hx[2 * ci] = in ? __ldcg(reinterpret_cast<const uint4*>(hr + 64 * ci + b_off0<QT>(q)))
+                      : make_uint4(0u, 0u, 0u, 0u);
+      hx[2 * ci + 1] = in ? __ldcg(reinterpret_cast<const uint4*>(hr + 64 * ci + b_off1<QT>(q)))
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
   };
-
-  Slot cur;
-  if (wid < items) {
-    cur = slot_of(wid, shared_slots, T, offsets, tile_map, n_tiles);
-    issue_weights(cur);
-  }
-  pdl_wait();
-  pdl_launch_dependents();
-  __syncthreads();  // slab zeroed
-
-  float* my = slab + (size_t)wid * T * 16;
-  uint32_t phase = 0;
-  bool ok_all = true;
-  for (int it = wid; it < items; it += nw) {
-    if (it != wid) {
-      cur = slot_of(it, shared_slots, T, offsets, tile_map, n_tiles);
-      issue_weights(cur);
-    }
-    issue_h(cur);
-    const bool ok = mbar_wait_bounded(bar, phase, kWaitIters);
-    phase ^= 1u;
-    if (!ok) {  // copies did not land: skip, flag, let them finish
-      ok_all = false;
-      mbar_wait_bounded(bar, phase ^ 1u, kWaitIters);
-      break;
-    }
-    // this thread's output columns 2q, 2q+1: token and routing weight
-    int tok[2];
-    float wt[2];
+  // the item's columns 2q, 2q+1: token and routing weight (the shared
+  // expert's gate is read after the wait: the gate_up launch writes it)
+  int tok[2] = {-1, -1};
+  float wt[2] = {0.f, 0.f};
+  auto columns = [&](const Slot& sl, bool gates_ready) {
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * q + cc;
       tok[cc] = -1;
       wt[cc] = 0.f;
-      if (c < cur.cnt) {
-        if (cur.e < 0) {  // shared expert: weight 1, or its gate
-          tok[cc] = cur.row0 + c;
-          wt[cc] = gbuf ? __ldcg(gbuf + tok[cc]) : 1.f;
+      if (c < sl.cnt) {
+        if (sl.e < 0) {  // shared expert: weight 1, or its gate
+          tok[cc] = sl.row0 + c;
+          wt[cc] = (gbuf && gates_ready) ? __ldcg(gbuf + tok[cc]) : 1.f;
         } else {
-          const int a = __ldcg(perm + cur.row0 + c);
+          const int a = __ldcg(perm + sl.row0 + c);
           tok[cc] = a / k;
           wt[cc] = __ldcg(topk_w + a);
         }
       }
     }
+  };
+
+  Slot cur, nxt;
+  if (wid < items) {
+    cur = slot_of(wid, shared_slots, T, offsets, tile_map, n_tiles);
+    issue_weights(cur, 0);
+    columns(cur, false);
+  }
+  if (wid + nw < items) {
+    nxt = slot_of(wid + nw, shared_slots, T, offsets, tile_map, n_tiles);
+    issue_weights(nxt, 1);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  __syncthreads();  // slab zeroed
+  if (wid < items) {
+    if (cur.e < 0 && gbuf) columns(cur, true);
+    load_h(cur);
+  }
+
+  float* my = slab + (size_t)wid * T * 16;
+  uint32_t ph[2] = {0u, 0u};
+  int b = 0;
+  bool ok_all = true;
+  for (int it = wid; it < items; it += nw) {
+    const bool ok = mbar_wait_bounded(&bars[wid][b], ph[b], kWaitIters);
+    ph[b] ^= 1u;
+    if (!ok) {  // copies did not land: skip, flag, let them (and the other slot's) finish
+      ok_all = false;
+      mbar_wait_bounded(&bars[wid][b], ph[b] ^ 1u, kWaitIters);
+      if (it + nw < items) mbar_wait_bounded(&bars[wid][b ^ 1], ph[b ^ 1], kWaitIters);
+      break;
+    }
+    const unsigned char* slot = wslot + b * geo.slot;
     const unsigned char* sc = slot + geo.wbytes;
-    const __half* hg = reinterpret_cast<const __half*>(slot + geo.hoff + min(g, hrows - 1) * geo.hpitch);
     const bool has_tok = g < cur.cnt;
+    const __half* hg = hbuf + (size_t)h_row_of(cur, has_tok ? g : 0) * I;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int ci = 0; ci < nch; ++ci) {
+    auto chunk = [&](int ci, const uint4& X0, const uint4& X1) {
       const int k0 = 64 * ci;
       RawA r;
       const unsigned char* rg = slot + g * geo.pitch;
@@ -477,12 +498,18 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
         r.sh = (uint32_t)s16[(g + 8) * (I / 64) + ci] |
                ((uint32_t)b16[(g + 8) * (I / 64) + ci] << 16);
       }
+      chunk_mma<QT>(acc, r, X0, X1);
+    };
+#pragma unroll
+    for (int ci = 0; ci < kD2HCh; ++ci)
+      if (ci < nch) chunk(ci, hx[2 * ci], hx[2 * ci + 1]);
+    for (int ci = kD2HCh; ci < nch; ++ci) {  // I > 512: the rest straight from L2
       uint4 X0 = make_uint4(0, 0, 0, 0), X1 = X0;
       if (has_tok) {
-        X0 = *reinterpret_cast<const uint4*>(hg + k0 + b_off0<QT>(q));
-        X1 = *reinterpret_cast<const uint4*>(hg + k0 + b_off1<QT>(q));
+        X0 = __ldcg(reinterpret_cast<const uint4*>(hg + 64 * ci + b_off0<QT>(q)));
+        X1 = __ldcg(reinterpret_cast<const uint4*>(hg + 64 * ci + b_off1<QT>(q)));
       }
-      chunk_mma<QT>(acc, r, X0, X1);
+      chunk(ci, X0, X1);
     }
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
@@ -492,7 +519,18 @@ d2_down_combine(qsm_qweights dn_w, qsm_qweights sdn_w,
         my[tok[cc] * 16 + g + 8] += s * acc[2 + cc];
       }
     }
-    __syncwarp();  // slot and slab free for the next item
+    consumed(acc);
+    __syncwarp();  // this slot free for the item after next
+    if (it + nw < items) {  // next: its h and lookups now, the one after into this slot
+      cur = nxt;
+      columns(cur, true);
+      load_h(cur);
+      if (it + 2 * nw < items) {
+        nxt = slot_of(it + 2 * nw, shared_slots, T, offsets, tile_map, n_tiles);
+        issue_weights(nxt, b);
+      }
+      b ^= 1;
+    }
   }
   if (!__syncthreads_and(ok_all)) {
     if (threadIdx.x == 0) set_status(dev_status, QSM_DEV_TIMEOUT);
@@ -539,12 +577,12 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
   const size_t smem1 = ((size_t)16 * (crow + kRowPad) + 16 * (H / 64 + 1) * 4 + 15) / 16 * 16 +
                        (size_t)xrows * (H + kXPad) * sizeof(__half);
   const int max_items = shared_slots + g->max_tiles;
-  const D2Geo geo = d2_geo<QT>(I, xrows);
+  const D2Geo geo = d2_geo<QT>(I);
   int w2 = max_items < kD2Warps ? max_items : kD2Warps;
   const size_t slab_bytes_per_warp = (size_t)T * 16 * sizeof(float);
   const size_t kSmemBudget = 200 * 1024;
-  while (w2 > 1 && (size_t)w2 * (geo.slot + slab_bytes_per_warp) > kSmemBudget) --w2;
-  const size_t smem2 = (size_t)w2 * (geo.slot + slab_bytes_per_warp);
+  while (w2 > 1 && (size_t)w2 * (2 * geo.slot + slab_bytes_per_warp) > kSmemBudget) --w2;
+  const size_t smem2 = (size_t)w2 * (2 * geo.slot + slab_bytes_per_warp);
   if (T > kTok && gate_up_stream_supported(L)) {
     // several slots: one persistent pass streams every touched expert's
     // gate_up rows once per slot, each slot's x rows staged once per CTA
@@ -569,7 +607,7 @@ static qsm_status decode_launch_qt(const qsm_moe_layer* L, const uint16_t* x,
                           stream, L->down, L->shared_down, (const __half*)hbuf, T,
                           H, I, k, (const int32_t*)g->perm,
                           (const int32_t*)g->offsets, (const int32_t*)g->tile_map,
-                          (const int32_t*)g->n_tiles, topk_w, shared_slots, xrows,
+                          (const int32_t*)g->n_tiles, topk_w, shared_slots,
                           L->shared_gate ? (const float*)gbuf : nullptr, y, y32,
                           dev_status));
   return QSM_OK;
