@@ -355,7 +355,7 @@ def run_ours(args, wl, rank, world):
         ffn_bytes_per_layer += ROUTER_BYTES
     hbm, _, peak_kind = peaks()
     # DRAM bytes per FFN call (ncu), or per layer launch for the one-launch path
-    traffic = measured_traffic(args.workload + ("_one_launch" if one_launch else ""))
+    traffic = measured_traffic(wl.get("name", args.workload) + ("_one_launch" if one_launch else ""))
     if args.chunk:
         # the dominant launch group is the whole chunked layer call
         ffn_ms = ms / nL
@@ -843,7 +843,7 @@ def main():
             # prefill layer is measured in the same run, same protocol
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
-            pwl = dict(WORKLOADS["prefill"])
+            pwl = dict(WORKLOADS["prefill"], name="prefill")
             pres, (psyn, pfwds, pxs) = run_ours(args, pwl, rank, world)
             if rank == 0 and not args.no_cpu_baseline:
                 psampler = OracleSampler(pwl, psyn, pxs, max_layers=1)
