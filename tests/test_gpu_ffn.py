@@ -59,6 +59,25 @@ def test_qwen_affine4_decode(qsm, T, one_launch):
     _check(qsm, synth.QWEN_A4, T, seed=1, one_launch=one_launch)
 
 
+# Past 8 tokens the decode path streams gate_up with one persistent CTA per
+# SM over (slot, 16-row tile) items: a slot of one token after full ones
+# (T = 9, 17), the small layer's shapes (H = 256: the chunk loop's generic
+# form; I = 128: 16 tiles per slot), and the largest T the decode path takes
+# when forced (128: every expert holds several slots).
+@pytest.mark.parametrize("shape,T", [(synth.QWEN, 9), (synth.QWEN_A4, 17), (synth.TINY, 9),
+                                     (synth.TINY, 64)])
+def test_decode_stream_edges(qsm, shape, T):
+    _check(qsm, shape, T, seed=2, one_launch=False)
+
+
+def test_decode_path_forced_at_128_tokens(qsm):
+    qsm.force_path("decode")
+    try:
+        _check(qsm, synth.QWEN, 128, seed=3, one_launch=False)
+    finally:
+        qsm.force_path("auto")
+
+
 @pytest.mark.parametrize("one_launch", [True, False])
 def test_full_softmax_weights(qsm, one_launch):
     _check(qsm, synth.QWEN, 5, seed=0, renorm=False, one_launch=one_launch)
