@@ -99,6 +99,9 @@ constexpr float kHScaleInv = 16.0f;
 constexpr int kBarCons = 1;               // named barrier of the consumer warps
 constexpr int kBarGrp = 2;                // + group: named barriers of the gate_up groups
 constexpr int kGW = 8;                    // warps per gate_up group
+constexpr int kGWC = 4;                   // warps per down group (ids kBarGrp + 2 + group)
+constexpr int kMaxGC = 4;                 // down groups at most
+constexpr int kMaxM = 3;                  // down tiles (slots) per C item at most
 constexpr uint32_t kShortWait = 1u << 10; // waits after a timeout
 
 struct Params {
@@ -727,13 +730,19 @@ decode_layer_kernel(const __grid_constant__ Params p) {
       __syncwarp();  // converged before the next MMAs
     }
   }
-  // ---- C: down rows n0..n0+15 of every slot, weighted per token; the
-  // group's own items, their (slot, chunk) pairs cut evenly over its warps
+  // ---- C: down rows n0..n0+15 of every slot, weighted per token.  The
+  // warps form smaller groups of kGWC here, so that several items (a few
+  // slots each) are worked on at once, each as soon as its slots' h is
+  // there; a group's own items, their (slot, chunk) pairs cut evenly over
+  // its warps
+  constexpr int ngc = kCW / kGWC;
+  static_assert(ngc <= kMaxGC && kBarGrp + ngr + ngc <= 16, "down groups");
+  const int gc = warp / kGWC, wc = warp % kGWC;
   for (int it = 0; it < items; ++it) {
     const int pos = nB + it, sl = pos % ns;
     wait(&full[sl], (pos / ns) & 1);
     const unsigned char* sb = ring + sl * p.slot_bytes;
-    if (pos % ngr != gi) {
+    if (it % ngc != gc) {
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&empty[sl]);
       continue;
@@ -742,18 +751,18 @@ decode_layer_kernel(const __grid_constant__ Params p) {
     // the item's h (its slots' words are contiguous) into the group's
     // buffer as fp16, by all of the group's warps, once this call wrote it:
     // the group's barrier first, so no warp still reads the previous item's
-    uint32_t* hsw = reinterpret_cast<uint32_t*>(ring + p.hs_off + gi * p.hs_bytes);
-    named_bar(kBarGrp + gi, kGW * 32);
-    if (!stage_h(p.hbuf + (size_t)p.m * it * T * (I / 2), hsw, cnt * T * (I / 2), wg * 32 + lane,
-                 kGW * 32, tag, s_bad ? kShortWait : kWaitIters)) {
+    uint32_t* hsw = reinterpret_cast<uint32_t*>(ring + p.hs_off + gc * p.hs_bytes);
+    named_bar(kBarGrp + ngr + gc, kGWC * 32);
+    if (!stage_h(p.hbuf + (size_t)p.m * it * T * (I / 2), hsw, cnt * T * (I / 2), wc * 32 + lane,
+                 kGWC * 32, tag, s_bad ? kShortWait : kWaitIters)) {
       s_bad = 1;
       set_status(p.status, QSM_DEV_TIMEOUT);
     }
-    named_bar(kBarGrp + gi, kGW * 32);
+    named_bar(kBarGrp + ngr + gc, kGWC * 32);
     const __half* hb = reinterpret_cast<const __half*>(hsw);
     // the (slot, chunk) pairs of the item, flattened and cut over the group
-    const int tot = cnt * ich, per = (tot + kGW - 1) / kGW;
-    const int lo = min(tot, wg * per), hi = min(tot, lo + per);
+    const int tot = cnt * ich, per = (tot + kGWC - 1) / kGWC;
+    const int lo = min(tot, wc * per), hi = min(tot, lo + per);
     for (int j = lo / ich; j * ich < hi; ++j) {
       const int s = p.m * it + j;
       const int c0 = max(lo, j * ich) - j * ich, c1 = min(hi, (j + 1) * ich) - j * ich;
@@ -872,7 +881,7 @@ bool geo_of(const qsm_moe_layer* L, int T, int nsm, Geo* o) {
   g.numax = T * k < E ? T * k : E;
   const int G = grid_of(L, nsm), epc = (E + G - 1) / G;
   // the deepest ring (then the largest C items) that fits
-  const int mmax = (int)(g.slot_bytes / dtile) > 8 ? 8 : (int)(g.slot_bytes / dtile);
+  const int mmax = std::min(kMaxM, (int)(g.slot_bytes / dtile));
   bool fit = false;
   for (g.ns = kMaxS; g.ns >= 2 && !fit; --g.ns) {
     for (g.m = mmax; g.m >= 1; --g.m) {
@@ -885,7 +894,8 @@ bool geo_of(const qsm_moe_layer* L, int T, int nsm, Geo* o) {
       // staging buffers share a region
       g.wr_off = g.hs_off = (int)off;
       g.hs_bytes = (int)((size_t)g.m * T * I * 2);
-      const size_t wr = (size_t)epc * H * 4, lg = (size_t)T * E * 4, hsz = 2 * (size_t)g.hs_bytes;
+      const size_t wr = (size_t)epc * H * 4, lg = (size_t)T * E * 4,
+                   hsz = kMaxGC * (size_t)g.hs_bytes;
       off = up(off + std::max(wr, std::max(lg, hsz)), 128);
       g.ul_off = (int)off;
       off = up(off + (size_t)g.numax * 4, 16);
