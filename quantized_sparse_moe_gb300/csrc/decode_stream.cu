@@ -12,12 +12,12 @@
 //
 // One CTA per SM takes a contiguous run of the items in slot order.  Its
 // producer thread streams the tiles through a ring of TMA stages (3D row
-// view of the codes, 128-byte swizzle, 8 rows per copy, with the rows'
-// block constants by bulk copies) and copies the x rows of each new slot
-// into one of two buffers, which the consumers convert to fp16 in place: an
-// expert's tokens are staged once per CTA rather than once per 16 weight
-// rows.  Two groups of eight consumer warps
-// take alternate items; the warps of a group split the tile's 64-wide K
+// view of the codes, 128-byte swizzle, 8 rows per copy; the rows' block
+// constants as 8-row boxes with the swizzle of their row width) and copies
+// the x rows of each new slot into one of two buffers, which the consumers
+// convert to fp16 in place: an expert's tokens are staged once per CTA
+// rather than once per 16 weight rows.  Four groups of four consumer warps
+// take the items in turn; the warps of a group split the tile's 64-wide K
 // chunks, add their partials in warp order and the group's first warp
 // applies SwiGLU and stores h.  A stage is waited for and released by the
 // warps of the group that owns its position only.
