@@ -46,8 +46,10 @@
 // expert's first tile and its down rows are requested before the wait; x
 // is loaded by the consumer threads themselves (through L2: the previous
 // launch wrote it), which is quicker than a bulk copy's round trip.
-// The consumer warps form two groups that take alternate ring positions,
-// so two tiles (or items) are in flight at once.
+// For the gate_up tiles the consumer warps form two groups that take
+// alternate ring positions, so two tiles are in flight at once; for the
+// down items they form four smaller groups, so that the items of a layer
+// run at once, each as soon as its slots' h is there.
 //
 // The grid has one CTA per SM (fewer when the layer has fewer gate_up
 // tiles): CTAs c < H / 16 also own rows of y, the others only gate_up tiles,
@@ -651,13 +653,13 @@ decode_layer_kernel(const __grid_constant__ Params p) {
   bool range_bad = false;
   float yp[4] = {0.f, 0.f, 0.f, 0.f};
   // ---- B: gate_up + SwiGLU tiles.  The warps form groups of kGW; group gi
-  // owns the ring positions p with p % ngr == gi (gate_up tiles, then C
-  // items), so ngr of them are in flight at once.  A tile's kGW warps take
-  // nch / kGW chunks each and reduce behind the group's own named barrier.
-  // Every warp still waits for every position (and every h copy) in order
-  // and arrives on its empty barrier, the others right away: a ring slot's
-  // next phase then waits for all warps, and no warp waits on a phase two
-  // ahead of the barrier's (a parity wait would take that one as done).
+  // owns the gate_up ring positions p with p % ngr == gi, so ngr of them
+  // are in flight at once.  A tile's kGW warps take nch / kGW chunks each
+  // and reduce behind the group's own named barrier.  Every warp still waits
+  // for every position in order (gate_up tiles, then the down items) and
+  // arrives on its empty barrier, the others right away: a ring slot's next
+  // phase then waits for all warps, and no warp waits on a phase two ahead
+  // of the barrier's (a parity wait would take that one as done).
   constexpr int ngr = kCW / kGW;
   const int gi = warp / kGW, wg = warp % kGW;
   for (int j = 0; j < nB; ++j) {
