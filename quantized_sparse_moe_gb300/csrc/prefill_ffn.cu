@@ -24,8 +24,8 @@
 //             16-byte pieces per sorted row
 //   down      per work item (same token block, 256 output rows):
 //             D (128 token rows x 256) = h rows x W_down tiles^T; epilogue
-//             y_acc[token] += routing weight * D row (16-byte fp32
-//             reduce-adds, one token per thread)
+//             y_acc[token] += routing weight * D row (8-byte fp32
+//             reduce-adds, four threads on 32 contiguous bytes of a row)
 // Rows of a short tile beyond its tokens hold stale data: their D rows are
 // never read.
 //   finalize  y = bf16(y_acc) (and the fp32 copy)
@@ -157,12 +157,22 @@ __device__ __forceinline__ int weight_row0(const Params& p, int mode, int sub, i
   return mode == kGateUp ? a * p.I + sub * BM : (2 * sub + a) * BM;
 }
 
-// y[0..3] += v0..v3 in one 16-byte reduction (16-byte aligned address).
-__device__ __forceinline__ void red_add_v4(float* y, float v0, float v1, float v2,
-                                           float v3) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(y), "f"(v0),
-               "f"(v1), "f"(v2), "f"(v3)
-               : "memory");
+// y[0..1] += v0, v1 in one 8-byte reduction (8-byte aligned address).
+__device__ __forceinline__ void red_add_v2(float* y, float v0, float v1) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(y), "f"(v0), "f"(v1) : "memory");
+}
+
+// 16 lanes from the lane in taddr, 32 columns: thread t gets, for j = 0..3,
+// columns 8j + 2(t % 4) and + 1 of lane t / 4 (registers 4j, 4j + 1) and of
+// lane t / 4 + 8 (registers 4j + 2, 4j + 3).
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 // One 32-bit word of affine-4 codes (K order k..k+7, lowest nibble first)
@@ -497,7 +507,6 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
           tc::tmem_ld16(taddr + BM + c0, uv);
           if (live) {
             uint32_t hw[8];
-#pragma unroll
             if (p.gu_dump) {  // test hook: the fused projection's values per h row
               float* dr = p.gu_dump + (size_t)srow * 2 * p.I + sub * BM + c0;
 #pragma unroll
@@ -506,6 +515,7 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
                 dr[p.I + c] = uv[c];
               }
             }
+#pragma unroll
             for (int c = 0; c < 16; c += 2) {
               const float h0 = silu(gv[c]) * uv[c] * kHScale;
               const float h1 = silu(gv[c + 1]) * uv[c + 1] * kHScale;
@@ -519,16 +529,40 @@ moe_prefill_gemm(const __grid_constant__ Params p) {
           }
         }
       } else {
-        // 16 consecutive output rows per load: four 16-byte reduce-adds
-        float* dst = p.yacc + (size_t)tok * p.H + sub * (NA * BM);
-        for (int c0 = 0; c0 < NA * BM; c0 += 16) {
-          float dv[16];
-          tc::tmem_ld16(taddr + c0, dv);
-          if (live) {
+        // The accumulator read in 16-lane halves with the 16x256b shape:
+        // four consecutive threads hold 8 consecutive output rows of one
+        // token, so a warp's reduce-add covers 32 contiguous bytes of each
+        // of 8 tokens (half the L2 transactions of 16 bytes of 32 tokens).
+        // Thread t handles warp rows t / 4 + 8 i (i = 0..3): their tokens and
+        // weights come from the rows' own threads.
+        const int rq = lane >> 2, cq = 2 * (lane & 3);
+        float* rdst[4];
+        float rwt[4];
+        bool rlive[4];
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              red_add_v4(dst + c0 + 4 * v, wt * dv[4 * v], wt * dv[4 * v + 1],
-                         wt * dv[4 * v + 2], wt * dv[4 * v + 3]);
+        for (int i = 0; i < 4; ++i) {
+          const int src = rq + 8 * i;
+          const int t2 = __shfl_sync(0xffffffffu, tok, src);
+          rwt[i] = __shfl_sync(0xffffffffu, wt, src);
+          rlive[i] = 32 * q4 + src < ti.cnt;
+          rdst[i] = p.yacc + (size_t)t2 * p.H + sub * (NA * BM) + cq;
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          for (int c0 = 0; c0 < NA * BM; c0 += 32) {
+            uint32_t r[16];
+            tmem_ld_16x256b_x4(taddr + ((uint32_t)(16 * hh) << 16) + c0, r);
+            tc::tmem_wait_ld(r);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int i0 = 2 * hh, i1 = 2 * hh + 1;
+              if (rlive[i0])
+                red_add_v2(rdst[i0] + c0 + 8 * jj, rwt[i0] * __uint_as_float(r[4 * jj]),
+                           rwt[i0] * __uint_as_float(r[4 * jj + 1]));
+              if (rlive[i1])
+                red_add_v2(rdst[i1] + c0 + 8 * jj, rwt[i1] * __uint_as_float(r[4 * jj + 2]),
+                           rwt[i1] * __uint_as_float(r[4 * jj + 3]));
+            }
           }
         }
       }
