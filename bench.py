@@ -96,6 +96,23 @@ def measured_traffic(workload):
     return ent["bytes_per_launch"] if m.hexdigest() == ent["sources_sha256"] else None
 
 
+def rank_max(x, dev, world):
+    """The largest of x over all ranks (x itself for one rank): every rank's
+    timed region is bracketed by the same barriers, so the job takes as long
+    as its slowest rank."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+def job_value(world, units_per_rank, ms):
+    """Whole-job throughput: the units all ranks processed per second of the
+    slowest rank's time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -306,12 +323,8 @@ def run_ours(args, wl, rank, world):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
-    value = world * T * nL / (ms / 1e3)
+    ms = rank_max(ev0.elapsed_time(ev1) / args.steps, dev, world)
+    value = job_value(world, T * nL, ms)
     replays = replay_stats(graph, stream, fwds, args.replays)
 
     # dominant launch pair: the expert FFN (gate_up+SwiGLU, down+combine),
@@ -389,11 +402,7 @@ def run_ours(args, wl, rank, world):
         t1 = time.perf_counter()
         if rep >= args.warmup:
             e_ms.append((t1 - t0) * 1e3)
-    e2e_ms = statistics.median(e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = rank_max(statistics.median(e_ms), dev, world)
 
     achieved = ffn_bytes_per_layer / (ffn_ms / 1e3) / 1e9
     # algorithmic FLOPs per layer: expert matmuls (k routed + shared per
@@ -454,12 +463,12 @@ def run_ours(args, wl, rank, world):
             "frac": (flops_layer - 2.0 * T * sh.E * sh.H) / (ffn_ms / 1e3) / 1e12 / tc_peak,
             "traffic": traffic, "flops_per_launch": flops_layer - 2.0 * T * sh.E * sh.H,
             "launch_ms": ffn_ms, "peak_kind": peak_kind}),
-        "e2e": {"value": world * T * nL / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_value(world, T * nL, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": xh.numel() * 2,
                 "d2h_bytes_per_step": yh.numel() * 2, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
-        "replays": dict(replays, tokens_per_s_at_median=world * T * nL / (replays["median_ms"] / 1e3)),
+        "replays": dict(replays, tokens_per_s_at_median=job_value(world, T * nL, replays["median_ms"])),
     }
     return result, (syn, fwds, xs)
 
@@ -660,11 +669,7 @@ def run_gemv(args, wl, rank, world):
             graph.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / (replays * R)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = t.item()
+    ms = rank_max(ev0.elapsed_time(ev1) / (replays * R), dev, world)
     # per shape: a graph of its R rotations, timed alone
     per_shape = {}
     for name, (n, k) in shapes:
@@ -709,10 +714,10 @@ def run_gemv(args, wl, rank, world):
         stream.synchronize()
         if r >= args.warmup:
             e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e_ms = statistics.median(e_ms)
+    e2e_ms = rank_max(statistics.median(e_ms), dev, world)
     result = {
         "metric": gemv_metric(wl),
-        "value": world * step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "value": job_value(world, step_bytes, ms) / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("int8 activation codes x int8 weight codes, s32 block sums, f32 scales"
@@ -731,7 +736,7 @@ def run_gemv(args, wl, rank, world):
                      "bytes_per_launch": per_shape[top]["N"] * per_shape[top]["K"] * 34 // 32,
                      "launch_ms": per_shape[top]["us"] / 1e3, "peak_kind": peak_kind},
         "step_roofline": {"bytes_per_step": step_bytes, "frac": step_bytes / (ms * 1e-3) / 1e9 / hbm},
-        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_value(world, step_bytes, e2e_ms) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": sum(2 * k for _, (_, k) in shapes),
                 "d2h_bytes_per_step": sum(2 * n for _, (n, _) in shapes), "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_replay * replays,
